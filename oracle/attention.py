@@ -1,0 +1,211 @@
+"""fp64 oracle: paged gather, decode attention (GQA and absorbed MLA), LSE merge,
+and the KV append. TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Conventions (readings of points the pages leave open; each is also listed in
+the design notes):
+
+* Pool layout is ``[num_pages, page_size, H_kv, D]`` ("NHD"): row ``r`` of
+  physical page ``p`` holds token ``page_slot * page_size + r`` of whatever
+  sequence owns the page. The MLA latent pool is ``[num_pages, page_size, 576]``.
+* Query head ``h`` reads kv head ``h // g`` with ``g = H_q // H_kv``.
+* ``LSE`` is the natural-log log-sum-exp of the scaled scores.
+* An empty context (length 0) gives ``O = 0`` and ``LSE = -inf``.
+
+No blocking, fusion or reordering beyond the definition: gather the rows,
+score them, softmax, weight the values.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def gather_sequence(pool: np.ndarray, block_table_row: np.ndarray, length: int,
+                    page_size: int) -> np.ndarray:
+    """Rows ``0 .. length-1`` of one sequence, gathered through its block table.
+
+    SwiftLLM page, section 3.1: a request's cache is a list of non-contiguous
+    fixed-size blocks found through its block table; token ``t`` lives in block
+    ``block_table[t // page_size]`` at row ``t % page_size``.
+
+    Pinned by: brute-force unpaged attention (the test scatters contiguous K/V
+    into shuffled pages itself) and page-permutation invariance.
+    """
+    length = int(length)
+    if length == 0:
+        return np.zeros((0,) + pool.shape[2:], dtype=pool.dtype)
+    n_pages = (length + page_size - 1) // page_size
+    pages = np.asarray(block_table_row[:n_pages], dtype=np.int64)
+    rows = pool[pages]  # [n_pages, page_size, ...]
+    rows = rows.reshape((n_pages * page_size,) + pool.shape[2:])
+    return rows[:length]
+
+
+def _softmax_attend(scores: np.ndarray, values: np.ndarray):
+    """softmax over the last axis of ``scores`` [n, L], then weight ``values`` [L, Dv].
+
+    Returns (O [n, Dv], LSE [n]) in float64.
+    """
+    m = scores.max(axis=-1, keepdims=True)
+    e = np.exp(scores - m)
+    s = e.sum(axis=-1, keepdims=True)
+    out = (e @ values) / s
+    lse = (m + np.log(s))[:, 0]
+    return out, lse
+
+
+def decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale):
+    """One decode step of GQA attention over a paged KV cache, in float64.
+
+    For every sequence ``b`` and query head ``h`` (kv head ``kh = h // g``):
+    ``s_t = scale * <q[b,h], K_b[t,kh]>`` for ``t < L_b``, ``p = softmax(s)``,
+    ``O[b,h] = sum_t p_t V_b[t,kh]`` and ``LSE[b,h] = log sum_t exp(s_t)``.
+
+    SwiftLLM page, sections 3.1 and 5.1 (query, block tables and context
+    lengths are the attention inputs); the GQA sharing of one kv head by
+    ``g`` consecutive query heads is the reading stated in the module docstring.
+
+    Args:
+        q: [B, H_q, D] float array.
+        k_pool, v_pool: [P, page_size, H_kv, D] float arrays.
+        block_table: [B, >= max pages] integer array of physical page ids.
+        seq_lens: [B] context lengths (tokens attended).
+        scale: softmax scale.
+
+    Returns:
+        (O [B, H_q, D] float64, LSE [B, H_q] float64).
+
+    Pinned by: torch's fp64 scaled_dot_product_attention on the unpaged K/V,
+    scipy's logsumexp, page-permutation invariance, identical keys (O = mean V),
+    one-token context (O = V exactly) and the two-token sigmoid closed form.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, H_q, D = q.shape
+    page_size, H_kv = k_pool.shape[1], k_pool.shape[2]
+    if H_q % H_kv != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
+    g = H_q // H_kv
+    Dv = v_pool.shape[3]
+    out = np.zeros((B, H_q, Dv), dtype=np.float64)
+    lse = np.full((B, H_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        K = gather_sequence(k_pool, block_table[b], L, page_size).astype(np.float64)
+        V = gather_sequence(v_pool, block_table[b], L, page_size).astype(np.float64)
+        for kh in range(H_kv):
+            heads = slice(kh * g, (kh + 1) * g)
+            scores = scale * (q[b, heads] @ K[:, kh, :].T)  # [g, L]
+            o, l = _softmax_attend(scores, V[:, kh, :])
+            out[b, heads] = o
+            lse[b, heads] = l
+    return out, lse
+
+
+def mla_decode_attention(q, kv_pool, block_table, seq_lens, scale, d_v):
+    """Absorbed-MLA decode: every query head attends one shared latent head.
+
+    ``s[h,t] = scale * <q[b,h,0:Dqk], C_b[t,0:Dqk]>``, softmax over ``t``,
+    ``O[b,h] = sum_t p[h,t] C_b[t,0:d_v]`` (the values are the first ``d_v``
+    columns of the same latent rows).
+
+    TokenSpeed deep dive (wth2jhl.online), section 7, fig. 3: MLA decode with a
+    512-wide output per head row; the 576 = 512 latent + 64 rope row width and
+    ``V = C[:, :512]`` are the workload's statement of the absorbed form.
+
+    Args:
+        q: [B, H, Dqk]; kv_pool: [P, page_size, Dqk]; d_v <= Dqk.
+
+    Returns:
+        (O [B, H, d_v] float64, LSE [B, H] float64).
+
+    Pinned by: torch's fp64 scaled_dot_product_attention with one kv head and a
+    value width different from the key width, and the one-token closed form.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, H, Dqk = q.shape
+    page_size = kv_pool.shape[1]
+    out = np.zeros((B, H, d_v), dtype=np.float64)
+    lse = np.full((B, H), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        C = gather_sequence(kv_pool, block_table[b], L, page_size).astype(np.float64)
+        scores = scale * (q[b] @ C.T)  # [H, L]
+        o, l = _softmax_attend(scores, C[:, :d_v])
+        out[b] = o
+        lse[b] = l
+    return out, lse
+
+
+def merge_states(o_a, lse_a, o_b, lse_b):
+    """Merge two attention states over disjoint key sets by their log-sum-exp.
+
+    With ``m = max(lse_a, lse_b)``, ``w_a = exp(lse_a - m)``, ``w_b = exp(lse_b - m)``:
+    ``O = (w_a O_a + w_b O_b) / (w_a + w_b)`` and ``LSE = m + log(w_a + w_b)``.
+    A state with ``LSE = -inf`` (no keys) has weight 0; two empty states merge
+    to ``O = 0``, ``LSE = -inf``.
+
+    TokenSpeed deep dive, section 7 fig. 3 (stage 3 reduces the split partials
+    by their LSE) and section 7.1; Tokasaurus blog, "Dynamic prefix
+    identification and exploration" (shared-prefix attention is combined with
+    the per-sequence part).
+
+    Args: o_* [..., D]; lse_* [...] (natural log).
+    Returns: (O [..., D] float64, LSE [...] float64).
+
+    Pinned by: prefix-state merged with suffix-state equals flat attention over
+    prefix ++ suffix (an independent oracle call), and N-way associativity.
+    """
+    o_a = np.asarray(o_a, dtype=np.float64)
+    o_b = np.asarray(o_b, dtype=np.float64)
+    lse_a = np.asarray(lse_a, dtype=np.float64)
+    lse_b = np.asarray(lse_b, dtype=np.float64)
+    m = np.maximum(lse_a, lse_b)
+    empty = np.isneginf(m)
+    m_safe = np.where(empty, 0.0, m)
+    w_a = np.where(np.isneginf(lse_a), 0.0, np.exp(lse_a - m_safe))
+    w_b = np.where(np.isneginf(lse_b), 0.0, np.exp(lse_b - m_safe))
+    w = w_a + w_b
+    w_div = np.where(empty, 1.0, w)
+    o = (w_a[..., None] * o_a + w_b[..., None] * o_b) / w_div[..., None]
+    o = np.where(empty[..., None], 0.0, o)
+    lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, w)))
+    return o, lse
+
+
+def merge_states_many(os, lses):
+    """Left fold of :func:`merge_states` over a list of states (split-KV reduce)."""
+    o, lse = os[0], lses[0]
+    for o_n, lse_n in zip(os[1:], lses[1:]):
+        o, lse = merge_states(o, lse, o_n, lse_n)
+    return np.asarray(o, dtype=np.float64), np.asarray(lse, dtype=np.float64)
+
+
+def kv_append(k_pool, v_pool, k_new, v_new, block_table, positions, page_size):
+    """Write one new token's K/V per sequence into its page; return new pools.
+
+    SwiftLLM page, section 3.1: blocks are handed to a request on demand, so the
+    token at position ``pos`` goes to page ``block_table[b][pos // page_size]``,
+    row ``pos % page_size``. Works on raw element arrays of any dtype (bf16 is
+    carried as uint16 bit patterns), so the copy is exact; the inputs are not
+    modified.
+
+    Args:
+        k_pool, v_pool: [P, page_size, H_kv, D]; k_new, v_new: [B, H_kv, D];
+        positions: [B] token index to write (= context length before append).
+
+    Pinned by: an element-wise loop in the tests that writes the expected pool
+    cell by cell, and the check that every other byte is unchanged.
+    """
+    k_out = np.array(k_pool, copy=True)
+    v_out = np.array(v_pool, copy=True)
+    for b in range(len(positions)):
+        pos = int(positions[b])
+        page = int(block_table[b][pos // page_size])
+        row = pos % page_size
+        k_out[page, row] = k_new[b]
+        v_out[page, row] = v_new[b]
+    return k_out, v_out

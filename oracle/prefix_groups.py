@@ -1,0 +1,120 @@
+"""Invariant checker for shared-prefix groups. TEST INFRASTRUCTURE ONLY.
+
+Tokasaurus blog (Stanford), "Dynamic prefix identification and exploration":
+before every forward pass a greedy depth-first search iteratively finds the
+longest possible shared prefixes, so that attention over each shared prefix
+can be computed once for the whole group (Hydragen / cascade attention).
+
+The pages fix no tie-break, depth or data format, so several groupings can be
+valid. This module therefore does not re-implement the search; it checks the
+properties any output of the reading below must have (several correct results:
+compare what is unique, check the rest is valid):
+
+* prefixes are whole pages, shared *by physical page id* in the block table;
+* every member keeps at least one suffix token (``n_pages * page_size <= L - 1``);
+* each sequence is in at most one group, and every group has at least
+  ``min_group`` members;
+* a group's prefix is maximal: its members do not all share the next page too;
+* greedy longest-first: a sequence that starts with a group's whole prefix
+  (and may share that many pages) is in that group or in a deeper one;
+* nothing is missed: among ungrouped sequences that could share a page, no
+  ``min_group`` of them start with the same page id.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List
+
+import numpy as np
+
+
+@dataclass
+class PrefixGroups:
+    """Single-level prefix groups in CSR form (host copy).
+
+    prefix_indptr[G+1] / prefix_pages: each group's shared physical page ids.
+    prefix_len[G]: shared tokens (= pages * page_size).
+    member_indptr[G+1] / member_ids: the sequences of each group.
+    """
+
+    prefix_indptr: np.ndarray
+    prefix_pages: np.ndarray
+    prefix_len: np.ndarray
+    member_indptr: np.ndarray
+    member_ids: np.ndarray
+    num_groups: int = field(default=0)
+
+    def groups(self):
+        for gi in range(self.num_groups):
+            pages = self.prefix_pages[self.prefix_indptr[gi]:self.prefix_indptr[gi + 1]]
+            members = self.member_ids[self.member_indptr[gi]:self.member_indptr[gi + 1]]
+            yield gi, pages, int(self.prefix_len[gi]), members
+
+
+def shareable_pages(seq_len: int, page_size: int) -> int:
+    """Whole pages a sequence may share while keeping >= 1 suffix token."""
+    return max(0, (int(seq_len) - 1) // page_size)
+
+
+def check_prefix_groups(block_table, seq_lens, page_size: int, min_group: int,
+                        groups: PrefixGroups) -> List[str]:
+    """Return a list of violated invariants (empty when ``groups`` is valid)."""
+    bt = np.asarray(block_table)
+    lens = np.asarray(seq_lens)
+    B = len(lens)
+    errors: List[str] = []
+    owner = np.full(B, -1, dtype=np.int64)
+    for gi, pages, plen, members in groups.groups():
+        n = len(pages)
+        if n < 1:
+            errors.append(f"group {gi}: empty prefix")
+            continue
+        if plen != n * page_size:
+            errors.append(f"group {gi}: prefix_len {plen} != {n} pages * {page_size}")
+        if len(members) < min_group:
+            errors.append(f"group {gi}: {len(members)} members < min_group {min_group}")
+        for b in members:
+            b = int(b)
+            if not 0 <= b < B:
+                errors.append(f"group {gi}: member {b} out of range")
+                continue
+            if owner[b] >= 0:
+                errors.append(f"sequence {b} in groups {owner[b]} and {gi}")
+            owner[b] = gi
+            if n > shareable_pages(lens[b], page_size):
+                errors.append(f"group {gi}: member {b} (L={lens[b]}) keeps no suffix token")
+                continue
+            if not np.array_equal(bt[b, :n], pages):
+                errors.append(f"group {gi}: member {b} does not start with the group prefix")
+        # maximality: not every member shares page n as well
+        valid = [int(b) for b in members if 0 <= int(b) < B]
+        if valid and all(shareable_pages(lens[b], page_size) > n for b in valid):
+            nxt = {int(bt[b, n]) for b in valid}
+            if len(nxt) == 1:
+                errors.append(f"group {gi}: prefix not maximal (all members share page {n})")
+    # greedy longest-first: whoever starts with a group's whole prefix belongs
+    # to it or to a deeper group
+    depth = np.zeros(B, dtype=np.int64)
+    for gi, pages, plen, members in groups.groups():
+        for b in members:
+            if 0 <= int(b) < B:
+                depth[int(b)] = len(pages)
+    caps = np.maximum(0, (lens.astype(np.int64) - 1) // page_size)
+    for gi, pages, plen, members in groups.groups():
+        n = len(pages)
+        if n < 1 or n > bt.shape[1]:
+            continue
+        starts = np.all(bt[:, :n] == np.asarray(pages)[None, :], axis=1) & (caps >= n)
+        bad = np.nonzero(starts & (owner != gi) & (depth <= n))[0]
+        for b in bad[:5]:
+            errors.append(f"sequence {b} starts with group {gi}'s prefix but is not in it or deeper")
+    # completeness: ungrouped sequences with a shareable first page
+    first_counts = {}
+    for b in range(B):
+        if owner[b] < 0 and shareable_pages(lens[b], page_size) >= 1:
+            first_counts.setdefault(int(bt[b, 0]), []).append(b)
+    for page, seqs in first_counts.items():
+        if len(seqs) >= min_group:
+            errors.append(f"{len(seqs)} ungrouped sequences share first page {page}")
+    return errors

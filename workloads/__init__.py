@@ -1,0 +1,315 @@
+"""Seeded synthetic inputs for decode attention over a paged KV cache.
+
+This module is shared by the tests, the benchmark and the smoke check. It holds
+none of the attention arithmetic: only shapes, lengths, page placement and
+random values. Both the CUDA library and the CPU oracle read the inputs it
+builds; neither reads the other's outputs.
+
+Recipe (all seeded):
+* structure (lengths, page permutation, block tables) comes from
+  ``numpy.random.default_rng(seed)`` on the host;
+* values (q, K, V, new-token K/V) are N(0, 1) drawn by a ``torch.Generator``
+  seeded with ``seed`` on the device the case lives on; bf16 values are the
+  float32 draws rounded to nearest-even by torch;
+* every pool row no sequence owns is a NaN sentinel: unused pages, the rows
+  past each sequence's length in its last page, and the row a pending append
+  will fill. Block-table entries past a sequence's pages point at an unused
+  (all-NaN) page, so a masked-read bug shows as NaN instead of a stray access.
+
+Layouts: pools are ``[P, page_size, H_kv, D]`` (MLA: ``[P, page_size, Dqk]``),
+block tables ``int32 [B, bt_stride]`` row-major, lengths ``int32 [B]``.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass
+class PagedCase:
+    """One decode-step workload over a paged cache (GQA or MLA)."""
+
+    name: str
+    seed: int
+    B: int
+    H_q: int
+    H_kv: int           # 1 for MLA
+    D: int              # key width (Dqk for MLA)
+    Dv: int             # value width (= D for GQA, 512 for MLA)
+    page_size: int
+    num_pages: int
+    dtype: str          # "f32" | "bf16"
+    scale: float
+    mla: bool
+    append: bool
+    seq_lens: np.ndarray        # int32 [B]: cached tokens before this step's append
+    block_table: np.ndarray     # int32 [B, bt_stride]
+    sentinel_page: int          # an all-NaN page (or 0 if the pool has none spare)
+    q: torch.Tensor = None
+    k_pool: torch.Tensor = None  # MLA: the latent pool
+    v_pool: Optional[torch.Tensor] = None
+    k_new: Optional[torch.Tensor] = None
+    v_new: Optional[torch.Tensor] = None
+    groups_truth: Optional[List[np.ndarray]] = None  # cascade: members per constructed group
+    prefix_pages_truth: int = 0
+    meta: Dict = field(default_factory=dict)
+
+    @property
+    def attn_lens(self) -> np.ndarray:
+        """Tokens attended by the step (one more than cached when appending)."""
+        return (self.seq_lens + (1 if self.append else 0)).astype(np.int32)
+
+    @property
+    def bt_stride(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def positions(self) -> np.ndarray:
+        """Append positions (= cached length before the append)."""
+        return self.seq_lens.astype(np.int32)
+
+    def kv_bytes_read(self) -> int:
+        """Algorithmic K/V (or latent) bytes one attention pass must read."""
+        esize = 4 if self.dtype == "f32" else 2
+        tokens = int(self.attn_lens.astype(np.int64).sum())
+        if self.mla:
+            return tokens * self.D * esize
+        return kv_cache_bytes(tokens, self.H_kv, self.D, self.Dv, esize)
+
+
+def kv_cache_bytes(tokens: int, H_kv: int, D: int, Dv: int, elem_bytes: int) -> int:
+    """Bytes of uncompressed K plus V rows for ``tokens`` tokens of one layer.
+
+    Same count as the approximate KV-size formula of the tokenspeed deep dive
+    (fiv.co.kr), section 7-2 (there multiplied by the layer count).
+    """
+    return int(tokens) * int(H_kv) * (int(D) + int(Dv)) * int(elem_bytes)
+
+
+def _pages_for(n_tokens: np.ndarray, page_size: int) -> np.ndarray:
+    return (n_tokens.astype(np.int64) + page_size - 1) // page_size
+
+
+def _randn(shape, generator, device, dtype: str, chunk_elems: int = 1 << 28) -> torch.Tensor:
+    """N(0,1) draws in float32 rounded to ``dtype``, generated in chunks."""
+    numel = int(np.prod(shape))
+    out = torch.empty(numel, dtype=_TORCH_DTYPE[dtype], device=device)
+    for start in range(0, numel, chunk_elems):
+        n = min(chunk_elems, numel - start)
+        out[start:start + n] = torch.randn(n, generator=generator, device=device,
+                                           dtype=torch.float32).to(out.dtype)
+    return out.view(*shape)
+
+
+def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
+               page_size: int, seq_lens: Sequence[int], dtype: str, scale: float,
+               append: bool = False, mla: bool = False, Dv: Optional[int] = None,
+               pool_factor: float = 1.25, shared_groups: Optional[List[np.ndarray]] = None,
+               shared_pages: int = 0, device="cpu", rng: Optional[np.random.Generator] = None,
+               extra_pages: int = 1, num_pages: Optional[int] = None) -> PagedCase:
+    """Build a case: lengths -> page need -> shuffled pool -> block tables -> values.
+
+    ``shared_groups``: lists of sequence ids; each list shares its first
+    ``shared_pages`` pages by physical id (the cascade workload).
+    """
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    lens = np.asarray(seq_lens, dtype=np.int32)
+    assert len(lens) == B
+    attn = lens + (1 if append else 0)
+    n_alloc = _pages_for(attn, page_size)                  # pages each sequence needs
+    own = n_alloc.copy()
+    if shared_groups:
+        for members in shared_groups:
+            own[members] -= shared_pages
+    need = int(own.sum()) + (len(shared_groups) * shared_pages if shared_groups else 0)
+    if num_pages is None:
+        num_pages = max(int(math.ceil(pool_factor * need)), need + extra_pages)
+    assert num_pages >= need
+    perm = rng.permutation(num_pages).astype(np.int32)
+    sentinel = int(perm[need]) if num_pages > need else 0
+    bt_stride = max(1, int(n_alloc.max()) if B else 1)
+    bt = np.full((B, bt_stride), sentinel, dtype=np.int32)
+    cursor = 0
+    grouped = np.zeros(B, dtype=bool)
+    if shared_groups:
+        for members in shared_groups:
+            pages = perm[cursor:cursor + shared_pages]
+            cursor += shared_pages
+            bt[np.asarray(members), :shared_pages] = pages
+            grouped[np.asarray(members)] = True
+    for b in range(B):
+        start = shared_pages if grouped[b] else 0
+        n_own = int(n_alloc[b]) - start
+        bt[b, start:start + n_own] = perm[cursor:cursor + n_own]
+        cursor += n_own
+    assert cursor == need
+
+    # NaN sentinel mask over [num_pages, page_size]: everything not holding a
+    # cached token of some sequence (the pending append row included).
+    sentinel_rows = np.ones((num_pages, page_size), dtype=bool)
+    for b in range(B):
+        L = int(lens[b])
+        full, rem = divmod(L, page_size)
+        if full:
+            sentinel_rows[bt[b, :full]] = False
+        if rem:
+            sentinel_rows[bt[b, full], :rem] = False
+
+    Dv = Dv if Dv is not None else D
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    if mla:
+        k_pool = _randn((num_pages, page_size, D), g, device, dtype)
+        v_pool = None
+    else:
+        k_pool = _randn((num_pages, page_size, H_kv, D), g, device, dtype)
+        v_pool = _randn((num_pages, page_size, H_kv, Dv), g, device, dtype)
+    q = _randn((B, H_q, D), g, device, dtype)
+    k_new = v_new = None
+    if append:
+        k_new = _randn((B, H_kv, D), g, device, dtype)
+        v_new = _randn((B, H_kv, Dv), g, device, dtype)
+    mask = torch.from_numpy(sentinel_rows).to(device)
+    nan = float("nan")
+    k_pool.view(num_pages, page_size, -1).masked_fill_(mask[:, :, None], nan)
+    if v_pool is not None:
+        v_pool.view(num_pages, page_size, -1).masked_fill_(mask[:, :, None], nan)
+    return PagedCase(name=name, seed=seed, B=B, H_q=H_q, H_kv=H_kv, D=D, Dv=Dv,
+                     page_size=page_size, num_pages=num_pages, dtype=dtype, scale=scale,
+                     mla=mla, append=append, seq_lens=lens, block_table=bt,
+                     sentinel_page=sentinel, q=q, k_pool=k_pool, v_pool=v_pool,
+                     k_new=k_new, v_new=v_new,
+                     groups_truth=[np.asarray(m) for m in shared_groups] if shared_groups else None,
+                     prefix_pages_truth=shared_pages if shared_groups else 0)
+
+
+# --------------------------------------------------------------------------
+# The five workloads (sizes as stated by the workload list) and small variants
+# --------------------------------------------------------------------------
+
+def tiny_gqa_append(device="cpu", seed: int = 1) -> PagedCase:
+    """Tiny paged GQA decode: B=4, 8/2 heads, D=64, page 16, fp32, lens
+    {17, 40, 64, 100}, 64-page pool, scale 1/8, one appended token."""
+    return build_case("tiny_gqa_append_fp32", seed, B=4, H_q=8, H_kv=2, D=64, page_size=16,
+                      seq_lens=[17, 40, 64, 100], dtype="f32", scale=1.0 / math.sqrt(64),
+                      append=True, num_pages=64, device=device)
+
+
+def llama3_8b_layer(device="cpu", seed: int = 2, B: int = 64, lo: int = 512, hi: int = 4096,
+                    append: bool = True) -> PagedCase:
+    """Llama-3-8B-shaped decode layer: 32/8 heads, D=128, bf16, page 16,
+    lens ~ U[lo, hi], pool 1.25x the need."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_case(f"llama3_8b_layer_B{B}", seed, B=B, H_q=32, H_kv=8, D=128, page_size=16,
+                      seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128),
+                      append=append, device=device, rng=rng)
+
+
+def mixed_lengths(device="cpu", seed: int = 3, repeat: int = 32) -> PagedCase:
+    """Mixed-length batch: lens {20,30,50,80,120,200,500,1000} x repeat, shuffled;
+    32/8 heads, D=64, bf16, page 16, random page placement."""
+    rng = np.random.default_rng(seed)
+    base = np.array([20, 30, 50, 80, 120, 200, 500, 1000], dtype=np.int32)
+    lens = rng.permutation(np.tile(base, repeat)).astype(np.int32)
+    return build_case(f"mixed_lengths_B{len(lens)}", seed, B=len(lens), H_q=32, H_kv=8, D=64,
+                      page_size=16, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(64),
+                      device=device, rng=rng)
+
+
+def shared_prefix_cascade(device="cpu", seed: int = 4, groups: int = 16, members: int = 1024,
+                          prefix_tokens: int = 2048, suffix_lo: int = 64,
+                          suffix_hi: int = 512, ungrouped: int = 0) -> PagedCase:
+    """Shared-prefix cascade: ``groups`` x ``members`` sequences, each group one
+    shared prefix of ``prefix_tokens`` tokens (whole pages, shared by id) plus
+    per-sequence suffix ~ U[suffix_lo, suffix_hi]; 32/8 heads, D=64, bf16,
+    page 16. Sequence order is shuffled; ``ungrouped`` extra sequences own
+    all their pages."""
+    ps = 16
+    assert prefix_tokens % ps == 0
+    rng = np.random.default_rng(seed)
+    B = groups * members + ungrouped
+    order = rng.permutation(B)
+    group_lists = [np.sort(order[gi * members:(gi + 1) * members]) for gi in range(groups)]
+    suffix = rng.integers(suffix_lo, suffix_hi + 1, size=B).astype(np.int32)
+    lens = (prefix_tokens + suffix).astype(np.int32)
+    return build_case(f"cascade_{groups}x{members}", seed, B=B, H_q=32, H_kv=8, D=64,
+                      page_size=ps, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(64),
+                      shared_groups=group_lists, shared_pages=prefix_tokens // ps,
+                      device=device, rng=rng)
+
+
+def absorbed_mla(device="cpu", seed: int = 5, B: int = 64, lo: int = 8192,
+                 hi: int = 50000) -> PagedCase:
+    """Absorbed-MLA paged decode: 128 heads, one latent head of 576 (V = first
+    512), bf16, page 64, lens ~ U[lo, hi], scale 1/sqrt(192)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_case(f"absorbed_mla_B{B}", seed, B=B, H_q=128, H_kv=1, D=576, Dv=512,
+                      page_size=64, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(192),
+                      mla=True, device=device, rng=rng)
+
+
+# --------------------------------------------------------------------------
+# Moving inputs to the oracle (data movement only)
+# --------------------------------------------------------------------------
+
+def _to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def oracle_view(case: PagedCase, seq_idx: Optional[Sequence[int]] = None,
+                k_pool: Optional[torch.Tensor] = None,
+                v_pool: Optional[torch.Tensor] = None) -> Dict[str, np.ndarray]:
+    """The inputs of sequences ``seq_idx`` as float64 numpy arrays.
+
+    Only the pages those sequences own are copied; their block-table rows are
+    renumbered to the compacted pool. ``k_pool``/``v_pool`` default to the
+    case's pools (pass a snapshot taken before an append to get pre-append data).
+    """
+    B = case.B
+    idx = np.arange(B) if seq_idx is None else np.asarray(seq_idx, dtype=np.int64)
+    lens = case.attn_lens[idx]
+    n_alloc = _pages_for(lens, case.page_size)
+    rows = case.block_table[idx]
+    used = np.unique(np.concatenate([rows[i, :n_alloc[i]] for i in range(len(idx))] + [np.zeros(0, np.int32)]))
+    remap = {int(p): i for i, p in enumerate(used)}
+    bt = np.zeros((len(idx), max(1, rows.shape[1])), dtype=np.int64)
+    for i in range(len(idx)):
+        for j in range(int(n_alloc[i])):
+            bt[i, j] = remap[int(rows[i, j])]
+    kp = case.k_pool if k_pool is None else k_pool
+    vp = case.v_pool if v_pool is None else v_pool
+    dev_pages = torch.from_numpy(used.astype(np.int64)).to(kp.device)
+    out = {
+        "q": _to_f64(case.q[torch.from_numpy(idx).to(case.q.device)]),
+        "k_pool": _to_f64(kp.index_select(0, dev_pages)) if len(used) else None,
+        "v_pool": _to_f64(vp.index_select(0, dev_pages)) if (vp is not None and len(used)) else None,
+        "block_table": bt,
+        "seq_lens": lens.astype(np.int64),
+        "positions": case.seq_lens[idx].astype(np.int64),
+        "page_of_remapped": used,
+    }
+    if case.append:
+        dev_idx = torch.from_numpy(idx).to(case.q.device)
+        out["k_new"] = _to_f64(case.k_new[dev_idx])
+        out["v_new"] = _to_f64(case.v_new[dev_idx])
+    return out
+
+
+def sample_sequences(case: PagedCase, n: int, seed: int = 0) -> np.ndarray:
+    """A seeded sample of sequence ids that always includes the shortest and
+    the longest sequence (ragged extremes)."""
+    rng = np.random.default_rng(seed + 1000 * case.seed)
+    n = min(n, case.B)
+    pick = set(rng.choice(case.B, size=n, replace=False).tolist())
+    pick.add(int(np.argmin(case.attn_lens)))
+    pick.add(int(np.argmax(case.attn_lens)))
+    return np.array(sorted(pick), dtype=np.int64)
