@@ -1,0 +1,263 @@
+/*
+ * ts_attn.h - decode-step attention over a paged KV cache, for GB300 (sm_103a).
+ *
+ * A C ABI: plain pointers and sizes, no framework types. Every function that
+ * takes a `stream` (a cudaStream_t passed as void*, NULL = legacy default
+ * stream) is asynchronous on it: it validates its arguments on the host,
+ * enqueues its kernels and returns. Inputs must stay alive and unmodified
+ * until the stream reaches the call. The library never allocates device
+ * memory and keeps no state besides a per-device cache of the SM count and
+ * of kernel attributes; scratch memory ("workspace") is passed in by the
+ * caller and sized by the matching *_workspace_size function.
+ *
+ * Shared conventions
+ *   - Element types: TS_F32 (float) or TS_BF16 (bfloat16, round-to-nearest-
+ *     even on output). Arithmetic is float32 everywhere (fp32 accumulate).
+ *   - K/V page pool layout ("NHD"): [num_pages, page_size, H_kv, D], row-major.
+ *     Token t of sequence b lives in physical page block_table[b*bt_stride +
+ *     t/page_size] at row t%page_size. (SwiftLLM page, section 3.1: the cache
+ *     is split into fixed-size blocks found through a per-request block
+ *     table; section 5.1: attention takes the query, block tables and
+ *     context lengths.)
+ *   - GQA: query head h reads kv head h / (H_q / H_kv).
+ *   - LSE outputs are natural-log log-sum-exp of the scaled scores, float32.
+ *     A sequence of length 0 yields O = 0 and LSE = -inf.
+ *   - Device-side safety: a page id outside [0, num_pages) is never
+ *     dereferenced. Attention treats the tokens of such a page as absent and
+ *     sets bit TS_DEVERR_PAGE_RANGE in the workspace's error word; the append
+ *     skips the write. No kernel traps; every pipeline wait is time-bounded
+ *     and on timeout sets TS_DEVERR_TIMEOUT and leaves the kernel.
+ *   - Errors: argument errors are returned before anything is enqueued; a
+ *     failed launch returns TS_ERR_CUDA. ts_last_error_detail() describes the
+ *     last non-OK status of the calling thread.
+ */
+#ifndef TS_ATTN_H_
+#define TS_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TS_API __attribute__((visibility("default")))
+#else
+#define TS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
+  TS_ERR_UNSUPPORTED = 2,   /* valid but not compiled (head dim, group size...) */
+  TS_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+  TS_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  TS_ERR_CAPACITY = 5       /* a caller-provided output array is too small */
+} ts_status;
+
+typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
+
+/* Bits of the sticky device error word kept in the first 4 bytes of an
+ * attention workspace. The library sets bits and never clears them. */
+#define TS_DEVERR_PAGE_RANGE 0x1u
+#define TS_DEVERR_TIMEOUT 0x2u
+
+/* Human-readable name of a status code. Never NULL. */
+TS_API const char* ts_status_string(int status);
+
+/* Details of the last non-OK status returned on the calling thread ("" if none). */
+TS_API const char* ts_last_error_detail(void);
+
+/* Library version string. */
+TS_API const char* ts_version(void);
+
+/*
+ * ts_kv_append - write one new token's K and V per sequence into the pools.
+ *
+ * SwiftLLM page, section 3.1: blocks are allocated to a request on demand;
+ * the token at position pos lands in page block_table[b][pos / page_size],
+ * row pos % page_size. The block table must already hold that page.
+ *
+ *   k_new, v_new  device [B, H_kv, D] of dtype
+ *   k_pool,v_pool device [num_pages, page_size, H_kv, D] of dtype (written)
+ *   block_table   device int32 [B, bt_stride]
+ *   positions     device int32 [B]: token index to write (= cached length
+ *                 before the append); afterwards attention covers pos + 1
+ *                 tokens.
+ * The copy is bit-exact. Rows whose page index or page id is out of range
+ * are skipped. B == 0 returns TS_OK with nothing enqueued.
+ */
+TS_API ts_status ts_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                       const int32_t* block_table, int32_t bt_stride, const int32_t* positions,
+                       int32_t B, int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages,
+                       ts_dtype dtype, void* stream);
+
+/*
+ * ts_paged_decode_workspace_size - bytes of workspace ts_paged_decode_attn
+ * needs on the current device for a batch of B sequences. Depends on the
+ * device's SM count (the kernel runs one persistent CTA per SM). Returns 0 on
+ * invalid arguments.
+ */
+TS_API size_t ts_paged_decode_workspace_size(int32_t B, int32_t H_q, int32_t D);
+
+/*
+ * ts_paged_decode_attn - one decode step of GQA attention over a paged cache.
+ *
+ * For every sequence b and query head h (kv head h / g, g = H_q / H_kv):
+ *   s_t = scale * <q[b,h,:], K_b[t,:]> for t < seq_lens[b],
+ *   O[b,h,:] = sum_t softmax(s)_t V_b[t,:],  LSE[b,h] = log sum_t exp(s_t).
+ *
+ * Flash-decoding split-KV (TokenSpeed deep dive, section 7 fig. 3 and 7.1):
+ * the pages of the whole batch are cut into equal contiguous ranges, one per
+ * SM; a sequence cut across ranges produces float32 partial (O, LSE) states
+ * in the workspace that a second kernel reduces by LSE. Planning runs on the
+ * device from seq_lens, so no host copy of the lengths is needed and the
+ * call can be captured in a CUDA graph.
+ *
+ *   q             device [B, H_q, D] of dtype
+ *   k_pool,v_pool device [num_pages, page_size, H_kv, D] of dtype
+ *   block_table   device int32 [B, bt_stride]
+ *   seq_lens      device int32 [B] tokens attended per sequence (>= 0)
+ *   out           device [B, H_q, D] of dtype (written)
+ *   lse           device float32 [B, H_q] (written) or NULL
+ *   workspace     device, >= ts_paged_decode_workspace_size(B, H_q, D) bytes,
+ *                 256-byte aligned; its first 4 bytes are the sticky device
+ *                 error word (see TS_DEVERR_*), zero it to check it later.
+ * Supported: D in {64, 128}, H_q / H_kv in {1, 2, 4, 8}, H_kv in {1, 2, 4, 8},
+ * page_size in {8, 16, 32}, and one page of K+V for all kv heads within the
+ * shared-memory stage budget. Others return TS_ERR_UNSUPPORTED.
+ */
+TS_API ts_status ts_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                               int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                               ts_dtype dtype, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
+ * ts_merge_states - merge two attention states over disjoint key sets.
+ *
+ * Per row r: m = max(lse_a, lse_b), w_a = exp(lse_a - m), w_b = exp(lse_b - m),
+ *   O = (w_a O_a + w_b O_b) / (w_a + w_b),  LSE = m + log(w_a + w_b).
+ * A state with LSE = -inf has weight 0; two empty states give O = 0,
+ * LSE = -inf. (TokenSpeed deep dive, section 7 fig. 3: partials are reduced
+ * by their LSE; Tokasaurus blog, shared-prefix attention is combined with the
+ * per-sequence part.)
+ *
+ *   o_a, o_b   device [rows, D] of dtype;  lse_a, lse_b device float32 [rows]
+ *   o_out      device [rows, D] of dtype;  lse_out device float32 [rows] or NULL
+ * o_out may alias o_a or o_b (each element is read before it is written by
+ * the same thread). D must be a multiple of 4 (bf16: of 8), at most 1024.
+ */
+TS_API ts_status ts_merge_states(const void* o_a, const float* lse_a, const void* o_b,
+                          const float* lse_b, void* o_out, float* lse_out, int64_t rows,
+                          int32_t D, ts_dtype dtype, void* stream);
+
+/*
+ * Shared-prefix groups (Tokasaurus blog, "Dynamic prefix identification and
+ * exploration": a greedy depth-first search before each forward pass finds
+ * the longest shared prefixes; Hydragen / cascade attention then computes
+ * attention over each shared prefix once per group).
+ *
+ * CSR arrays, all int32. The caller allocates every array; the capacities say
+ * how large they are.
+ *   prefix_indptr[capacity_groups + 1], prefix_pages[capacity_prefix_pages]
+ *   prefix_len[capacity_groups]        tokens shared (= pages * page_size)
+ *   member_indptr[capacity_groups + 1], member_ids[capacity_members]
+ *   group_of[B]                        group of each sequence, -1 if none
+ */
+typedef struct {
+  int32_t num_groups;
+  int32_t* prefix_indptr;
+  int32_t* prefix_pages;
+  int32_t* prefix_len;
+  int32_t* member_indptr;
+  int32_t* member_ids;
+  int32_t* group_of;
+  int32_t capacity_groups;
+  int32_t capacity_prefix_pages;
+  int32_t capacity_members;
+} ts_prefix_groups;
+
+/*
+ * ts_group_prefixes - host-side greedy longest-shared-prefix grouping.
+ *
+ * Runs on the CPU over HOST copies of the block table and lengths. Prefixes
+ * are whole pages shared by physical page id; each member keeps at least one
+ * suffix token (a member of length L shares at most (L-1)/page_size pages).
+ * Greedy longest-first: repeatedly the deepest prefix shared by at least
+ * min_group ungrouped sequences becomes a group with all of them (ties: more
+ * members first, then the smaller page-id path). Sequences in no group take
+ * the flat paged path. min_group >= 2. Returns TS_ERR_CAPACITY if an output
+ * array is too small (num_groups is then the count needed, if known).
+ */
+TS_API ts_status ts_group_prefixes(const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                            int32_t B, int32_t page_size, int32_t min_group, ts_prefix_groups* out);
+
+/*
+ * ts_cascade_decode_workspace_size - workspace bytes for ts_cascade_decode_attn.
+ */
+TS_API size_t ts_cascade_decode_workspace_size(int32_t B, int32_t H_q, int32_t D);
+
+/*
+ * ts_cascade_decode_attn - decode attention with shared prefixes computed once.
+ *
+ * Same result as ts_paged_decode_attn over the full block tables (up to
+ * float32 rounding). For each group the queries of all members (members * g
+ * rows per kv head) attend the group's prefix pages as one dense
+ * tensor-core product (tcgen05, accumulators in TMEM); each sequence's own
+ * pages (the suffix after its group's prefix, or everything if ungrouped)
+ * go through the paged split-KV path; the two states are merged by LSE.
+ *
+ *   groups       device copies of the CSR arrays of ts_group_prefixes
+ *                (num_groups, prefix_indptr, prefix_pages, prefix_len,
+ *                member_indptr, member_ids, group_of; capacities ignored)
+ *   other arguments as in ts_paged_decode_attn (seq_lens = full lengths).
+ * Supported: D == 64 with H_q / H_kv == 4 and bf16 for the tensor-core
+ * prefix; page_size 16.
+ */
+TS_API ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                 const ts_prefix_groups* groups, const int32_t* block_table,
+                                 int32_t bt_stride, const int32_t* seq_lens, int32_t B,
+                                 int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                                 int32_t num_pages, float scale, ts_dtype dtype, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * ts_mla_workspace_size - workspace bytes for ts_mla_paged_decode.
+ */
+TS_API size_t ts_mla_workspace_size(int32_t B, int32_t H, int32_t D_v);
+
+/*
+ * ts_mla_paged_decode - absorbed multi-head latent attention decode.
+ *
+ * Every query head attends the one shared latent head:
+ *   s[h,t] = scale * <q[b,h,0:D_qk], C_b[t,0:D_qk]>,
+ *   O[b,h,:] = sum_t softmax_t(s[h,:]) C_b[t,0:D_v],  LSE[b,h] = log sum_t exp(s[h,t]).
+ * (TokenSpeed deep dive, section 7 fig. 3 and 7.1: split-KV partials plus a
+ * reduction kernel, 512-wide output rows.)
+ *
+ *   q        device bf16 [B, H, D_qk]
+ *   kv_pool  device bf16 [num_pages, page_size, D_qk]  (V = first D_v columns)
+ *   out      device bf16 [B, H, D_v];  lse device float32 [B, H] or NULL
+ * Supported: H == 128, D_qk == 576, D_v == 512, page_size 64, bf16.
+ */
+TS_API ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t H,
+                              int32_t D_qk, int32_t D_v, int32_t page_size, int32_t num_pages,
+                              float scale, void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * ts_read_device_error - copy the sticky error word of an attention
+ * workspace to *error_bits (synchronises the stream).
+ */
+TS_API ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TS_ATTN_H_ */

@@ -1,0 +1,80 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every symbol the
+public headers declare, and rejects bad arguments on the host before any
+launch (CPU only: no compute call is made)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_46_gb300 as ts
+from paged_kv_cache_46_gb300 import build as ts_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ts_build.build()
+    return ts.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"^TS_API\s+[\w\s\*]+?\b(ts_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    assert lib.ts_status_string(0) == b"TS_OK"
+    assert lib.ts_status_string(1) == b"TS_ERR_INVALID_ARG"
+    assert lib.ts_status_string(99) == b"TS_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.ts_version()
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    f = lib.ts_paged_decode_attn
+    vp = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    # H_q not a multiple of H_kv
+    st = f(vp, vp, vp, vp, 4, vp, 2, 6, 4, 64, 16, 8, 1.0, 1, vp, None, vp, 1 << 20, None)
+    assert st == ts.TS_ERR_INVALID_ARG
+    assert b"multiple" in lib.ts_last_error_detail()
+    # negative batch
+    st = f(vp, vp, vp, vp, 4, vp, -1, 8, 2, 64, 16, 8, 1.0, 1, vp, None, vp, 1 << 20, None)
+    assert st == ts.TS_ERR_INVALID_ARG
+    # bad dtype
+    st = f(vp, vp, vp, vp, 4, vp, 2, 8, 2, 64, 16, 8, 1.0, 7, vp, None, vp, 1 << 20, None)
+    assert st == ts.TS_ERR_INVALID_ARG
+    # non-finite scale
+    st = f(vp, vp, vp, vp, 4, vp, 2, 8, 2, 64, 16, 8, float("nan"), 1, vp, None, vp, 1 << 20, None)
+    assert st == ts.TS_ERR_INVALID_ARG
+    # empty batch is a no-op
+    st = f(None, None, None, None, 4, None, 0, 8, 2, 64, 16, 8, 1.0, 1, None, None, None, 0, None)
+    assert st == ts.TS_OK
+    # append and merge: empty batches are no-ops, bad sizes are rejected
+    assert lib.ts_kv_append(None, None, None, None, None, 4, None, 0, 2, 64, 16, 8, 1, None) == ts.TS_OK
+    assert lib.ts_kv_append(vp, vp, vp, vp, vp, 4, vp, 2, 0, 64, 16, 8, 1, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_merge_states(None, None, None, None, None, None, 0, 64, 1, None) == ts.TS_OK
+    assert lib.ts_merge_states(vp, vp, vp, vp, vp, vp, 3, 12, 1, None) == ts.TS_ERR_UNSUPPORTED
+    unaligned = ctypes.c_void_p(24)
+    assert lib.ts_merge_states(unaligned, vp, vp, vp, vp, vp, 3, 64, 1, None) == ts.TS_ERR_INVALID_ARG
+
+
+def test_python_binding_requires_int32_metadata():
+    import torch
+    q = torch.zeros(1, 8, 64)
+    with pytest.raises(TypeError):
+        ts.ts_paged_decode_attn(q, torch.zeros(2, 16, 2, 64), torch.zeros(2, 16, 2, 64),
+                                torch.zeros(1, 1, dtype=torch.int64), torch.zeros(1, dtype=torch.int32), 1.0)
