@@ -42,15 +42,21 @@ constexpr int kMaxConsumerWarps = 8;
 // Three warp groups: group 0 holds the producer (warp 0; warps 1-3 leave after
 // the prologue), groups 1-2 hold the consumer warps (warp 4 + kv head).
 // Register split: launched at kLaunchRegs per thread; the producer group gives
-// registers back (setmaxnreg.dec to kProducerRegs) and the consumer groups take
-// them (setmaxnreg.inc to kConsumerRegs). 128*40 + 256*232 == 384*168.
+// registers back (setmaxnreg.dec, RegSplit) and the consumer groups take
+// them (setmaxnreg.inc): 128*56 + 256*224 == 384*168, or
+// 128*40 + 256*232 == 384*168 for group size 8.
 constexpr int kThreads = 384;
 constexpr int kFirstConsumerWarp = 4;
 constexpr int kLaunchRegs = 168;
-constexpr int kProducerRegs = 40;
-constexpr int kConsumerRegs = 232;
-static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= kThreads * kLaunchRegs,
-              "register split exceeds the launch allocation");
+// Group size 8 keeps twice the query/accumulator registers per lane pair and
+// takes the larger consumer share.
+template <int G>
+struct RegSplit {
+  static constexpr int kProducer = G >= 8 ? 40 : 56;
+  static constexpr int kConsumer = G >= 8 ? 232 : 224;
+  static_assert(128 * kProducer + 256 * kConsumer <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+};
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;
 constexpr uint32_t kFlagFirst = 1u, kFlagLast = 2u, kFlagEnd = 4u, kFlagBadPage = 8u;
@@ -79,8 +85,10 @@ struct PagedParams {
   float* part_o;     // [2 * gridDim.x, H_q, D]
   float* part_lse;   // [2 * gridDim.x, H_q]
   int32_t num_stages;
-  uint32_t stage_bytes;  // bytes per stage (K page + V page + q rows, aligned)
+  uint32_t stage_bytes;  // bytes per stage (K rows + V rows + q rows, aligned)
   uint32_t page_bytes;   // bytes of one full page of K (or V), all kv heads
+  int32_t chunk_rows;    // token rows per stage (a page, or a contiguous part of one)
+  uint32_t kv_area;      // chunk_rows * row_bytes: K (and V) area of a stage
   uint32_t row_bytes;    // bytes of one token row of K (or V), all kv heads
   uint32_t q_bytes;      // bytes of one sequence's query rows
 };
@@ -201,8 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     total += v;
   }
   const long long excl = wbase + incl - mine;
-  const long long start = total * k / G_ctas;
-  const long long end = total * (k + 1) / G_ctas;
+  // Balanced cut: the first (total % G) CTAs take one page more. Non-empty
+  // ranges are contiguous, so a sequence's pages always lie in consecutive
+  // non-empty CTAs (the merge relies on it).
+  const long long q_pages = total / G_ctas, r_pages = total % G_ctas;
+  const long long start = k * q_pages + min(static_cast<long long>(k), r_pages);
+  const long long end = start + q_pages + (k < r_pages ? 1 : 0);
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
     for (int b = lo; b < hi; ++b) {
@@ -219,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   __syncthreads();
 
   if (warp < kFirstConsumerWarp) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<G>::kProducer));
     if (warp != 0) return;
     // ======================= producer warp ================================
     int it = 0;
@@ -242,8 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         const bool complete = (pg == 0) && (n_here == np);
         const int out_slot = complete ? -1 : (first_seg ? 2 * k : 2 * k + 1);
         if (pg == 0 && lane == 0) {
-          const long long last = g + np - 1;
-          const int k1 = static_cast<int>(((last + 1) * G_ctas - 1) / total);
+          const long long last = g + np - 1;  // global index of the sequence's last page
+          const long long big = r_pages * (q_pages + 1);
+          const int k1 = static_cast<int>(last < big ? last / (q_pages + 1)
+                                                     : r_pages + (last - big) / max(q_pages, 1ll));
           const int nparts = k1 - k + 1;
           p.split_info[b] = make_int2(k, (nparts << 1) | (first_seg ? 0 : 1));
         }
@@ -255,48 +269,54 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
           if (lane < cnt && pg + base + lane < p.bt_stride) pid = bt_row[base + lane];
           for (int i = 0; i < cnt; ++i) {
             const int page = __shfl_sync(0xffffffffu, pid, i);
-            if (lane == 0) {
-              const int s = it % S;
-              if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
-                set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
-                aborted = true;
-              } else {
-                const int pidx = pg + base + i;
-                int valid = (pidx == np - 1) ? (L - pidx * ps) : ps;
-                uint32_t flags = (base + i == 0 ? kFlagFirst : 0u) |
-                                 (base + i == n_here - 1 ? kFlagLast : 0u);
-                const bool ok = page >= 0 && page < p.num_pages;
-                if (!ok) {
-                  flags |= kFlagBadPage;
-                  valid = 0;
-                  set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
+            const int pidx = pg + base + i;
+            const bool ok = page >= 0 && page < p.num_pages;
+            const int rows = ok ? ((pidx == np - 1) ? (L - pidx * ps) : ps) : 0;
+            const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
+            for (int c = 0; c < nchunks; ++c) {
+              if (lane == 0) {
+                const int s = it % S;
+                if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
+                  set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+                  aborted = true;
+                } else {
+                  const int r0 = c * p.chunk_rows;
+                  const int valid = max(0, min(rows - r0, p.chunk_rows));
+                  uint32_t flags = (base + i == 0 && c == 0 ? kFlagFirst : 0u) |
+                                   (base + i == n_here - 1 && c == nchunks - 1 ? kFlagLast : 0u);
+                  if (!ok) {
+                    flags |= kFlagBadPage;
+                    set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
+                  }
+                  StageDesc d;
+                  d.b = b;
+                  d.valid = valid;
+                  d.flags = flags;
+                  d.out_slot = out_slot;
+                  desc[s] = d;
+                  const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
+                  const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
+                  const uint32_t full_bar = smem_u32(&full[s]);
+                  mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
+                  const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
+                  if (bytes) {
+                    const size_t off = static_cast<size_t>(page) * p.page_bytes +
+                                       static_cast<size_t>(r0) * p.row_bytes;
+                    bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
+                    bulk_g2s_hint(st + p.kv_area, static_cast<const char*>(p.v_pool) + off, bytes,
+                                  full_bar, pol);
+                  }
+                  if (qb)
+                    bulk_g2s(st + 2 * p.kv_area,
+                             static_cast<const char*>(p.q) + static_cast<size_t>(b) * p.q_bytes, qb,
+                             full_bar);
                 }
-                StageDesc d;
-                d.b = b;
-                d.valid = valid;
-                d.flags = flags;
-                d.out_slot = out_slot;
-                desc[s] = d;
-                const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
-                const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
-                const uint32_t full_bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
-                const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-                if (bytes) {
-                  const size_t off = static_cast<size_t>(page) * p.page_bytes;
-                  bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
-                  bulk_g2s_hint(st + p.page_bytes, static_cast<const char*>(p.v_pool) + off, bytes,
-                                full_bar, pol);
-                }
-                if (qb)
-                  bulk_g2s(st + 2 * p.page_bytes,
-                           static_cast<const char*>(p.q) + static_cast<size_t>(b) * p.q_bytes, qb,
-                           full_bar);
               }
+              aborted = __shfl_sync(0xffffffffu, aborted, 0);
+              if (aborted) break;
+              ++it;
             }
-            aborted = __shfl_sync(0xffffffffu, aborted, 0);
             if (aborted) break;
-            ++it;
           }
         }
         g += n_here;
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     }
     return;
   }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<G>::kConsumer));
   if (warp - kFirstConsumerWarp >= n_consumer) return;
 
   // ========================= consumer warps ================================
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int j = lane / C::kLPT;
   const int l = lane % C::kLPT;
   const int tokens_per_pass = C::kNG * C::kTPG;
-  const int npass = (ps + tokens_per_pass - 1) / tokens_per_pass;
+  const int npass = (p.chunk_rows + tokens_per_pass - 1) / tokens_per_pass;
   const int H_kv = p.H_kv;
 
   int dim_off[C::kNV];
@@ -356,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     const StageDesc d = desc[s];
     if (d.flags & kFlagEnd) break;
     const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-    const uint32_t kbase = st, vbase = st + p.page_bytes, qbase = st + 2 * p.page_bytes;
+    const uint32_t kbase = st, vbase = st + p.kv_area, qbase = st + 2 * p.kv_area;
 
     if (d.flags & kFlagFirst) {
 #pragma unroll
@@ -706,10 +726,25 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
   prm.row_bytes = static_cast<uint32_t>(H_kv * D * es);
   prm.page_bytes = static_cast<uint32_t>(page_size) * prm.row_bytes;
   prm.q_bytes = static_cast<uint32_t>(H_q * D * es);
-  prm.stage_bytes = static_cast<uint32_t>(align_up(2 * prm.page_bytes + prm.q_bytes, 128));
+  // A stage holds chunk_rows token rows of one page (all kv heads, K and V)
+  // plus room for one sequence's query rows. Whole pages when two stages fit,
+  // else halves, quarters... TS_PAGED_DECODE_CHUNK_ROWS overrides (tuning).
+  int chunk_rows = page_size;
+  if (const char* env = getenv("TS_PAGED_DECODE_CHUNK_ROWS")) {
+    const int v = atoi(env);
+    if (v > 0 && v <= page_size) chunk_rows = v;
+  }
+  auto stage_of = [&](int rows) {
+    return static_cast<uint32_t>(align_up(2ull * rows * prm.row_bytes + prm.q_bytes, 128));
+  };
+  while (chunk_rows > 1 && (kSmemBudget - kHeaderBytes) / stage_of(chunk_rows) < 2)
+    chunk_rows = (chunk_rows + 1) / 2;
+  prm.chunk_rows = chunk_rows;
+  prm.kv_area = static_cast<uint32_t>(chunk_rows) * prm.row_bytes;
+  prm.stage_bytes = stage_of(chunk_rows);
   const int stages = std::min<int>(kMaxStages, (kSmemBudget - kHeaderBytes) / prm.stage_bytes);
   if (stages < 2)
-    return fail(TS_ERR_UNSUPPORTED, "%s: one page of K+V for all kv heads (%u B) exceeds the stage budget",
+    return fail(TS_ERR_UNSUPPORTED, "%s: one token row of K+V plus the query rows (%u B) exceeds the stage budget",
                 who, prm.stage_bytes);
   prm.num_stages = stages;
   const size_t smem = kHeaderBytes + static_cast<size_t>(stages) * prm.stage_bytes;
