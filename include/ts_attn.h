@@ -136,6 +136,36 @@ TS_API ts_status ts_paged_decode_attn(const void* q, const void* k_pool, const v
                                size_t workspace_bytes, void* stream);
 
 /*
+ * ts_paged_decode_attn_noalloc - ts_paged_decode_attn without a workspace.
+ *
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory: a plugin that its host runtime hands only
+ * input and output buffers, or an engine that has reserved all free HBM for
+ * its KV-cache pool and must not pay cudaMalloc's latency and implicit
+ * synchronisation in its decode loop. Same arguments and results as
+ * ts_paged_decode_attn minus the workspace. It allocates nothing: the
+ * split-KV scratch is a fixed array of TS_NOALLOC_SCRATCH_BYTES bytes inside
+ * the library's device image, held by every GPU that loads the library until
+ * the process exits.
+ *   - Sizes whose scratch need (ts_paged_decode_workspace_size(B, H_q, D))
+ *     exceeds TS_NOALLOC_SCRATCH_BYTES return TS_ERR_WORKSPACE, nothing
+ *     enqueued. On a 152-SM GB300 that allows H_q * D up to about 13,000 for
+ *     moderate batches (e.g. 32 x 128 with B up to ~1.4 million).
+ *   - All calls on one device share the array: calls that may overlap on the
+ *     GPU (unordered streams) race and give wrong results.
+ *   - The error word in the array is cleared at the start of every call.
+ *   - The first call on each device looks up the array's address with that
+ *     device current; make it before any stream capture.
+ */
+#define TS_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+TS_API ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_pool,
+                                              const void* v_pool, const int32_t* block_table,
+                                              int32_t bt_stride, const int32_t* seq_lens,
+                                              int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                                              int32_t page_size, int32_t num_pages, float scale,
+                                              ts_dtype dtype, void* out, float* lse, void* stream);
+
+/*
  * ts_merge_states - merge two attention states over disjoint key sets.
  *
  * Per row r: m = max(lse_a, lse_b), w_a = exp(lse_a - m), w_b = exp(lse_b - m),

@@ -63,6 +63,8 @@ _SIGNATURES = {
     "ts_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "ts_paged_decode_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
                                             _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
+    "ts_paged_decode_attn_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32,
+                                                    _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP]),
     "ts_merge_states": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, ctypes.c_int, _VP]),
     "ts_group_prefixes": (ctypes.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, ctypes.POINTER(PrefixGroupsC)]),
     "ts_cascade_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
@@ -176,6 +178,24 @@ def ts_paged_decode_attn(q, k_pool, v_pool, block_table, seq_lens, scale: float,
                                       float(scale), _dt(q), _ptr(out), _ptr(lse), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
     return (out, lse) if return_lse else out
+
+
+def ts_paged_decode_attn_noalloc(q, k_pool, v_pool, block_table, seq_lens, scale: float, out, lse=None,
+                                 stream=None) -> None:
+    """ts_paged_decode_attn for callers that cannot allocate device memory.
+
+    The library takes its split-KV scratch from a fixed array in its own device
+    image (TS_NOALLOC_SCRATCH_BYTES, one per GPU, kept until exit) instead of a
+    caller workspace. ``out`` (and ``lse`` if wanted) must be passed in: this
+    wrapper allocates nothing either. Calls that may overlap on one GPU share
+    the array and race; see include/ts_attn.h.
+    """
+    _require_i32(block_table, seq_lens)
+    B, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    _check(lib().ts_paged_decode_attn_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                              block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, ps, P,
+                                              float(scale), _dt(q), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def ts_merge_states(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
