@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths"], default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling run for ncu: one pool copy, no e2e / CPU baseline / clock sampling")
     return ap.parse_args()
 
 
@@ -282,7 +284,11 @@ def run_ours(args):
     lens = torch.from_numpy(case.attn_lens).to(dev)
     pos = torch.from_numpy(case.positions).to(dev)
     # second copy of the pools: consecutive steps read different memory
-    pools = [(case.k_pool, case.v_pool), (case.k_pool.clone(), case.v_pool.clone())]
+    if args.profile:
+        args.no_e2e = args.no_cpu_baseline = True
+        pools = [(case.k_pool, case.v_pool)] * 2
+    else:
+        pools = [(case.k_pool, case.v_pool), (case.k_pool.clone(), case.v_pool.clone())]
     out = torch.empty_like(case.q)
     lse = torch.empty(case.B, case.H_q, dtype=torch.float32, device=dev)
     ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D), dev)
@@ -305,6 +311,8 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
+    if args.profile:
+        sampler.ok = False
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler.start()

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ts_attn.h"
+#include "ts_attn.h"
 
 namespace ts {
 

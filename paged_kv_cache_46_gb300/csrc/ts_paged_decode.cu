@@ -62,6 +62,9 @@ constexpr int kHeaderBytes = 1024;
 constexpr uint32_t kFlagFirst = 1u, kFlagLast = 2u, kFlagEnd = 4u, kFlagBadPage = 8u;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Largest score excess over the reference max (log2 units) before the
+// accumulators are rescaled: unnormalised weights stay <= 2^8.
+constexpr float kRescaleSlack = 8.0f;
 
 struct StageDesc {
   int32_t b;         // sequence
@@ -435,26 +438,42 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) sc[i][hh] = -INFINITY;
 
+      // Online softmax with a lazily moved reference max: m[] only moves when a
+      // score exceeds it by more than kRescaleSlack (log2 units), so p <= 2^slack
+      // and the accumulators are rescaled only a few times per sequence. The
+      // decision is made warp-uniform so the rescale branch never diverges.
+      float mx[G];
+      bool need = false;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        mx[hh] = sc[0][hh];
+#pragma unroll
+        for (int i = 1; i < C::kTPG; ++i) mx[hh] = fmaxf(mx[hh], sc[i][hh]);
+        need |= mx[hh] > m[hh] + kRescaleSlack;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float mnew = fmaxf(m[hh], mx[hh]);
+          const float alpha = m[hh] == -INFINITY ? 0.f : fast_exp2(m[hh] - mnew);
+          m[hh] = mnew;
+          lsum[hh] *= alpha;
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __fmul2_rn(acc[hh][x], a2);
+        }
+      }
       float pr[C::kTPG][G];
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float mx = sc[0][hh];
-#pragma unroll
-        for (int i = 1; i < C::kTPG; ++i) mx = fmaxf(mx, sc[i][hh]);
-        const float mnew = fmaxf(m[hh], mx);
-        const float msafe = mnew == -INFINITY ? 0.f : mnew;
-        const float alpha = fast_exp2(m[hh] - msafe);
-        m[hh] = mnew;
-        float ls = lsum[hh] * alpha;
+        const float msafe = m[hh] == -INFINITY ? 0.f : m[hh];
+        float ls = lsum[hh];
 #pragma unroll
         for (int i = 0; i < C::kTPG; ++i) {
           pr[i][hh] = fast_exp2(sc[i][hh] - msafe);
           ls += pr[i][hh];
         }
         lsum[hh] = ls;
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __fmul2_rn(acc[hh][x], a2);
       }
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
