@@ -59,6 +59,7 @@ struct RegSplit {
 };
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;
+constexpr int kZeroRowOff = kHeaderBytes;  // one zeroed token row (<= 4 KB)
 constexpr uint32_t kFlagFirst = 1u, kFlagLast = 2u, kFlagEnd = 4u, kFlagBadPage = 8u;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -89,6 +90,7 @@ struct PagedParams {
   float* part_lse;   // [2 * gridDim.x, H_q]
   int32_t num_stages;
   uint32_t stage_bytes;  // bytes per stage (K rows + V rows + q rows, aligned)
+  uint32_t stages_off;   // offset of the first stage in dynamic shared memory
   uint32_t page_bytes;   // bytes of one full page of K (or V), all kv heads
   int32_t chunk_rows;    // token rows per stage (a page, or a contiguous part of one)
   uint32_t kv_area;      // chunk_rows * row_bytes: K (and V) area of a stage
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   StageDesc* desc = reinterpret_cast<StageDesc*>(smem + 128);
   long long* warp_tot = reinterpret_cast<long long*>(smem + 512);
   int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
-  unsigned char* stages = smem + kHeaderBytes;
+  unsigned char* stages = smem + p.stages_off;
 
   pdl_wait_primary();
   pdl_launch_dependents();
@@ -184,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     s_start[1] = 0;
     fence_mbar_init();
   }
+  // A row of zeros that masked rows of empty units read instead of the stage.
+  for (int i = tid; i < static_cast<int>(p.row_bytes / 4); i += blockDim.x)
+    reinterpret_cast<uint32_t*>(smem + kZeroRowOff)[i] = 0u;
 
   // ---- prologue: total pages T and this CTA's range [start, end) ----------
   const int B = p.B;
@@ -362,8 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int H_kv = p.H_kv;
 
   int dim_off[C::kNV];
+  uint32_t lane_off[C::kNV];  // byte offset of this lane's vectors within a token row
 #pragma unroll
-  for (int v = 0; v < C::kNV; ++v) dim_off[v] = v * (D / C::kNV) + C::kVE * l;
+  for (int v = 0; v < C::kNV; ++v) {
+    dim_off[v] = v * (D / C::kNV) + C::kVE * l;
+    lane_off[v] = static_cast<uint32_t>((h * D + dim_off[v]) * C::kES);
+  }
+  const uint32_t zero_row = smem_u32(smem + kZeroRowOff);
+  const uint32_t row_stride = p.row_bytes;
 
   float2 qv[G][C::kPairsPL];
   float2 acc[G][C::kPairsPL];
@@ -403,18 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     const int valid = d.valid;
     for (int pass = 0; pass < npass; ++pass) {
       const int t0 = pass * tokens_per_pass + j * C::kTPG;
+      // Rows past `valid` read the last valid row (their scores are masked and
+      // their weights are 0); a unit with no valid row reads the zero row. So the
+      // token loop has no branches and its dependency chains interleave freely.
       float sc[C::kTPG][G];
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
         const int t = t0 + i;
+        const uint32_t ra = valid > 0 ? kbase + min(t, valid - 1) * row_stride : zero_row;
         uint4 kv[C::kNV];
 #pragma unroll
-        for (int v = 0; v < C::kNV; ++v) kv[v] = make_uint4(0, 0, 0, 0);
-        if (t < valid) {
-#pragma unroll
-          for (int v = 0; v < C::kNV; ++v)
-            kv[v] = lds128(kbase + ((t * H_kv + h) * D + dim_off[v]) * C::kES);
-        }
+        for (int v = 0; v < C::kNV; ++v) kv[v] = lds128(ra + lane_off[v]);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           float2 a = make_float2(0.f, 0.f);
@@ -433,10 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) sc[i][hh] += __shfl_xor_sync(0xffffffffu, sc[i][hh], o);
 #pragma unroll
-      for (int i = 0; i < C::kTPG; ++i)
-        if (t0 + i >= valid)
+      for (int i = 0; i < C::kTPG; ++i) {
+        const bool in = t0 + i < valid;
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) sc[i][hh] = -INFINITY;
+        for (int hh = 0; hh < G; ++hh) sc[i][hh] = in ? sc[i][hh] : -INFINITY;
+      }
 
       // Online softmax with a lazily moved reference max: m[] only moves when a
       // score exceeds it by more than kRescaleSlack (log2 units), so p <= 2^slack
@@ -478,21 +489,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
         const int t = t0 + i;
-        if (t < valid) {
-          uint4 vv[C::kNV];
+        const uint32_t ra = valid > 0 ? vbase + min(t, valid - 1) * row_stride : zero_row;
+        uint4 vv[C::kNV];
+#pragma unroll
+        for (int v = 0; v < C::kNV; ++v) vv[v] = lds128(ra + lane_off[v]);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
 #pragma unroll
           for (int v = 0; v < C::kNV; ++v)
-            vv[v] = lds128(vbase + ((t * H_kv + h) * D + dim_off[v]) * C::kES);
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
-#pragma unroll
-            for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-              for (int w = 0; w < Elem<T>::kPairs; ++w)
-                acc[hh][v * Elem<T>::kPairs + w] =
-                    __ffma2_rn(p2, Elem<T>::pair(vv[v], w), acc[hh][v * Elem<T>::kPairs + w]);
-          }
+            for (int w = 0; w < Elem<T>::kPairs; ++w)
+              acc[hh][v * Elem<T>::kPairs + w] =
+                  __ffma2_rn(p2, Elem<T>::pair(vv[v], w), acc[hh][v * Elem<T>::kPairs + w]);
         }
       }
     }
@@ -756,17 +765,19 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
   auto stage_of = [&](int rows) {
     return static_cast<uint32_t>(align_up(2ull * rows * prm.row_bytes + prm.q_bytes, 128));
   };
-  while (chunk_rows > 1 && (kSmemBudget - kHeaderBytes) / stage_of(chunk_rows) < 2)
+  while (chunk_rows > 1 &&
+         (kSmemBudget - kHeaderBytes - align_up(prm.row_bytes, 128)) / stage_of(chunk_rows) < 2)
     chunk_rows = (chunk_rows + 1) / 2;
   prm.chunk_rows = chunk_rows;
   prm.kv_area = static_cast<uint32_t>(chunk_rows) * prm.row_bytes;
   prm.stage_bytes = stage_of(chunk_rows);
-  const int stages = std::min<int>(kMaxStages, (kSmemBudget - kHeaderBytes) / prm.stage_bytes);
-  if (stages < 2)
+  prm.stages_off = static_cast<uint32_t>(kHeaderBytes + align_up(prm.row_bytes, 128));
+  const int stages = std::min<int>(kMaxStages, (kSmemBudget - prm.stages_off) / prm.stage_bytes);
+  if (stages < 2 || prm.row_bytes > 4096)
     return fail(TS_ERR_UNSUPPORTED, "%s: one token row of K+V plus the query rows (%u B) exceeds the stage budget",
                 who, prm.stage_bytes);
   prm.num_stages = stages;
-  const size_t smem = kHeaderBytes + static_cast<size_t>(stages) * prm.stage_bytes;
+  const size_t smem = prm.stages_off + static_cast<size_t>(stages) * prm.stage_bytes;
 
   ts_status st = cuda_check(
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)),
