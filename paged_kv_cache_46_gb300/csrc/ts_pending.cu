@@ -2,10 +2,6 @@
 // report TS_ERR_UNSUPPORTED so callers fail loudly instead of silently.
 #include "ts_common.cuh"
 
-extern "C" ts_status ts_group_prefixes(const int32_t*, int32_t, const int32_t*, int32_t, int32_t,
-                                       int32_t, ts_prefix_groups*) {
-  return ts::fail(TS_ERR_UNSUPPORTED, "ts_group_prefixes: not built yet");
-}
 extern "C" size_t ts_cascade_decode_workspace_size(int32_t, int32_t, int32_t) { return 0; }
 extern "C" ts_status ts_cascade_decode_attn(const void*, const void*, const void*,
                                             const ts_prefix_groups*, const int32_t*, int32_t,

@@ -113,7 +113,7 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
                append: bool = False, mla: bool = False, Dv: Optional[int] = None,
                pool_factor: float = 1.25, shared_groups: Optional[List[np.ndarray]] = None,
                shared_pages: int = 0, device="cpu", rng: Optional[np.random.Generator] = None,
-               extra_pages: int = 1, num_pages: Optional[int] = None) -> PagedCase:
+               extra_pages: int = 1, num_pages: Optional[int] = None, values: bool = True) -> PagedCase:
     """Build a case: lengths -> page need -> shuffled pool -> block tables -> values.
 
     ``shared_groups``: lists of sequence ids; each list shares its first
@@ -163,6 +163,12 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
             sentinel_rows[bt[b, full], :rem] = False
 
     Dv = Dv if Dv is not None else D
+    if not values:  # structure only (block tables and lengths), no tensors
+        return PagedCase(name=name, seed=seed, B=B, H_q=H_q, H_kv=H_kv, D=D, Dv=Dv, page_size=page_size,
+                         num_pages=num_pages, dtype=dtype, scale=scale, mla=mla, append=append,
+                         seq_lens=lens, block_table=bt, sentinel_page=sentinel,
+                         groups_truth=[np.asarray(m) for m in shared_groups] if shared_groups else None,
+                         prefix_pages_truth=shared_pages if shared_groups else 0)
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     if mla:
@@ -226,7 +232,7 @@ def mixed_lengths(device="cpu", seed: int = 3, repeat: int = 32) -> PagedCase:
 
 def shared_prefix_cascade(device="cpu", seed: int = 4, groups: int = 16, members: int = 1024,
                           prefix_tokens: int = 2048, suffix_lo: int = 64,
-                          suffix_hi: int = 512, ungrouped: int = 0) -> PagedCase:
+                          suffix_hi: int = 512, ungrouped: int = 0, values: bool = True) -> PagedCase:
     """Shared-prefix cascade: ``groups`` x ``members`` sequences, each group one
     shared prefix of ``prefix_tokens`` tokens (whole pages, shared by id) plus
     per-sequence suffix ~ U[suffix_lo, suffix_hi]; 32/8 heads, D=64, bf16,
@@ -243,7 +249,7 @@ def shared_prefix_cascade(device="cpu", seed: int = 4, groups: int = 16, members
     return build_case(f"cascade_{groups}x{members}", seed, B=B, H_q=32, H_kv=8, D=64,
                       page_size=ps, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(64),
                       shared_groups=group_lists, shared_pages=prefix_tokens // ps,
-                      device=device, rng=rng)
+                      device=device, rng=rng, values=values)
 
 
 def absorbed_mla(device="cpu", seed: int = 5, B: int = 64, lo: int = 8192,
