@@ -1,0 +1,582 @@
+// ts_cascade_decode_attn: decode attention with shared prefixes computed once.
+//
+// Tokasaurus blog, "Dynamic prefix identification and exploration": shared
+// prefixes (Hydragen / cascade attention) let the attention over a prefix run
+// once for all sequences that share it. For a group, the queries of all
+// members against the group's prefix keys form a real dense product: here a
+// tcgen05 kernel computes it with 128 query rows (members x the g query heads
+// of one kv head) per CTA against 128-key tiles of the prefix.
+//
+//   cascade_plan_kernel    tile offsets per group (device-side, from the CSR)
+//   cascade_prefix_kernel  per (group tile, kv head): S = Q K^T and O += P V on
+//                          the tensor cores, online softmax in between; writes
+//                          the fp32 prefix state (O, LSE) of every member row
+//   paged kernel (prefix mode) + split merge (ts_paged_decode.cu): each
+//                          sequence's own pages after the prefix, merged with
+//                          the prefix state by LSE into the final output.
+//
+// Prefix kernel roles (192 threads): warps 0-3 own one query row per thread
+// (Q load, softmax, epilogue), warp 4 lane 0 issues the TMA loads of K and V
+// page boxes (128-byte swizzle), warp 5 lane 0 issues the MMAs. TMEM holds
+// S (128 fp32 columns) and O (64 columns). K and V each have one buffer: the
+// K tile is refilled as soon as S's MMA has read it, the V tile as soon as
+// PV's MMA has, so loads overlap the softmax. P goes through shared memory in
+// the MMA's K-major 128-byte-swizzled layout.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "ts_common.cuh"
+
+namespace ts {
+namespace {
+
+constexpr int kHD = 64;            // head dim of the tensor-core prefix path
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per tile
+constexpr int kPS = 16;            // page size of the prefix path
+constexpr int kPagesPerTile = kBN / kPS;
+constexpr int kThreadsPfx = 192;
+constexpr uint32_t kTmemCols = 256;  // S: [0, 128), O: [128, 192)
+constexpr uint32_t kTmemO = 128;
+constexpr float kLog2eC = 1.4426950408889634f;
+constexpr float kLn2C = 0.6931471805599453f;
+constexpr float kSlack = 8.0f;
+
+// Shared memory (offsets from a 1024-aligned base).
+constexpr int kOffQ = 0;          // [128 x 64] bf16, SW128 K-major      16 KB
+constexpr int kOffK = 16384;      // [128 keys x 64] bf16, SW128          16 KB
+constexpr int kOffV = 32768;      // [128 keys x 64] bf16, SW128          16 KB
+constexpr int kOffP = 49152;      // 2 x [128 x 64 keys] bf16, SW128      32 KB
+constexpr int kOffBar = 81920;    // mbarriers
+constexpr int kOffTmem = kOffBar + 128;
+constexpr int kSmemPfx = kOffTmem + 16 + 1024;  // + alignment slack
+
+struct PrefixParams {
+  const __nv_bfloat16* q;  // [B, H_q, 64]
+  const int32_t* prefix_indptr;
+  const int32_t* prefix_pages;
+  const int32_t* prefix_len;
+  const int32_t* member_indptr;
+  const int32_t* member_ids;
+  const int32_t* tile_offset;  // [G + 1]
+  int32_t num_groups, H_q, H_kv, g, mpt, num_pages;
+  float scale_log2;
+  float* prefix_o;    // [B, H_q, 64]
+  float* prefix_lse;  // [B, H_q]
+  uint32_t* err_word;
+};
+
+// --- tcgen05 / TMA helpers --------------------------------------------------
+
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk16) {
+  return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, SBO 1024 B (8-row groups).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(1) << 16;                   // LBO (unused by swizzled K-major) = 16 B
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // SBO
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;                   // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// --- kernels -----------------------------------------------------------------
+
+// tile_offset[g + 1] = sum over groups <= g of ceil(members / mpt). One CTA.
+__global__ void __launch_bounds__(1024) cascade_plan_kernel(const int32_t* member_indptr, int G,
+                                                            int mpt, int32_t* tile_offset) {
+  __shared__ int warp_sum[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    carry = 0;
+    tile_offset[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < G; base += blockDim.x) {
+    const int i = base + tid;
+    const int c = i < G ? (member_indptr[i + 1] - member_indptr[i] + mpt - 1) / mpt : 0;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+      if (w < warp) before += warp_sum[w];
+      total += warp_sum[w];
+    }
+    if (i < G) tile_offset[i + 1] = carry + before + x;
+    __syncthreads();
+    if (tid == 0) carry += total;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
+    const PrefixParams p, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int n_tiles_total = p.tile_offset[p.num_groups];
+  if (t >= n_tiles_total) return;
+  // group of this tile: largest gi with tile_offset[gi] <= t
+  int lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.tile_offset[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int gi = lo;
+  const int mbeg = p.member_indptr[gi] + (t - p.tile_offset[gi]) * p.mpt;
+  const int mcount = min(p.mpt, p.member_indptr[gi + 1] - mbeg);
+  const int pp0 = p.prefix_indptr[gi];
+  const int n_pages = p.prefix_indptr[gi + 1] - pp0;
+  const int plen = p.prefix_len[gi];
+  const int n_kt = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  const uint32_t b_kfull = smem_u32(&bars[0]), b_vfull = smem_u32(&bars[1]);
+  const uint32_t b_kempty = smem_u32(&bars[2]), b_vempty = smem_u32(&bars[3]);
+  const uint32_t b_sfull = smem_u32(&bars[4]), b_sfree = smem_u32(&bars[5]);
+  const uint32_t b_pfull = smem_u32(&bars[6]), b_pvdone = smem_u32(&bars[7]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK);
+  const uint32_t sV = smem_u32(smem + kOffV), sP = smem_u32(smem + kOffP);
+
+  if (tid == 0) {
+    mbar_init(b_kfull, 1);
+    mbar_init(b_vfull, 1);
+    mbar_init(b_kempty, 1);
+    mbar_init(b_vempty, 1);
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 4);
+    mbar_init(b_pfull, 4);
+    mbar_init(b_pvdone, 1);
+    fence_mbar_init();
+  }
+  // Q tile: row r = (member r / g, query head h*g + r % g); rows past the
+  // tile's members are zero.
+  if (warp < 4) {
+    const int r = tid;
+    const int mi = r / p.g;
+    uint4 chunk[8];
+    if (mi < mcount) {
+      const int b = p.member_ids[mbeg + mi];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(b) * p.H_q + h * p.g + r % p.g) * kHD);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) chunk[c] = src[c];
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) chunk[c] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(smem + kOffQ + sw128_off(r, c)) = chunk[c];
+    fence_async_smem();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
+      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
+        mbar_arrive_expect_tx(bar, kBN * kHD * 2);
+        for (int i = 0; i < kPagesPerTile; ++i) {
+          const int pi = j * kPagesPerTile + i;
+          int row = oob;
+          if (pi < n_pages) {
+            const int page = p.prefix_pages[pp0 + pi];
+            row = (page >= 0 && page < p.num_pages) ? page * kPS : oob;
+            if (!(page >= 0 && page < p.num_pages)) set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
+          }
+          tma_load_3d(dst + i * (kPS * 128), map, 0, h, row, bar);
+        }
+      };
+      for (int j = 0; j < n_kt && ok; ++j) {
+        if (j > 0 && !mbar_wait(b_kempty, (j - 1) & 1)) ok = false;
+        if (ok) load_tile(&kmap, sK, b_kfull, j);
+        if (ok && j > 0 && !mbar_wait(b_vempty, (j - 1) & 1)) ok = false;
+        if (ok) load_tile(&vmap, sV, b_vfull, j);
+      }
+      if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iS = idesc_bf16(kBM, kBN, 0);
+      constexpr uint32_t iO = idesc_bf16(kBM, kHD, 1);
+      auto issue_s = [&](int j) {
+        if (!mbar_wait(b_kfull, j & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kHD / 16; ++ks)
+          mma_bf16(tmem, desc_sw128(sQ + ks * 32), desc_sw128(sK + ks * 32), iS, ks > 0);
+        mma_commit(b_sfull);
+        mma_commit(b_kempty);
+        return true;
+      };
+      ok = n_kt > 0 ? issue_s(0) : true;
+      for (int j = 0; j < n_kt && ok; ++j) {
+        // S(j + 1) once the softmax has read S(j)
+        if (j + 1 < n_kt) {
+          ok = mbar_wait(b_sfree, j & 1) && issue_s(j + 1);
+          if (!ok) break;
+        }
+        ok = mbar_wait(b_pfull, j & 1) && mbar_wait(b_vfull, j & 1);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_bf16(tmem + kTmemO, desc_sw128(sP + (ks >> 2) * 16384 + (ks & 3) * 32),
+                   desc_sw128(sV + ks * 2048), iO, (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(b_pvdone);
+        mma_commit(b_vempty);
+      }
+      if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ---------------- softmax warps: thread = query row ----------------
+    const int r = tid;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_kt && ok; ++j) {
+      ok = mbar_wait(b_sfull, j & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float s[kBN];
+#pragma unroll
+      for (int c0 = 0; c0 < kBN; c0 += 16) {
+        uint32_t u[16];
+        tmem_ld16(trow + c0, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x) s[c0 + x] = __uint_as_float(u[x]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sfree);
+      const int key0 = j * kBN;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        s[c] = key0 + c < plen ? s[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      // the previous PV must be done before P and O are touched
+      if (j > 0) {
+        ok = mbar_wait(b_pvdone, (j - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const bool need = mx > m + kSlack;
+      if (j == 0) {
+        m = mx;
+      } else if (__any_sync(0xffffffffu, need)) {
+        const float mnew = fmaxf(m, mx);
+        const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
+        m = mnew;
+        l *= alpha;
+#pragma unroll
+        for (int c0 = 0; c0 < kHD; c0 += 16) {
+          uint32_t u[16];
+          tmem_ld16(trow + kTmemO + c0, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+          tmem_st16(trow + kTmemO + c0, u);
+        }
+        tmem_wait_st();
+      }
+      const float ms = m == -INFINITY ? 0.f : m;
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 8) {
+        float e[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          e[x] = fast_exp2(s[c + x] - ms);
+          ls += e[x];
+        }
+        uint4 pk;
+        pk.x = float2_to_bf16x2(e[0], e[1]);
+        pk.y = float2_to_bf16x2(e[2], e[3]);
+        pk.z = float2_to_bf16x2(e[4], e[5]);
+        pk.w = float2_to_bf16x2(e[6], e[7]);
+        *reinterpret_cast<uint4*>(smem + kOffP + (c >> 6) * 16384 + sw128_off(r, (c & 63) >> 3)) = pk;
+      }
+      l += ls;
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pfull);
+    }
+    // epilogue: O row / l, LSE (an empty prefix gives O = 0, LSE = -inf)
+    if (ok && n_kt == 0) {
+      const int mi = r / p.g;
+      if (mi < mcount) {
+        const int64_t row = static_cast<int64_t>(p.member_ids[mbeg + mi]) * p.H_q + h * p.g + r % p.g;
+        for (int c = 0; c < kHD; ++c) p.prefix_o[row * kHD + c] = 0.f;
+        p.prefix_lse[row] = -INFINITY;
+      }
+    }
+    if (ok && n_kt > 0) {
+      ok = mbar_wait(b_pvdone, (n_kt - 1) & 1);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const int mi = r / p.g;
+        const bool valid = mi < mcount;
+        const int b = valid ? p.member_ids[mbeg + mi] : 0;
+        const int64_t row = static_cast<int64_t>(b) * p.H_q + h * p.g + r % p.g;
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < kHD; c0 += 16) {
+          uint32_t u[16];
+          tmem_ld16(trow + kTmemO + c0, u);
+          tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.prefix_o + row * kHD + c0);
+#pragma unroll
+            for (int x = 0; x < 16; x += 4)
+              dst[x / 4] = make_float4(__uint_as_float(u[x]) * inv, __uint_as_float(u[x + 1]) * inv,
+                                       __uint_as_float(u[x + 2]) * inv, __uint_as_float(u[x + 3]) * inv);
+          }
+        }
+        if (valid) p.prefix_lse[row] = l > 0.f ? (m + log2f(l)) * kLn2C : -INFINITY;
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// --- host ------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a pool [P * page_size rows][H_kv][64] bf16 with a box of one
+// page of one kv head (16 rows x 128 B), 128-byte swizzle, zero fill.
+ts_status make_page_map(CUtensorMap* map, const void* pool, int num_pages, int H_kv) {
+  auto fn = encode_fn();
+  if (!fn) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(H_kv),
+                        static_cast<cuuint64_t>(num_pages) * kPS};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(H_kv) * kHD * 2};
+  cuuint32_t box[3] = {kHD, 1, kPS};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return TS_OK;
+}
+
+struct CascadeWs {
+  size_t paged, tile_offset, prefix_o, prefix_lse, total;
+};
+
+CascadeWs cascade_layout(int B, int H_q, int D) {
+  CascadeWs w;
+  w.paged = 0;
+  size_t off = align_up(paged_decode_workspace_bytes(B, H_q, D), kWorkspaceAlign);
+  w.tile_offset = off;
+  off = align_up(off + (static_cast<size_t>(B) + 2) * sizeof(int32_t), kWorkspaceAlign);
+  w.prefix_o = off;
+  off = align_up(off + static_cast<size_t>(B) * H_q * D * sizeof(float), kWorkspaceAlign);
+  w.prefix_lse = off;
+  off = align_up(off + static_cast<size_t>(B) * H_q * sizeof(float), kWorkspaceAlign);
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+}  // namespace ts
+
+extern "C" size_t ts_cascade_decode_workspace_size(int32_t B, int32_t H_q, int32_t D) {
+  if (B < 0 || H_q <= 0 || D <= 0 || ts::paged_decode_workspace_bytes(B, H_q, D) == 0) return 0;
+  return ts::cascade_layout(B, H_q, D).total;
+}
+
+extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                            const ts_prefix_groups* groups,
+                                            const int32_t* block_table, int32_t bt_stride,
+                                            const int32_t* seq_lens, int32_t B, int32_t H_q,
+                                            int32_t H_kv, int32_t D, int32_t page_size,
+                                            int32_t num_pages, float scale, ts_dtype dtype,
+                                            void* out, float* lse, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  using namespace ts;
+  const char* who = "ts_cascade_decode_attn";
+  if (!groups) return fail(TS_ERR_INVALID_ARG, "%s: null groups", who);
+  if (B == 0) return TS_OK;
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d)", who, B, H_q, H_kv);
+  const int g = H_q / H_kv;
+  if (dtype != TS_BF16 || D != kHD || page_size != kPS || (g != 1 && g != 2 && g != 4 && g != 8))
+    return fail(TS_ERR_UNSUPPORTED, "%s: needs bf16, D=64, page_size=16, H_q/H_kv in {1,2,4,8}", who);
+  const int G = groups->num_groups;
+  if (G < 0 || G > B) return fail(TS_ERR_INVALID_ARG, "%s: num_groups=%d", who, G);
+  if (!groups->group_of || (G > 0 && (!groups->prefix_indptr || !groups->prefix_pages ||
+                                      !groups->prefix_len || !groups->member_indptr ||
+                                      !groups->member_ids)))
+    return fail(TS_ERR_INVALID_ARG, "%s: null group array", who);
+  if (!q || !k_pool || !v_pool || !out || !block_table || !seq_lens)
+    return fail(TS_ERR_INVALID_ARG, "%s: null pointer", who);
+  for (const void* ptr : {q, k_pool, v_pool})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+      return fail(TS_ERR_INVALID_ARG, "%s: q and pools must be 16-byte aligned", who);
+  const size_t need = ts_cascade_decode_workspace_size(B, H_q, D);
+  if (need == 0) return fail(TS_ERR_CUDA, "%s: cannot size the workspace", who);
+  if (!workspace || workspace_bytes < need)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace %zu B < %zu B needed", who, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", who);
+  const CascadeWs ws = cascade_layout(B, H_q, D);
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* prefix_o = reinterpret_cast<float*>(wsb + ws.prefix_o);
+  float* prefix_lse = reinterpret_cast<float*>(wsb + ws.prefix_lse);
+
+  if (G > 0) {
+    int32_t* tile_offset = reinterpret_cast<int32_t*>(wsb + ws.tile_offset);
+    const int mpt = kBM / g;
+    cascade_plan_kernel<<<1, 1024, 0, s>>>(groups->member_indptr, G, mpt, tile_offset);
+    ts_status st = cuda_check(cudaGetLastError(), "cascade plan launch");
+    if (st != TS_OK) return st;
+    CUtensorMap kmap, vmap;
+    st = make_page_map(&kmap, k_pool, num_pages, H_kv);
+    if (st != TS_OK) return st;
+    st = make_page_map(&vmap, v_pool, num_pages, H_kv);
+    if (st != TS_OK) return st;
+    PrefixParams pp;
+    pp.q = static_cast<const __nv_bfloat16*>(q);
+    pp.prefix_indptr = groups->prefix_indptr;
+    pp.prefix_pages = groups->prefix_pages;
+    pp.prefix_len = groups->prefix_len;
+    pp.member_indptr = groups->member_indptr;
+    pp.member_ids = groups->member_ids;
+    pp.tile_offset = tile_offset;
+    pp.num_groups = G;
+    pp.H_q = H_q;
+    pp.H_kv = H_kv;
+    pp.g = g;
+    pp.mpt = mpt;
+    pp.num_pages = num_pages;
+    pp.scale_log2 = scale * kLog2eC;
+    pp.prefix_o = prefix_o;
+    pp.prefix_lse = prefix_lse;
+    pp.err_word = reinterpret_cast<uint32_t*>(wsb);
+    st = cuda_check(cudaFuncSetAttribute(cascade_prefix_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
+                    "prefix smem attribute");
+    if (st != TS_OK) return st;
+    // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
+    const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);
+    cascade_prefix_kernel<<<dim3(tiles, H_kv), kThreadsPfx, kSmemPfx, s>>>(pp, kmap, vmap);
+    st = cuda_check(cudaGetLastError(), "cascade prefix launch");
+    if (st != TS_OK) return st;
+  }
+  PrefixInputs pre;
+  pre.group_of = groups->group_of;
+  pre.prefix_len = groups->prefix_len;
+  pre.prefix_o = prefix_o;
+  pre.prefix_lse = prefix_lse;
+  return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q,
+                                  H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
+                                  ws.tile_offset, s, who, G > 0 ? &pre : nullptr);
+}

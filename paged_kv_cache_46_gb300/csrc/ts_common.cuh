@@ -23,6 +23,24 @@ int device_sm_count();
 int current_device();
 
 constexpr size_t kWorkspaceAlign = 256;
+
+// Shared-prefix state handed to the paged kernel in cascade mode (device pointers).
+struct PrefixInputs {
+  const int32_t* group_of;    // [B] group or -1
+  const int32_t* prefix_len;  // [groups] shared tokens (whole pages)
+  const float* prefix_o;      // [B, H_q, D] normalised prefix output (fp32)
+  const float* prefix_lse;    // [B, H_q] prefix LSE (natural log)
+};
+
+// Paged split-KV decode (ts_paged_decode.cu); `pre` selects cascade mode.
+ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                   int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                   ts_dtype dtype, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream, const char* who,
+                                   const PrefixInputs* pre);
+size_t paged_decode_workspace_bytes(int B, int H_q, int D);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------

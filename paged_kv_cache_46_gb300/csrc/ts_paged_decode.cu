@@ -88,6 +88,12 @@ struct PagedParams {
   int2* split_info;  // per sequence: {first CTA, (parts << 1) | slot of first part}
   float* part_o;     // [2 * gridDim.x, H_q, D]
   float* part_lse;   // [2 * gridDim.x, H_q]
+  // Shared-prefix (cascade) mode: a grouped sequence's own pages start after
+  // its group's prefix pages, and the prefix attention state is merged in.
+  const int32_t* group_of;    // [B] group or -1
+  const int32_t* prefix_len;  // [groups] shared tokens (whole pages)
+  const float* prefix_o;      // [B, H_q, D] normalised prefix output (fp32)
+  const float* prefix_lse;    // [B, H_q] prefix LSE (natural log)
   int32_t num_stages;
   uint32_t stage_bytes;  // bytes per stage (K rows + V rows + q rows, aligned)
   uint32_t stages_off;   // offset of the first stage in dynamic shared memory
@@ -144,17 +150,33 @@ struct Cfg {
   static_assert(kTPG >= 1, "tokens per group");
 };
 
-// Writes O = 0, LSE = -inf for a sequence with no tokens.
-template <typename T>
+// Tokens of sequence b covered by its group's shared prefix (prefix mode).
+template <bool kPfx>
+__device__ __forceinline__ int prefix_tokens(const PagedParams& p, int b) {
+  if constexpr (kPfx) {
+    const int g = p.group_of[b];
+    return g >= 0 ? p.prefix_len[g] : 0;
+  } else {
+    return 0;
+  }
+}
+
+// Writes the output of a sequence with no own tokens: O = 0, LSE = -inf, or
+// the prefix state alone in prefix mode.
+template <typename T, bool kPfx>
 __device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k) {
+  const bool grouped = kPfx && p.group_of[b] >= 0;
   T* out = static_cast<T*>(p.out) + static_cast<int64_t>(b) * p.H_q * D;
-  for (int i = 0; i < p.H_q * D; ++i) out[i] = static_cast<T>(0.0f);
+  const float* po = grouped ? p.prefix_o + static_cast<int64_t>(b) * p.H_q * D : nullptr;
+  for (int i = 0; i < p.H_q * D; ++i) out[i] = static_cast<T>(grouped ? po[i] : 0.0f);
   if (p.lse)
-    for (int h = 0; h < p.H_q; ++h) p.lse[static_cast<int64_t>(b) * p.H_q + h] = -INFINITY;
+    for (int h = 0; h < p.H_q; ++h)
+      p.lse[static_cast<int64_t>(b) * p.H_q + h] =
+          grouped ? p.prefix_lse[static_cast<int64_t>(b) * p.H_q + h] : -INFINITY;
   p.split_info[b] = make_int2(k, 0);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kPfx>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedParams p) {
   using C = Cfg<T, D, G>;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -196,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
   long long mine = 0;
   for (int b = lo; b < hi; ++b) {
-    const int L = p.seq_lens[b];
+    const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
     if (L > 0)
       mine += (L + ps - 1) / ps;
     else if (b % G_ctas == k)
-      write_empty_sequence<T>(p, D, b, k);
+      write_empty_sequence<T, kPfx>(p, D, b, k);
   }
   long long incl = mine;
 #pragma unroll
@@ -226,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
     for (int b = lo; b < hi; ++b) {
-      const int L = p.seq_lens[b];
+      const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
       const long long np = L > 0 ? (L + ps - 1) / ps : 0;
       if (start < off + np) {
         s_start[0] = b;
@@ -251,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       int pg = s_start[1];
       bool first_seg = true;
       while (g < end && !aborted && b < B) {
-        const int L = max(p.seq_lens[b], 0);
+        const int pre = prefix_tokens<kPfx>(p, b);
+        const int L = max(p.seq_lens[b] - pre, 0);
         const int np = (L + ps - 1) / ps;
         if (np == 0 || pg >= np) {
           ++b;
@@ -269,12 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
           const int nparts = k1 - k + 1;
           p.split_info[b] = make_int2(k, (nparts << 1) | (first_seg ? 0 : 1));
         }
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride + pg;
+        const int pre_pages = pre / ps;  // prefix pages come first in the row
+        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride + pre_pages + pg;
         for (int base = 0; base < n_here && !aborted; base += 32) {
           const int cnt = min(32, n_here - base);
           // entries past the row (length inconsistent with bt_stride) count as bad pages
           int pid = -1;
-          if (lane < cnt && pg + base + lane < p.bt_stride) pid = bt_row[base + lane];
+          if (lane < cnt && pre_pages + pg + base + lane < p.bt_stride) pid = bt_row[base + lane];
           for (int i = 0; i < cnt; ++i) {
             const int page = __shfl_sync(0xffffffffu, pid, i);
             const int pidx = pg + base + i;
@@ -534,10 +558,34 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         for (int hh = 0; hh < G; ++hh) {
           const int hq = h * G + hh;
           const float ls = lsum[hh];
-          const float inv = ls > 0.f ? 1.0f / ls : 0.f;
-          const float lse2 = ls > 0.f ? m[hh] + log2f(ls) : -INFINITY;
+          float inv = ls > 0.f ? 1.0f / ls : 0.f;
+          float lse2 = ls > 0.f ? m[hh] + log2f(ls) : -INFINITY;
           if (d.out_slot < 0) {
             T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(d.b) * p.H_q + hq) * D;
+            if constexpr (kPfx) {
+              if (p.group_of[d.b] >= 0) {
+                // merge the shared-prefix state: weights by LSE (log2 domain)
+                const int64_t row = static_cast<int64_t>(d.b) * p.H_q + hq;
+                const float lp2 = p.prefix_lse[row] * kLog2e;
+                const float M = fmaxf(lse2, lp2);
+                const float ws = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - M);
+                const float wp = lp2 == -INFINITY ? 0.f : fast_exp2(lp2 - M);
+                const float den = ws + wp;
+                const float cs = den > 0.f ? inv * ws / den : 0.f;
+                const float cp = den > 0.f ? wp / den : 0.f;
+                const float* po = p.prefix_o + row * D;
+#pragma unroll
+                for (int v = 0; v < C::kNV; ++v)
+#pragma unroll
+                  for (int w = 0; w < Elem<T>::kPairs; ++w) {
+                    const float2 pv2 = *reinterpret_cast<const float2*>(po + dim_off[v] + 2 * w);
+                    float2& a = acc[hh][v * Elem<T>::kPairs + w];
+                    a = make_float2(a.x * cs + pv2.x * cp, a.y * cs + pv2.y * cp);
+                  }
+                inv = 1.0f;  // the merged rows are already normalised
+                lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
+              }
+            }
 #pragma unroll
             for (int v = 0; v < C::kNV; ++v) {
               if constexpr (sizeof(T) == 2) {
@@ -581,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 // Reduces the partial states of sequences cut across CTAs (one warp per
 // (sequence, query head)); sequences written whole by the main kernel are
 // skipped.
-template <typename T>
+// In prefix mode a grouped sequence's shared-prefix state is one more part.
+template <typename T, bool kPfx>
 __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, int D) {
   pdl_wait_primary();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -592,7 +641,10 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
   const int nparts = info.y >> 1;
   if (nparts <= 1) return;
   const int k0 = info.x, slot0 = info.y & 1;
-  float mx = -INFINITY;
+  const int64_t row = static_cast<int64_t>(b) * p.H_q + hq;
+  const bool grouped = kPfx && p.group_of[b] >= 0;
+  const float lse_pre = grouped ? p.prefix_lse[row] : -INFINITY;
+  float mx = lse_pre;
   for (int i = 0; i < nparts; ++i) {
     const int slot = i == 0 ? 2 * k0 + slot0 : 2 * (k0 + i);
     mx = fmaxf(mx, p.part_lse[static_cast<int64_t>(slot) * p.H_q + hq]);
@@ -613,6 +665,15 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
       a.w += w * o.w;
       wsum += w;
     }
+    if (grouped && lse_pre != -INFINITY) {
+      const float w = __expf(lse_pre - ms);
+      const float4 o = *reinterpret_cast<const float4*>(p.prefix_o + row * D + d0);
+      a.x += w * o.x;
+      a.y += w * o.y;
+      a.z += w * o.z;
+      a.w += w * o.w;
+      wsum += w;
+    }
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
     T* out = static_cast<T*>(p.out) + (static_cast<int64_t>(b) * p.H_q + hq) * D + d0;
     if constexpr (sizeof(T) == 2) {
@@ -624,37 +685,30 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
       *reinterpret_cast<float4*>(out) = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
   }
-  if (lane == 0 && p.lse) {
-    if (wsum == 0.f) {
-      for (int i = 0; i < nparts; ++i) {
-        const int slot = i == 0 ? 2 * k0 + slot0 : 2 * (k0 + i);
-        wsum += __expf(p.part_lse[static_cast<int64_t>(slot) * p.H_q + hq] - ms);
-      }
-    }
-    p.lse[static_cast<int64_t>(b) * p.H_q + hq] = wsum > 0.f ? ms + logf(wsum) : -INFINITY;
-  }
+  if (lane == 0 && p.lse) p.lse[row] = wsum > 0.f ? ms + logf(wsum) : -INFINITY;
 }
 
 using KernelFn = void (*)(const PagedParams);
 
-template <typename T, int D>
+template <typename T, int D, bool kPfx>
 KernelFn pick_g(int g) {
   switch (g) {
-    case 1: return paged_decode_kernel<T, D, 1>;
-    case 2: return paged_decode_kernel<T, D, 2>;
-    case 4: return paged_decode_kernel<T, D, 4>;
-    case 8: return paged_decode_kernel<T, D, 8>;
+    case 1: return paged_decode_kernel<T, D, 1, kPfx>;
+    case 2: return paged_decode_kernel<T, D, 2, kPfx>;
+    case 4: return paged_decode_kernel<T, D, 4, kPfx>;
+    case 8: return paged_decode_kernel<T, D, 8, kPfx>;
     default: return nullptr;
   }
 }
 
-KernelFn pick_kernel(ts_dtype dt, int D, int g) {
+// The prefix (cascade) variants exist for bf16 only.
+KernelFn pick_kernel(ts_dtype dt, int D, int g, bool prefix) {
   if (dt == TS_BF16) {
-    if (D == 64) return pick_g<__nv_bfloat16, 64>(g);
-    if (D == 128) return pick_g<__nv_bfloat16, 128>(g);
-  } else {
-    if (D == 64) return pick_g<float, 64>(g);
-    if (D == 128) return pick_g<float, 128>(g);
+    if (D == 64) return prefix ? pick_g<__nv_bfloat16, 64, true>(g) : pick_g<__nv_bfloat16, 64, false>(g);
+    if (D == 128) return prefix ? pick_g<__nv_bfloat16, 128, true>(g) : pick_g<__nv_bfloat16, 128, false>(g);
+  } else if (!prefix) {
+    if (D == 64) return pick_g<float, 64, false>(g);
+    if (D == 128) return pick_g<float, 128, false>(g);
   }
   return nullptr;
 }
@@ -690,13 +744,15 @@ WsLayout workspace_layout(int B, int H_q, int D, int n_ctas) {
 
 }  // namespace
 
-// Shared with the cascade path: launches the paged split-KV kernel pair.
-ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_pool,
-                              const int32_t* block_table, int32_t bt_stride,
-                              const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
-                              int32_t D, int32_t page_size, int32_t num_pages, float scale,
-                              ts_dtype dtype, void* out, float* lse, void* workspace,
-                              size_t workspace_bytes, cudaStream_t stream, const char* who) {
+// Launches the paged split-KV kernel pair; `pre` non-null selects prefix
+// (cascade) mode.
+ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                   int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                   ts_dtype dtype, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream, const char* who,
+                                   const PrefixInputs* pre) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
       bt_stride <= 0)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
@@ -714,7 +770,7 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
     return fail(TS_ERR_UNSUPPORTED, "%s: H_kv=%d (supported 1, 2, 4, 8)", who, H_kv);
   if (page_size != 8 && page_size != 16 && page_size != 32)
     return fail(TS_ERR_UNSUPPORTED, "%s: page_size=%d (supported 8, 16, 32)", who, page_size);
-  KernelFn fn = pick_kernel(dtype, D, g);
+  KernelFn fn = pick_kernel(dtype, D, g, pre != nullptr);
   if (!fn)
     return fail(TS_ERR_UNSUPPORTED, "%s: D=%d, group size %d (supported D 64/128, g 1/2/4/8)", who,
                 D, g);
@@ -746,6 +802,10 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
   prm.scale_log2 = scale * kLog2e;
   prm.out = out;
   prm.lse = lse;
+  prm.group_of = pre ? pre->group_of : nullptr;
+  prm.prefix_len = pre ? pre->prefix_len : nullptr;
+  prm.prefix_o = pre ? pre->prefix_o : nullptr;
+  prm.prefix_lse = pre ? pre->prefix_lse : nullptr;
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   prm.err_word = reinterpret_cast<uint32_t*>(wsb);
   prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
@@ -815,12 +875,26 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
   if (dtype == TS_BF16)
-    st = cuda_check(cudaLaunchKernelEx(&mcfg, split_merge_kernel<__nv_bfloat16>, prm, D),
+    st = cuda_check(cudaLaunchKernelEx(&mcfg,
+                                       pre ? split_merge_kernel<__nv_bfloat16, true>
+                                           : split_merge_kernel<__nv_bfloat16, false>,
+                                       prm, D),
                     "split merge launch");
   else
-    st = cuda_check(cudaLaunchKernelEx(&mcfg, split_merge_kernel<float>, prm, D),
+    st = cuda_check(cudaLaunchKernelEx(&mcfg, split_merge_kernel<float, false>, prm, D),
                     "split merge launch");
   return st;
+}
+
+ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_table, int32_t bt_stride,
+                              const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                              int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                              ts_dtype dtype, void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream, const char* who) {
+  return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q,
+                                  H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
+                                  workspace_bytes, stream, who, nullptr);
 }
 
 size_t paged_decode_workspace_bytes(int B, int H_q, int D) {

@@ -2,14 +2,6 @@
 // report TS_ERR_UNSUPPORTED so callers fail loudly instead of silently.
 #include "ts_common.cuh"
 
-extern "C" size_t ts_cascade_decode_workspace_size(int32_t, int32_t, int32_t) { return 0; }
-extern "C" ts_status ts_cascade_decode_attn(const void*, const void*, const void*,
-                                            const ts_prefix_groups*, const int32_t*, int32_t,
-                                            const int32_t*, int32_t, int32_t, int32_t, int32_t,
-                                            int32_t, int32_t, float, ts_dtype, void*, float*,
-                                            void*, size_t, void*) {
-  return ts::fail(TS_ERR_UNSUPPORTED, "ts_cascade_decode_attn: not built yet");
-}
 extern "C" size_t ts_mla_workspace_size(int32_t, int32_t, int32_t) { return 0; }
 extern "C" ts_status ts_mla_paged_decode(const void*, const void*, const int32_t*, int32_t,
                                          const int32_t*, int32_t, int32_t, int32_t, int32_t,
