@@ -54,3 +54,10 @@ def oracle_decode(case: workloads.PagedCase, seq_idx=None, k_pool=None, v_pool=N
         kp, vp = oracle.kv_append(kp, vp, v["k_new"], v["v_new"], v["block_table"], v["positions"],
                                   case.page_size)
     return oracle.decode_attention(v["q"], kp, vp, v["block_table"], v["seq_lens"], case.scale)
+
+
+def oracle_mla(case: workloads.PagedCase, seq_idx=None):
+    """Oracle O/LSE of an absorbed-MLA case for sequences ``seq_idx``."""
+    v = workloads.oracle_view(case, seq_idx)
+    return oracle.mla_decode_attention(v["q"], v["k_pool"], v["block_table"], v["seq_lens"], case.scale,
+                                       case.Dv)
