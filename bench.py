@@ -56,20 +56,15 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths"], default="llama3_8b_layer")
+    ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla"],
+                    default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run for ncu: one pool copy, no e2e / CPU baseline / clock sampling")
+    ap.add_argument("--batch-scale", type=float, default=1.0,
+                    help="scale the batch (sequences / groups) down for small profiling captures")
     return ap.parse_args()
-
-
-def build_workload(name: str, device):
-    if name == "llama3_8b_layer":
-        return workloads.llama3_8b_layer(device=device)
-    if name == "mixed_lengths":
-        return workloads.mixed_lengths(device=device)
-    raise ValueError(name)
 
 
 # --------------------------------------------------------------------------
@@ -190,11 +185,52 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 
 # --------------------------------------------------------------------------
-# CPU oracle (baseline / reference arm)
+# Workloads: algorithmic bytes / flops, device steps, CPU oracle samples
 # --------------------------------------------------------------------------
+
+def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
+    """The named workload at full size (or a small instance with the same
+    per-sequence distributions, for CPU-side oracle timing; `scale` shrinks the
+    batch for profiling captures)."""
+    def n(full):
+        return max(1, int(round(full * scale)))
+    if name == "llama3_8b_layer":
+        return workloads.llama3_8b_layer(device=device, B=8 if small else n(64))
+    if name == "mixed_lengths":
+        return workloads.mixed_lengths(device=device, repeat=2 if small else n(32))
+    if name == "cascade":
+        return workloads.shared_prefix_cascade(device=device, groups=1 if small else n(16),
+                                               members=32 if small else 1024)
+    if name == "mla":
+        return workloads.absorbed_mla(device=device, B=2 if small else n(64))
+    raise ValueError(name)
+
+
+def algorithmic(case, groups=None):
+    """(bytes, tensor flops) one decode pass must move / compute.
+
+    Paged GQA: every attended token's K and V rows once. Cascade: each group's
+    prefix once plus every sequence's own rows. MLA: every latent row once;
+    flops of Q.C^T over 576 dims and P.V over 512."""
+    es = 2 if case.dtype == "bf16" else 4
+    tokens = int(case.attn_lens.astype(np.int64).sum())
+    if case.mla:
+        return tokens * case.D * es, tokens * case.H_q * (case.D + case.Dv) * 2
+    row = case.H_kv * (case.D + case.Dv) * es
+    if groups is not None and groups["num_groups"] > 0:
+        prefix_tokens = int(groups["prefix_len"].astype(np.int64).sum())
+        members = np.diff(groups["member_indptr"])
+        shared = int((groups["prefix_len"].astype(np.int64) * members).sum())
+        flops = 4 * int((groups["prefix_len"].astype(np.int64) * members).sum()) * case.H_q * case.D
+        return (tokens - shared + prefix_tokens) * row, flops
+    return tokens * row, 0
+
 
 def oracle_pass(view, case):
     import oracle
+    if case.mla:
+        return oracle.mla_decode_attention(view["q"], view["k_pool"], view["block_table"], view["seq_lens"],
+                                           case.scale, case.Dv)
     kp, vp = view["k_pool"], view["v_pool"]
     if case.append:
         kp, vp = oracle.kv_append(kp, vp, view["k_new"], view["v_new"], view["block_table"],
@@ -203,43 +239,53 @@ def oracle_pass(view, case):
 
 
 def sample_bytes(case, idx):
-    esize = 4 if case.dtype == "f32" else 2
-    return int(case.attn_lens[idx].astype(np.int64).sum()) * case.H_kv * (case.D + case.Dv) * esize
+    """Flat (ungrouped) algorithmic bytes of the sampled sequences."""
+    es = 4 if case.dtype == "f32" else 2
+    tokens = int(case.attn_lens[idx].astype(np.int64).sum())
+    if case.mla:
+        return tokens * case.D * es
+    return tokens * case.H_kv * (case.D + case.Dv) * es
 
 
-def cpu_baseline(case, budget_s: float = 12.0):
-    """The oracle on the full batch, repeated until ~budget_s of CPU time."""
-    view = workloads.oracle_view(case)
-    idx = np.arange(case.B)
-    nbytes = sample_bytes(case, idx)
+def time_oracle(case, idx, budget_s: float):
+    """Seconds per oracle pass over sequences idx (repeated up to budget_s)."""
+    view = workloads.oracle_view(case, idx)
     reps, t_total = 0, 0.0
-    while t_total < budget_s and reps < 1000:
+    while (t_total < budget_s or reps == 0) and reps < 1000:
         t = time.perf_counter()
         oracle_pass(view, case)
         t_total += time.perf_counter() - t
         reps += 1
-    sec = t_total / reps
+    return t_total / reps, reps
+
+
+def cpu_baseline(case, budget_s: float = 12.0):
+    """The oracle (fp64 numpy, one BLAS thread) on a bounded sample of the workload."""
+    t1, _ = time_oracle(case, [int(np.argmin(case.attn_lens))], 0.0)
+    per_seq_est = max(t1, 1e-4) * case.attn_lens.mean() / max(1, case.attn_lens.min())
+    n = int(max(1, min(case.B, budget_s / 2 / per_seq_est)))
+    idx = workloads.sample_sequences(case, n)[:n] if n < case.B else np.arange(case.B)
+    sec, reps = time_oracle(case, idx, budget_s)
+    nbytes = sample_bytes(case, idx)
     return {"value": nbytes / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"full batch ({case.B} sequences, {int(case.attn_lens.sum())} tokens) x {reps} passes, "
-                      f"fp64 numpy, 1 BLAS thread", "query_tokens_per_s": case.B / sec, "ms_per_pass": sec * 1e3}
+            "sample": f"{len(idx)} of {case.B} sequences ({int(case.attn_lens[idx].sum())} tokens) x {reps} passes, "
+                      f"fp64 numpy, 1 BLAS thread; bytes counted flat (no prefix sharing)",
+            "query_tokens_per_s": len(idx) / sec}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    case = build_workload(args.workload, "cpu")
-    view_all = workloads.oracle_view(case)
+    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla"))
     # size each step's sample so the whole run stays within ~2 minutes
-    t = time.perf_counter()
-    oracle_pass(workloads.oracle_view(case, [0]), case)
-    per_seq = max(time.perf_counter() - t, 1e-4)
+    t1, _ = time_oracle(case, [0], 0.0)
+    per_seq = max(t1, 1e-4)
     n_seq = int(max(1, min(case.B, 120.0 / max(1, args.steps + args.warmup) / per_seq)))
     views = []
     for s in range(min(case.B, 8)):
         idx = (np.arange(n_seq) + s * n_seq) % case.B
         views.append((idx, workloads.oracle_view(case, idx)))
-    del view_all
     for i in range(args.warmup):
         oracle_pass(views[i % len(views)][1], case)
     total_bytes, t0 = 0, time.perf_counter()
@@ -268,6 +314,69 @@ def run_reference(args):
 # GPU arm
 # --------------------------------------------------------------------------
 
+class DeviceStep:
+    """One decode pass of a workload on the device, through the C ABI."""
+
+    def __init__(self, ts, case, dev, rotate: int):
+        self.ts, self.case, self.dev = ts, case, dev
+        c = case
+        self.bt = torch.from_numpy(c.block_table).to(dev)
+        self.lens = torch.from_numpy(c.attn_lens).to(dev)
+        self.pos = torch.from_numpy(c.positions).to(dev)
+        self.out = torch.empty(c.B, c.H_q, c.Dv, dtype=c.q.dtype, device=dev)
+        self.lse = torch.empty(c.B, c.H_q, dtype=torch.float32, device=dev)
+        pools = [(c.k_pool, c.v_pool)]
+        for _ in range(rotate - 1):
+            pools.append((c.k_pool.clone(), c.v_pool.clone() if c.v_pool is not None else None))
+        self.pools = pools
+        self.groups = None
+        self.gdev = None
+        if c.name.startswith("cascade"):
+            t = time.perf_counter()
+            self.groups = ts.ts_group_prefixes(c.block_table, c.seq_lens, c.page_size, 2)
+            self.group_ms = (time.perf_counter() - t) * 1e3
+            self.gdev = ts.groups_to_device(self.groups, dev)
+            ws_bytes = ts.ts_cascade_decode_workspace_size(c.B, c.H_q, c.D)
+            self.launches = 4  # plan, prefix, paged suffix, split merge
+        elif c.mla:
+            ws_bytes = ts.ts_mla_workspace_size(c.B, c.H_q, c.Dv)
+            self.launches = 2
+        else:
+            ws_bytes = ts.ts_paged_decode_workspace_size(c.B, c.H_q, c.D)
+            self.launches = 2 + (1 if c.append else 0)
+        self.ws = ts.new_workspace(ws_bytes, dev)
+
+    def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None):
+        ts, c = self.ts, self.case
+        kp, vp = self.pools[i % len(self.pools)]
+        q = c.q if q is None else q
+        bt = self.bt if bt is None else bt
+        lens = self.lens if lens is None else lens
+        if self.groups is not None:
+            ts.ts_cascade_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=self.out, lse=self.lse,
+                                      workspace=self.ws, stream=stream)
+        elif c.mla:
+            ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=self.out, lse=self.lse,
+                                   workspace=self.ws, stream=stream)
+        else:
+            ts.ts_paged_decode_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse, workspace=self.ws,
+                                    stream=stream)
+
+    def step(self, i, ev=None, stream=None, inputs=None):
+        ts, c = self.ts, self.case
+        kp, vp = self.pools[i % len(self.pools)]
+        inputs = inputs or {}
+        if c.append:
+            ts.ts_kv_append(inputs.get("k_new", c.k_new), inputs.get("v_new", c.v_new), kp, vp,
+                            inputs.get("bt", self.bt), inputs.get("pos", self.pos), stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        self.attention(i, q=inputs.get("q"), bt=inputs.get("bt"), lens=inputs.get("lens"), stream=stream,
+                       gdev=inputs.get("gdev"))
+        if ev is not None:
+            ev[1].record(stream)
+
+
 def run_ours(args):
     rank, world, local, dist = dist_setup(args.gpus)
     import paged_kv_cache_46_gb300 as ts
@@ -279,36 +388,20 @@ def run_ours(args):
         ts_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    case = build_workload(args.workload, dev)
-    bt = torch.from_numpy(case.block_table).to(dev)
-    lens = torch.from_numpy(case.attn_lens).to(dev)
-    pos = torch.from_numpy(case.positions).to(dev)
-    # second copy of the pools: consecutive steps read different memory
+    case = build_workload(args.workload, dev, scale=args.batch_scale)
     if args.profile:
         args.no_e2e = args.no_cpu_baseline = True
-        pools = [(case.k_pool, case.v_pool)] * 2
-    else:
-        pools = [(case.k_pool, case.v_pool), (case.k_pool.clone(), case.v_pool.clone())]
-    out = torch.empty_like(case.q)
-    lse = torch.empty(case.B, case.H_q, dtype=torch.float32, device=dev)
-    ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D), dev)
+    pool_bytes = case.k_pool.numel() * case.k_pool.element_size() * (2 if case.v_pool is not None else 1)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    rotate = 1 if args.profile else max(2, int(math.ceil(4 * l2 / pool_bytes)) if pool_bytes < 4 * l2 else 2)
+    if pool_bytes > 2 * 1e9:
+        rotate = 1  # already many times larger than L2
+    runner = DeviceStep(ts, case, dev, rotate)
     stream = torch.cuda.current_stream()
-    nbytes = case.kv_bytes_read()
-    launches_per_step = 3 if case.append else 2
-
-    def step(i, ev=None):
-        kp, vp = pools[i % 2]
-        if case.append:
-            ts.ts_kv_append(case.k_new, case.v_new, kp, vp, bt, pos, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        ts.ts_paged_decode_attn(case.q, kp, vp, bt, lens, case.scale, out=out, lse=lse, workspace=ws,
-                                stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+    nbytes, flops = algorithmic(case, runner.groups)
 
     for i in range(args.warmup):
-        step(i)
+        runner.step(i, stream=stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
     if args.profile:
@@ -321,89 +414,112 @@ def run_ours(args):
     t_wall0 = time.perf_counter()
     start.record(stream)
     for i in range(args.steps):
-        step(i, evs[i])
+        runner.step(i, evs[i], stream=stream)
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     barrier(dist)
     sampler.stop()
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, dist, dev)
-    ms_step = ms_total / args.steps
+    ms_step = max_over_ranks(start.elapsed_time(end), dist, dev) / args.steps
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    err_word = ts.ts_read_device_error(ws)
+    err_word = ts.ts_read_device_error(runner.ws)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers (pinned): the step's
+    # inputs go up, its output comes back, every step
     e2e = None
     if not args.no_e2e:
-        h_q = case.q.cpu().pin_memory()
-        h_kn = case.k_new.cpu().pin_memory() if case.append else None
-        h_vn = case.v_new.cpu().pin_memory() if case.append else None
-        h_bt = torch.from_numpy(case.block_table).pin_memory()
-        h_lens = torch.from_numpy(case.attn_lens).pin_memory()
-        h_pos = torch.from_numpy(case.positions).pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q, d_kn, d_vn = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new)
-        d_bt, d_lens, d_pos = torch.empty_like(bt), torch.empty_like(lens), torch.empty_like(pos)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_lens, h_pos) if t is not None)
+        hin = {"q": case.q.cpu().pin_memory(), "bt": torch.from_numpy(case.block_table).pin_memory(),
+               "lens": torch.from_numpy(case.attn_lens).pin_memory()}
+        if case.append:
+            hin.update(k_new=case.k_new.cpu().pin_memory(), v_new=case.v_new.cpu().pin_memory(),
+                       pos=torch.from_numpy(case.positions).pin_memory())
+        din = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+        h_out = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hin.values())
         d2h = h_out.numel() * h_out.element_size()
+        host_group_ms = []
 
         def e2e_step(i):
-            kp, vp = pools[i % 2]
-            d_q.copy_(h_q, non_blocking=True)
-            d_bt.copy_(h_bt, non_blocking=True)
-            d_lens.copy_(h_lens, non_blocking=True)
-            if case.append:
-                d_kn.copy_(h_kn, non_blocking=True)
-                d_vn.copy_(h_vn, non_blocking=True)
-                d_pos.copy_(h_pos, non_blocking=True)
-                ts.ts_kv_append(d_kn, d_vn, kp, vp, d_bt, d_pos, stream=stream)
-            ts.ts_paged_decode_attn(d_q, kp, vp, d_bt, d_lens, case.scale, out=out, lse=lse, workspace=ws,
-                                    stream=stream)
-            h_out.copy_(out, non_blocking=True)
+            for k, v in hin.items():
+                din[k].copy_(v, non_blocking=True)
+            inputs = dict(din)
+            if runner.groups is not None:
+                # the user's call sequence: group on the host, upload the groups, attend
+                t = time.perf_counter()
+                g = ts.ts_group_prefixes(case.block_table, case.seq_lens, case.page_size, 2)
+                host_group_ms.append((time.perf_counter() - t) * 1e3)
+                inputs["gdev"] = ts.groups_to_device(g, dev)
+            runner.step(i, stream=stream, inputs=inputs)
+            h_out.copy_(runner.out, non_blocking=True)
 
-        for i in range(args.warmup):
+        n_e2e = min(args.steps, 50) if runner.groups is not None else args.steps
+        for i in range(min(args.warmup, 3)):
             e2e_step(i)
         torch.cuda.synchronize()
         barrier(dist)
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
         s2.record(stream)
-        for i in range(args.steps):
+        for i in range(n_e2e):
             e2e_step(i)
         e2.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(s2.elapsed_time(e2), dist, dev) / args.steps
+        wall_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e_ms = max(max_over_ranks(s2.elapsed_time(e2), dist, dev) / n_e2e, wall_ms)
         e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
                "query_tokens_per_s": world * case.B / (e2e_ms * 1e-3)}
+        if host_group_ms:
+            e2e["host_grouping_ms"] = statistics.median(host_group_ms)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
-    peak, peak_kind = measured_peaks()
+    peaks = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        peaks = json.load(open(path))
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_kind = "measured" if peaks else "fallback"
     achieved = nbytes / (attn_ms * 1e-3) / 1e9
     value = world * nbytes / (ms_step * 1e-3) / 1e9
+    kernel = {"llama3_8b_layer": "ts_paged_decode_attn (split-KV kernel + LSE merge kernel)",
+              "mixed_lengths": "ts_paged_decode_attn (split-KV kernel + LSE merge kernel)",
+              "cascade": "ts_cascade_decode_attn (plan + tcgen05 prefix + paged suffix + merge)",
+              "mla": "ts_mla_paged_decode (2-CTA tcgen05 kernel + merge)"}[args.workload]
+    source = {"cascade": "ts_cascade.cu", "mla": "ts_mla.cu"}.get(args.workload, "ts_paged_decode.cu")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if case.dtype == "bf16" else "f32", "accumulate": "f32",
         "data": "synthetic",
         "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D,
-                   "page_size": case.page_size, "tokens_attended": int(case.attn_lens.sum()),
+                   "Dv": case.Dv, "page_size": case.page_size, "tokens_attended": int(case.attn_lens.sum()),
                    "kv_bytes_per_step": nbytes, "append": case.append, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: two rotated copies of the K/V pool "
-                         f"({2 * case.k_pool.numel() * case.k_pool.element_size() / 1e9:.2f} GB each)"},
+                   "l2": f"inputs larger than L2: {rotate} rotated pool cop{'y' if rotate == 1 else 'ies'} of "
+                         f"{pool_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)"},
         "query_tokens_per_s": world * case.B / (ms_step * 1e-3),
         "hbm_frac_of_8tbs": value / world / 8000.0,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                     "kernel": "ts_paged_decode_attn (split-KV kernel + LSE merge kernel)",
-                     "traffic": kernel_traffic(f"paged_decode_{case.name}.md", "ts_paged_decode.cu")},
-        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "kernel": kernel,
+                     "traffic": kernel_traffic(f"{args.workload}.md", source)},
+        "gpu_launches": runner.launches * args.steps,
         "device_error_word": err_word,
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
+    if flops:
+        tflops = flops / (attn_ms * 1e-3) / 1e12
+        line["tensor"] = {"achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                          "flops_per_step": flops, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                          "note": "whole call's flops over the whole call's time"}
+    if runner.groups is not None:
+        flat = sample_bytes(case, np.arange(case.B))
+        line["config"]["flat_kv_bytes"] = flat
+        line["config"]["groups"] = int(runner.groups["num_groups"])
+        line["flat_equivalent_gbs"] = flat / (ms_step * 1e-3) / 1e9
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline and world == 1:
