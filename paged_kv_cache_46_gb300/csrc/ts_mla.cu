@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kH = 128, kDqk = 576, kDv = 512, kPS = 64, kTok = 64;
 constexpr int kAtomBytes = kTok * 128;  // 64 tokens x 64 bf16 = 8 KB (128-byte rows)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kStageBytes = 5 * kAtomBytes;
 constexpr int kXRow = 272;              // padded fp32 row of the score exchange buffer
 constexpr uint32_t kTQ = 0, kTS = 160, kTP = 224, kTO = 256, kTCols = 512;
@@ -43,8 +43,10 @@ constexpr float kSlackM = 8.0f;
 
 // Shared memory map (from a 1024-aligned base).
 constexpr int kOffStages = 0;
-constexpr int kOffX = kOffStages + kStages * kStageBytes;   // exchange buffer 128 x 272 B
-constexpr int kOffBars = kOffX + kH * kXRow;
+constexpr int kOffX = kOffStages + kStages * kStageBytes;   // peer's partial scores 128 x 272 B
+constexpr int kOffStage = kOffX + kH * kXRow;                 // my partial scores (outbound)
+constexpr int kWarpX = 32 * kXRow;                             // one softmax warp's rows
+constexpr int kOffBars = kOffStage + kH * kXRow;
 constexpr int kOffMisc = kOffBars + 256;
 constexpr int kSmemMla = kOffMisc + 256 + 1024;
 
@@ -148,13 +150,13 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   // [0,4) kv_full  [4,8) kv_empty  8 s_full  9 s_free  10 p_full  11 pv_done
-  // 12 q_ready  13 xfull (peer wrote my buffer)  14 consumed (peer read its buffer)
+  // 12 q_ready  [16,20) xfull[w]: the peer's rows for softmax warp w landed here
+  // [20,24) consumed[w]: the peer has read what warp w sent it
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(smem + kOffMisc + 16);  // warp sums (8)
   int* s_start = reinterpret_cast<int*>(smem + kOffMisc + 96);
-  const uint32_t x_local = smem_u32(smem + kOffX);
-  const uint32_t x_peer = map_to_cta(x_local, peer);
+  const uint32_t x_peer = map_to_cta(smem_u32(smem + kOffX), peer);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -166,8 +168,10 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     mbar_init(bar(10), 4);
     mbar_init(bar(11), 1);
     mbar_init(bar(12), 4);
-    mbar_init(bar(13), kH);
-    mbar_init(bar(14), kH);
+    for (int w = 0; w < 4; ++w) {
+      mbar_init(bar(16 + w), 1);
+      mbar_init(bar(20 + w), 1);
+    }
     s_start[0] = -1;
     s_start[1] = 0;
     fence_mbar_init();
@@ -235,7 +239,16 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     Tile t;
     int n_here = 0;
     long long first_pg = 0;
+    auto page_of = [&](const Tile& x) {
+      return x.pidx < p.bt_stride ? p.block_table[static_cast<int64_t>(x.b) * p.bt_stride + x.pidx] : -1;
+    };
+    // the page id of the next tile is loaded one tile ahead
+    Walker wa = w;
+    Tile ta;
+    int page_next = wa.next(ta) ? page_of(ta) : -1;
     for (int j = 0; ok && w.next(t, &n_here, &first_pg); ++j) {
+      const int page = page_next;
+      page_next = wa.next(ta) ? page_of(ta) : -1;
       if (t.first && t.pidx == 0 && rank == 0) {
         const long long last_pg = first_pg + (w.np - 1);
         const long long big = r_pages * (q_pages + 1);
@@ -248,8 +261,6 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         ok = false;
         break;
       }
-      int page = -1;
-      if (t.pidx < p.bt_stride) page = p.block_table[static_cast<int64_t>(t.b) * p.bt_stride + t.pidx];
       int row = p.num_pages * kPS;  // past the pool: zero fill
       if (page >= 0 && page < p.num_pages)
         row = page * kPS;
@@ -379,28 +390,40 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float s[kTok];
+      {
+        uint32_t u[4][16];
 #pragma unroll
-      for (int c0 = 0; c0 < kTok; c0 += 16) {
-        uint32_t u[16];
-        tmem_ld16(trow + kTS + c0, u);
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(trow + kTS + q4 * 16, u[q4]);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) s[c0 + x] = __uint_as_float(u[x]);
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int x = 0; x < 16; ++x) s[q4 * 16 + x] = __uint_as_float(u[q4][x]);
       }
       if (has_nxt && nxt.first) load_q(nxt.b);  // S(j) is read: Q may change
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(9));
-      // swap partial scores with the peer
+      // Swap partial scores with the peer, one bulk copy per warp: my 32 rows go
+      // to the peer's buffer (completing on its xfull[w]); its rows arrive in
+      // mine. consumed[w] (from the peer) frees my outbound rows and its inbound
+      // buffer for the next tile.
+      const int wq = warp & 3;
       if (j > 0) {
-        ok = mbar_wait_cluster(bar(14), (j - 1) & 1);
+        ok = lane == 0 ? mbar_wait_cluster(bar(20 + wq), (j - 1) & 1) : true;
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
 #pragma unroll
       for (int c = 0; c < kTok; c += 4)
-        st_cluster_v4(x_peer + h * kXRow + c * 4, s[c], s[c + 1], s[c + 2], s[c + 3]);
-      mbar_arrive_cluster(map_to_cta(bar(13), peer));
-      ok = mbar_wait_cluster(bar(13), j & 1);
+        *reinterpret_cast<float4*>(smem + kOffStage + h * kXRow + c * 4) = make_float4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_s2s_cluster(x_peer + wq * kWarpX, smem_u32(smem + kOffStage + wq * kWarpX), kWarpX,
+                         map_to_cta(bar(16 + wq), peer));
+        mbar_arrive_expect_tx(bar(16 + wq), kWarpX);
+      }
+      ok = mbar_wait(bar(16 + wq), j & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
       for (int c = 0; c < kTok; c += 4) {
@@ -410,7 +433,8 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         s[c + 2] += o.z;
         s[c + 3] += o.w;
       }
-      mbar_arrive_cluster(map_to_cta(bar(14), peer));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(20 + wq), peer));
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kTok; ++c) {

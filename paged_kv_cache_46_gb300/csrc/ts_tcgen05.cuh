@@ -141,6 +141,18 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                "f"(c), "f"(d)
                : "memory");
 }
+// Bulk copy from this CTA's shared memory into another CTA's (shared::cluster
+// address), completion counted on an mbarrier in the destination CTA. 16-byte
+// aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
 // Release-arrive (cluster scope) on an mbarrier that may live in another CTA.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
