@@ -62,6 +62,9 @@ typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
  * attention workspace. The library sets bits and never clears them. */
 #define TS_DEVERR_PAGE_RANGE 0x1u
 #define TS_DEVERR_TIMEOUT 0x2u
+/* A kernel found its dynamic shared memory not aligned as its tile layout
+ * needs (1024 bytes) and returned without computing anything. */
+#define TS_DEVERR_SMEM_ALIGN 0x4u
 
 /* Human-readable name of a status code. Never NULL. */
 TS_API const char* ts_status_string(int status);

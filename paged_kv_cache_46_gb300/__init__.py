@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(HERE, "libts_attn.so")
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_WORKSPACE, TS_ERR_CUDA, TS_ERR_CAPACITY = range(6)
 TS_F32, TS_BF16 = 0, 1
-TS_DEVERR_PAGE_RANGE, TS_DEVERR_TIMEOUT = 0x1, 0x2
+TS_DEVERR_PAGE_RANGE, TS_DEVERR_TIMEOUT, TS_DEVERR_SMEM_ALIGN = 0x1, 0x2, 0x4
 
 
 class TSError(RuntimeError):

@@ -21,8 +21,9 @@
 // cluster; a sequence cut across clusters leaves fp32 partial states that a
 // second kernel merges by LSE.
 //
-// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
-// allocator, warps 4-7 softmax / epilogue (one head row per thread).
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
+// allocator, warps 4-11 softmax / epilogue (one head row and half of the
+// tile's tokens per thread). Four K/V stages keep three pages in flight.
 #include <cmath>
 
 #include "ts_tcgen05.cuh"
@@ -30,25 +31,29 @@
 namespace ts {
 namespace {
 
-constexpr int kH = 128, kDqk = 576, kDv = 512, kPS = 64, kTok = 64;
+constexpr int kH = 128, kDqk = 576, kDv = 512, kPS = 64, kTok = 64, kTokHalf = kTok / 2;
 constexpr int kAtomBytes = kTok * 128;  // 64 tokens x 64 bf16 = 8 KB (128-byte rows)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kStageBytes = 5 * kAtomBytes;
-constexpr int kXRow = 272;              // padded fp32 row of the score exchange buffer
 constexpr uint32_t kTQ = 0, kTS = 160, kTP = 224, kTO = 256, kTCols = 512;
-constexpr int kThreadsMla = 256;
+constexpr int kThreadsMla = 384;
 constexpr float kLog2eM = 1.4426950408889634f;
 constexpr float kLn2M = 0.6931471805599453f;
 constexpr float kSlackM = 8.0f;
 
 // Shared memory map (from a 1024-aligned base).
 constexpr int kOffStages = 0;
-constexpr int kOffX = kOffStages + kStages * kStageBytes;   // peer's partial scores 128 x 272 B
-constexpr int kOffStage = kOffX + kH * kXRow;                 // my partial scores (outbound)
-constexpr int kWarpX = 32 * kXRow;                             // one softmax warp's rows
-constexpr int kOffBars = kOffStage + kH * kXRow;
-constexpr int kOffMisc = kOffBars + 256;
-constexpr int kSmemMla = kOffMisc + 256 + 1024;
+// Score exchange buffers hold one 32 x 32 fp32 block per softmax warp (its
+// rows, its half of the tokens), 128-byte rows with the 16-byte chunks
+// swizzled by row, so that one bulk copy moves a warp's block.
+constexpr int kWarpX = 32 * kTokHalf * 4;                       // 4 KB
+constexpr int kXBufBytes = 8 * kWarpX;                          // a tile's 128 x 64 scores
+constexpr int kOffX = kOffStages + kStages * kStageBytes;       // score exchange, 2 tiles
+constexpr int kOffRed = kOffX + 2 * kXBufBytes;                 // pair exchange: [2][2][128] floats
+constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;              // 36 mbarriers
+constexpr int kOffMisc = kOffBars + 36 * 8;
+constexpr int kSmemMla = kOffMisc + 192;
+static_assert(kSmemMla <= 232448, "shared memory of one CTA");
 
 struct MlaParams {
   const __nv_bfloat16* q;   // [B, 128, 576]
@@ -136,10 +141,16 @@ struct Walker {
 
 __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaParams p,
                                                                     const __grid_constant__ CUtensorMap kvmap) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The whole 227 KB is in use, with no room to realign: the swizzled tiles
+  // need a 1024-byte aligned base, which the declaration asks for and the
+  // check below confirms (both CTAs of a cluster see the same offset).
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) set_device_error(p.err_word, TS_DEVERR_SMEM_ALIGN);
+    return;
+  }
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
@@ -150,12 +161,13 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   // [0,4) kv_full  [4,8) kv_empty  8 s_full  9 s_free  10 p_full  11 pv_done
-  // 12 q_ready  [16,20) xfull[w]: the peer's rows for softmax warp w landed here
-  // [20,24) consumed[w]: the peer has read what warp w sent it
+  // 12 q_ready  [16,32) xfull[buf][w]: the peer's half rows for softmax warp w
+  // landed in inbound buffer buf  [32,36) pair[q]: both softmax warps of TMEM
+  // lane quarter q posted their value
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  long long* scratch = reinterpret_cast<long long*>(smem + kOffMisc + 16);  // warp sums (8)
-  int* s_start = reinterpret_cast<int*>(smem + kOffMisc + 96);
+  long long* scratch = reinterpret_cast<long long*>(smem + kOffMisc + 16);  // warp sums (12)
+  int* s_start = reinterpret_cast<int*>(smem + kOffMisc + 16 + 8 * (kThreadsMla / 32));
   const uint32_t x_peer = map_to_cta(smem_u32(smem + kOffX), peer);
 
   if (tid == 0) {
@@ -164,14 +176,12 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       mbar_init(bar(4 + i), 1);
     }
     mbar_init(bar(8), 1);
-    mbar_init(bar(9), 4);
-    mbar_init(bar(10), 4);
+    mbar_init(bar(9), 8);
+    mbar_init(bar(10), 8);
     mbar_init(bar(11), 1);
-    mbar_init(bar(12), 4);
-    for (int w = 0; w < 4; ++w) {
-      mbar_init(bar(16 + w), 1);
-      mbar_init(bar(20 + w), 1);
-    }
+    mbar_init(bar(12), 8);
+    for (int i = 16; i < 32; ++i) mbar_init(bar(i), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar(32 + q), 2);
     s_start[0] = -1;
     s_start[1] = 0;
     fence_mbar_init();
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   } else if (have_work && warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t iS = idesc_bf16(kH, kTok, 0);
-    constexpr uint32_t iO = idesc_bf16(kH, 64, 1);
+    constexpr uint32_t iO = idesc_bf16(kH, 256, 1);
     Walker w;
     w.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
     auto issue_s = [&](int j) {
@@ -290,14 +300,18 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       mma_commit(bar(8));
       return true;
     };
-    Tile cur, nxt;
+    // S runs two tiles ahead of P V: the softmax reads S(j+1) (freeing the S
+    // columns, and reloading Q when tile j+2 starts a sequence) before it
+    // writes P(j), so S(j+2) is issued ahead of PV(j).
+    Tile cur, nxt, nn;
     bool has_cur = w.next(cur);
+    bool has_nxt = has_cur && w.next(nxt);
     ok = mbar_wait(bar(12), 0) && (!has_cur || issue_s(0));
+    if (ok && has_nxt) ok = mbar_wait(bar(9), 0) && issue_s(1);
     for (int j = 0; ok && has_cur; ++j) {
-      const bool has_nxt = w.next(nxt);
-      if (has_nxt) {
-        // S(j+1) once the softmax read S(j) (and reloaded Q for a new sequence)
-        ok = mbar_wait(bar(9), j & 1) && issue_s(j + 1);
+      const bool has_nn = has_nxt && w.next(nn);
+      if (has_nn) {
+        ok = mbar_wait(bar(9), (j + 1) & 1) && issue_s(j + 2);
         if (!ok) break;
       }
       ok = mbar_wait(bar(10), j & 1);
@@ -305,29 +319,38 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       tc_fence_after();
       const int s = j % kStages;
       const uint32_t st = smem_u32(smem + kOffStages + s * kStageBytes);
+      // O[:, 0:256] += P V: V is MN-major over four 64-column atoms (LBO = atom stride)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb)
-          mma_bf16_tmem_a(tmem + kTO + nb * 64, tmem + kTP + ks * 8,
-                          desc_sw128(st + nb * kAtomBytes + ks * 2048), iO, !(cur.first && ks == 0));
+        mma_bf16_tmem_a(tmem + kTO, tmem + kTP + ks * 8, desc_sw128(st + ks * 2048, kAtomBytes, 1024), iO,
+                        !(cur.first && ks == 0));
       mma_commit(bar(11));
       mma_commit(bar(4 + s));
       cur = nxt;
       has_cur = has_nxt;
+      nxt = nn;
+      has_nxt = has_nn;
     }
     if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
   } else if (have_work && warp >= 4) {
-    // ---------------- softmax / epilogue: one head row per thread ----------
-    const int h = tid - 128;
-    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const int dim0 = rank == 0 ? 0 : 256;  // this CTA's output columns
+    // ---------------- softmax / epilogue -------------------------------------
+    // Eight warps: warp w reads TMEM lane quarter w % 4 (head rows 32(w%4) ..
+    // +31, one row per thread) and handles one half of the columns: tokens
+    // 32 hf .. 32 hf + 31 of each tile and O columns 128 hf .. 128 hf + 127 of
+    // this CTA's 256. The two warps of a quarter agree on the row maximum (and
+    // at the end on the row sum) through pair_exchange.
+    const int sw = warp - 4;                  // softmax warp 0..7
+    const int quarter = warp & 3, hf = sw >> 2;
+    const int h = quarter * 32 + lane;        // head row
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int dim0 = (rank == 0 ? 0 : 256) + hf * 128;  // first output column of this thread
+    const int q_half = q_words / 2;           // TMEM columns of Q this warp loads
     Walker w;
     w.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
     auto load_q = [&](int b) {
       const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(b) * kH + h) * kDqk + atom0 * 64);
-      for (int c0 = 0; c0 < q_words; c0 += 16) {
+          p.q + (static_cast<int64_t>(b) * kH + h) * kDqk + atom0 * 64 + hf * q_half * 2);
+      for (int c0 = 0; c0 < q_half; c0 += 16) {
         uint32_t u[16];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
@@ -337,15 +360,33 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
           u[4 * x + 2] = v.z;
           u[4 * x + 3] = v.w;
         }
-        tmem_st16(trow + kTQ + c0, u);
+        tmem_st16(trow + kTQ + hf * q_half + c0, u);
       }
       tmem_wait_st();
     };
-    auto epilogue = [&](const Tile& t, float m, float l) {
+    // Swap one float per row with the other warp of this quarter (bounded
+    // wait on the pair's mbarrier; the two warps make the same calls in the
+    // same order, so the phase counter nx agrees).
+    float* const red = reinterpret_cast<float*>(smem + kOffRed);
+    int nx = 0;
+    auto pair_exchange = [&](float v, float& other) {
+      const int slot = nx & 1;
+      red[(slot * 2 + hf) * kH + h] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(32 + quarter));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(32 + quarter), slot));
+      other = red[(slot * 2 + (hf ^ 1)) * kH + h];
+      ++nx;
+      return got;
+    };
+    auto epilogue = [&](const Tile& t, float m, float l_half) {
+      float l_other = 0.f;
+      if (!pair_exchange(l_half, l_other)) return false;
+      const float l = l_half + l_other;
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      for (int c0 = 0; c0 < 256; c0 += 16) {
+      for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t u[16];
-        tmem_ld16(trow + kTO + c0, u);
+        tmem_ld16(trow + kTO + hf * 128 + c0, u);
         tmem_wait_ld();
         if (t.out_slot < 0) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t.b) * kH + h) * kDv + dim0 + c0);
@@ -367,118 +408,134 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         }
       }
       const float lse = l > 0.f ? (m + log2f(l)) * kLn2M : -INFINITY;
-      if (rank == 0) {
+      if (rank == 0 && hf == 0) {
         if (t.out_slot < 0) {
           if (p.lse) p.lse[static_cast<int64_t>(t.b) * kH + h] = lse;
         } else {
           p.part_lse[static_cast<int64_t>(t.out_slot) * kH + h] = lse;
         }
       }
+      return true;
     };
-
-    Tile cur, nxt, prev;
+    // Score exchange, pipelined one tile ahead: this warp reads its block of
+    // S(j+1) from TMEM and sends it with one bulk copy into the peer's buffer
+    // X[(j+1) % 2], completing on the peer's xfull[(j+1) % 2][sw], before the
+    // softmax of tile j, so the transfer hides behind that math. The thread
+    // keeps its own partial scores in registers. The copy's source is this
+    // CTA's X[j % 2], whose inbound scores of tile j were just read. Both
+    // directions of reuse are ordered by the copies themselves: the peer sends
+    // its copy j+2 (into X[j % 2] here) only after it saw copy j+1 land, i.e.
+    // after that copy finished reading X[j % 2].
+    auto xoff = [&](int c) {  // 16-byte chunk c (0..7) of this thread's row in a warp block
+      return static_cast<uint32_t>(sw * kWarpX + lane * (kTokHalf * 4) + ((c ^ (lane & 7)) << 4));
+    };
+    float mine[kTokHalf];
+    auto send_next = [&](int jn, bool reload_q, int qb) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(8), jn & 1))) return false;
+      tc_fence_after();
+      {
+        uint32_t u[2][16];
+        tmem_ld16(trow + kTS + hf * kTokHalf, u[0]);
+        tmem_ld16(trow + kTS + hf * kTokHalf + 16, u[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < kTokHalf; ++x) mine[x] = __uint_as_float(u[x / 16][x % 16]);
+      }
+      if (reload_q) load_q(qb);  // S(jn) is read: Q may change for S(jn+1)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(9));
+      const int src = (jn + 1) & 1, dst = jn & 1;
+#pragma unroll
+      for (int c = 0; c < kTokHalf / 4; ++c)
+        *reinterpret_cast<float4*>(smem + kOffX + src * kXBufBytes + xoff(c)) =
+            make_float4(mine[4 * c], mine[4 * c + 1], mine[4 * c + 2], mine[4 * c + 3]);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(16 + 8 * dst + sw), kWarpX);
+        bulk_s2s_cluster(x_peer + dst * kXBufBytes + sw * kWarpX,
+                         smem_u32(smem + kOffX + src * kXBufBytes + sw * kWarpX), kWarpX,
+                         map_to_cta(bar(16 + 8 * dst + sw), peer));
+      }
+      return true;
+    };
+    Tile cur, nxt, nn, prev;
     bool has_cur = w.next(cur);
     if (has_cur) load_q(cur.b);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(12));
-    float m = -INFINITY, l = 0.f;
+    bool has_nxt = has_cur && w.next(nxt);
+    if (has_cur) ok = send_next(0, has_nxt && nxt.first, nxt.b);
+    float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
     bool prev_last = false;
+    int n_tiles = 0;
     for (int j = 0; ok && has_cur; ++j) {
-      const bool has_nxt = w.next(nxt);
-      ok = mbar_wait(bar(8), j & 1);
+      const bool has_nn = has_nxt && w.next(nn);
+      // full scores of tile j: this thread's partial + the peer's
+      const int xb = j & 1;
+      ok = mbar_wait(bar(16 + 8 * xb + sw), (j >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      float s[kTok];
-      {
-        uint32_t u[4][16];
+      float s[kTokHalf];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(trow + kTS + q4 * 16, u[q4]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int x = 0; x < 16; ++x) s[q4 * 16 + x] = __uint_as_float(u[q4][x]);
+      for (int c = 0; c < kTokHalf / 4; ++c) {
+        const float4 o = *reinterpret_cast<const float4*>(smem + kOffX + xb * kXBufBytes + xoff(c));
+        s[4 * c] = mine[4 * c] + o.x;
+        s[4 * c + 1] = mine[4 * c + 1] + o.y;
+        s[4 * c + 2] = mine[4 * c + 2] + o.z;
+        s[4 * c + 3] = mine[4 * c + 3] + o.w;
       }
-      if (has_nxt && nxt.first) load_q(nxt.b);  // S(j) is read: Q may change
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(9));
-      // Swap partial scores with the peer, one bulk copy per warp: my 32 rows go
-      // to the peer's buffer (completing on its xfull[w]); its rows arrive in
-      // mine. consumed[w] (from the peer) frees my outbound rows and its inbound
-      // buffer for the next tile.
-      const int wq = warp & 3;
-      if (j > 0) {
-        ok = lane == 0 ? mbar_wait_cluster(bar(20 + wq), (j - 1) & 1) : true;
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-#pragma unroll
-      for (int c = 0; c < kTok; c += 4)
-        *reinterpret_cast<float4*>(smem + kOffStage + h * kXRow + c * 4) = make_float4(s[c], s[c + 1], s[c + 2], s[c + 3]);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_s2s_cluster(x_peer + wq * kWarpX, smem_u32(smem + kOffStage + wq * kWarpX), kWarpX,
-                         map_to_cta(bar(16 + wq), peer));
-        mbar_arrive_expect_tx(bar(16 + wq), kWarpX);
-      }
-      ok = mbar_wait(bar(16 + wq), j & 1);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-#pragma unroll
-      for (int c = 0; c < kTok; c += 4) {
-        const float4 o = *reinterpret_cast<const float4*>(smem + kOffX + h * kXRow + c * 4);
-        s[c] += o.x;
-        s[c + 1] += o.y;
-        s[c + 2] += o.z;
-        s[c + 3] += o.w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(20 + wq), peer));
+      if (has_nxt && !send_next(j + 1, has_nn && nn.first, nn.b)) { ok = false; break; }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTok; ++c) {
-        s[c] = c < cur.valid ? s[c] * p.scale_log2 : -INFINITY;
+      for (int c = 0; c < kTokHalf; ++c) {
+        s[c] = hf * kTokHalf + c < cur.valid ? s[c] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[c]);
+      }
+      {
+        float mo;
+        if (!pair_exchange(mx, mo)) { ok = false; break; }
+        mx = fmaxf(mx, mo);
       }
       // PV(j-1) done: P and O are free; finish the previous sequence if it ended
       if (j > 0) {
         ok = mbar_wait(bar(11), (j - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        if (prev_last) epilogue(prev, m, l);
+        if (prev_last && !epilogue(prev, m, l)) { ok = false; break; }
       }
       if (cur.first) {
         m = mx;
         l = 0.f;
       } else if (__any_sync(0xffffffffu, mx > m + kSlackM)) {
+        // both warps of the quarter see the same row maxima: same decision
         const float mnew = fmaxf(m, mx);
         const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
         m = mnew;
         l *= alpha;
-        for (int c0 = 0; c0 < 256; c0 += 16) {
+        for (int c0 = 0; c0 < 128; c0 += 16) {
           uint32_t u[16];
-          tmem_ld16(trow + kTO + c0, u);
+          tmem_ld16(trow + kTO + hf * 128 + c0, u);
           tmem_wait_ld();
 #pragma unroll
           for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
-          tmem_st16(trow + kTO + c0, u);
+          tmem_st16(trow + kTO + hf * 128 + c0, u);
         }
         tmem_wait_st();
       }
       const float ms = m == -INFINITY ? 0.f : m;
       float ls = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
         uint32_t u[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          const float e0 = fast_exp2(s[half * 32 + 2 * x] - ms);
-          const float e1 = fast_exp2(s[half * 32 + 2 * x + 1] - ms);
+          const float e0 = fast_exp2(s[2 * x] - ms);
+          const float e1 = fast_exp2(s[2 * x + 1] - ms);
           ls += e0 + e1;
           u[x] = float2_to_bf16x2(e0, e1);
         }
-        tmem_st16(trow + kTP + half * 16, u);
+        tmem_st16(trow + kTP + hf * 16, u);
       }
       tmem_wait_st();
       l += ls;
@@ -489,7 +546,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         ok = mbar_wait(bar(sj), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         unsigned char* st = smem + kOffStages + sj * kStageBytes;
-        for (int i = h; i < (kTok - cur.valid) * 4 * 8; i += kH) {
+        for (int i = sw * 32 + lane; i < (kTok - cur.valid) * 4 * 8; i += 8 * 32) {
           const int row = cur.valid + i / 32, a = (i / 8) & 3, c = i & 7;
           *reinterpret_cast<uint4*>(st + a * kAtomBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -502,20 +559,16 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       prev_last = cur.last;
       cur = nxt;
       has_cur = has_nxt;
+      nxt = nn;
+      has_nxt = has_nn;
+      n_tiles = j + 1;
     }
     if (ok && prev_last) {
       // the last tile's PV, then the last sequence's epilogue
-      int jl = 0;
-      {
-        Walker w2;
-        w2.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
-        Tile t2;
-        while (w2.next(t2)) ++jl;
-      }
-      ok = mbar_wait(bar(11), (jl - 1) & 1);
+      ok = mbar_wait(bar(11), (n_tiles - 1) & 1);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        epilogue(prev, m, l);
+        ok = epilogue(prev, m, l);
       } else {
         ok = false;
       }
