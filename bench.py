@@ -226,6 +226,16 @@ def algorithmic(case, groups=None):
     return tokens * row, 0
 
 
+def suffix_bytes(case, groups):
+    """Algorithmic bytes of the paged (suffix) kernel of a cascade call: every
+    sequence's own rows past its group's shared prefix."""
+    es = 2 if case.dtype == "bf16" else 4
+    tokens = int(case.attn_lens.astype(np.int64).sum())
+    members = np.diff(groups["member_indptr"])
+    shared = int((groups["prefix_len"].astype(np.int64) * members).sum())
+    return (tokens - shared) * case.H_kv * (case.D + case.Dv) * es
+
+
 def oracle_pass(view, case):
     import oracle
     if case.mla:
@@ -337,13 +347,10 @@ class DeviceStep:
             self.group_ms = (time.perf_counter() - t) * 1e3
             self.gdev = ts.groups_to_device(self.groups, dev)
             ws_bytes = ts.ts_cascade_decode_workspace_size(c.B, c.H_q, c.D)
-            self.launches = 4  # plan, prefix, paged suffix, split merge
         elif c.mla:
             ws_bytes = ts.ts_mla_workspace_size(c.B, c.H_q, c.Dv)
-            self.launches = 2
         else:
             ws_bytes = ts.ts_paged_decode_workspace_size(c.B, c.H_q, c.D)
-            self.launches = 2 + (1 if c.append else 0)
         self.ws = ts.new_workspace(ws_bytes, dev)
 
     def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None):
@@ -424,6 +431,25 @@ def run_ours(args):
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     err_word = ts.ts_read_device_error(runner.ws)
 
+    # per-kernel device times: a second timed pass with the library's launch
+    # trace on (CUDA events recorded around each of its launches, on the
+    # launching stream); kept apart from the pass above, whose step time the
+    # extra event records would perturb
+    n_tr = min(args.steps, 50)
+    ts.ts_trace_collect()
+    ts.ts_trace_enable(True)
+    for i in range(n_tr):
+        runner.step(i, stream=stream)
+    torch.cuda.synchronize()
+    ts.ts_trace_enable(False)
+    per_kernel = {}
+    for name, ms in ts.ts_trace_collect(capacity=64 * n_tr):
+        per_kernel.setdefault(name, []).append(ms)
+    kernels = {k: {"launches_per_step": len(v) / n_tr, "mean_ms": statistics.mean(v),
+                   "share": sum(v) / sum(sum(x) for x in per_kernel.values())}
+               for k, v in per_kernel.items()}
+    launches_per_step = sum(len(v) for v in per_kernel.values()) / n_tr
+
     # end to end through the public API with host buffers (pinned): the step's
     # inputs go up, its output comes back, every step
     e2e = None
@@ -483,13 +509,28 @@ def run_ours(args):
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
     peak_kind = "measured" if peaks else "fallback"
-    achieved = nbytes / (attn_ms * 1e-3) / 1e9
     value = world * nbytes / (ms_step * 1e-3) / 1e9
-    kernel = {"llama3_8b_layer": "ts_paged_decode_attn (split-KV kernel + LSE merge kernel)",
-              "mixed_lengths": "ts_paged_decode_attn (split-KV kernel + LSE merge kernel)",
-              "cascade": "ts_cascade_decode_attn (plan + tcgen05 prefix + paged suffix + merge)",
-              "mla": "ts_mla_paged_decode (2-CTA tcgen05 kernel + merge)"}[args.workload]
-    source = {"cascade": "ts_cascade.cu", "mla": "ts_mla.cu"}.get(args.workload, "ts_paged_decode.cu")
+    # the dominant kernel and its algorithmic work per launch
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    dom_ms = kernels[dom]["mean_ms"]
+    dom_bytes, dom_flops = nbytes, flops
+    if runner.groups is not None and dom == "paged_decode_kernel":
+        dom_bytes, dom_flops = suffix_bytes(case, runner.groups), 0
+    source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu"}.get(
+        dom, "ts_paged_decode.cu")
+    hbm_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = kernel_traffic(f"{args.workload}.md", source)
+    if case.mla:
+        tflops = dom_flops / (dom_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": tflops / tc_peak, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                    "kernel": dom, "kernel_ms": dom_ms, "flops_per_launch": dom_flops, "traffic": traffic,
+                    "hbm": {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
+                            "frac": hbm_achieved / hbm_peak, "bytes_per_launch": dom_bytes}}
+    else:
+        roofline = {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": hbm_achieved / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                    "kernel": dom, "kernel_ms": dom_ms, "bytes_per_launch": dom_bytes, "traffic": traffic}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -502,19 +543,19 @@ def run_ours(args):
                          f"{pool_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)"},
         "query_tokens_per_s": world * case.B / (ms_step * 1e-3),
         "hbm_frac_of_8tbs": value / world / 8000.0,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                     "kernel": kernel,
-                     "traffic": kernel_traffic(f"{args.workload}.md", source)},
-        "gpu_launches": runner.launches * args.steps,
+        "attention_call_gbs": nbytes / (attn_ms * 1e-3) / 1e9,
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
         "device_error_word": err_word,
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
-    if flops:
-        tflops = flops / (attn_ms * 1e-3) / 1e12
-        line["tensor"] = {"achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s", "frac": tflops / tc_peak,
-                          "flops_per_step": flops, "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                          "note": "whole call's flops over the whole call's time"}
+    if flops and "cascade_prefix_kernel" in kernels:
+        pms = kernels["cascade_prefix_kernel"]["mean_ms"]
+        tflops = flops / (pms * 1e-3) / 1e12
+        line["tensor"] = {"kernel": "cascade_prefix_kernel", "achieved": tflops, "peak": tc_peak,
+                          "unit": "TFLOP/s", "frac": tflops / tc_peak, "flops_per_launch": flops,
+                          "kernel_ms": pms, "peak_source": f"{peak_kind} bf16_tflops (burst)"}
     if runner.groups is not None:
         flat = sample_bytes(case, np.arange(case.B))
         line["config"]["flat_kv_bytes"] = flat

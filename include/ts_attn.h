@@ -289,6 +289,31 @@ TS_API ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const i
  */
 TS_API ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream);
 
+/*
+ * Launch trace (a measurement aid; the pages have no counterpart). While it
+ * is enabled, every kernel the library launches is bracketed by two CUDA
+ * events recorded on the launch's own stream, so that a caller can learn how
+ * long each kernel of a call ran. Off by default; enabling it adds two event
+ * records per launch and serialises launches that would otherwise overlap
+ * (programmatic dependent launch), so time a step without it.
+ *
+ * ts_trace_enable(on): 1 = record from now on, 0 = stop recording. Process-
+ *   wide; records made while on stay until collected.
+ * ts_trace_collect(out, capacity): waits for every recorded launch to finish,
+ *   writes up to `capacity` records in launch order (kernel name, NUL-
+ *   terminated, and its device time in milliseconds) to the caller's array
+ *   `out` (may be NULL to only count), forgets all records, and returns how
+ *   many there were (possibly more than `capacity`), or -1 if reading an
+ *   event failed (ts_last_error_detail() says which).
+ */
+typedef struct {
+  char kernel[48];
+  float ms;
+} ts_launch_record;
+
+TS_API ts_status ts_trace_enable(int32_t on);
+TS_API int32_t ts_trace_collect(ts_launch_record* out, int32_t capacity);
+
 #ifdef __cplusplus
 }
 #endif

@@ -51,6 +51,10 @@ class PrefixGroupsC(ctypes.Structure):
     ]
 
 
+class LaunchRecordC(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char * 48), ("ms", ctypes.c_float)]
+
+
 _VP, _I32, _I64, _F32, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                      ctypes.c_float, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32))
 
@@ -75,6 +79,8 @@ _SIGNATURES = {
     "ts_mla_paged_decode": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _I32,
                                            _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_read_device_error": (ctypes.c_int, [_VP, _U32P, _VP]),
+    "ts_trace_enable": (ctypes.c_int, [_I32]),
+    "ts_trace_collect": (_I32, [ctypes.POINTER(LaunchRecordC), _I32]),
 }
 
 _lib = None
@@ -303,3 +309,16 @@ def ts_read_device_error(workspace, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().ts_read_device_error(_ptr(workspace), ctypes.byref(v), _stream(stream)))
     return int(v.value)
+
+
+def ts_trace_enable(on: bool) -> None:
+    _check(lib().ts_trace_enable(1 if on else 0))
+
+
+def ts_trace_collect(capacity: int = 4096):
+    """[(kernel name, device ms)] of the launches recorded since the last collect."""
+    buf = (LaunchRecordC * capacity)()
+    n = lib().ts_trace_collect(buf, capacity)
+    if n < 0:
+        raise TSError(TS_ERR_CUDA, lib().ts_last_error_detail().decode())
+    return [(buf[i].kernel.decode(), float(buf[i].ms)) for i in range(min(n, capacity))]

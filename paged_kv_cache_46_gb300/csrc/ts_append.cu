@@ -65,6 +65,7 @@ extern "C" ts_status ts_kv_append(const void* k_new, const void* v_new, void* k_
       return fail(TS_ERR_INVALID_ARG, "ts_kv_append: tensors must be 16-byte aligned");
   const int row_vecs = static_cast<int>(row_bytes / 16);
   const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
+  LaunchTrace trace("kv_append_kernel", static_cast<cudaStream_t>(stream));
   kv_append_kernel<<<B, threads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
       static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, bt_stride, positions,

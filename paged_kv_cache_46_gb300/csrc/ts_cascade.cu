@@ -463,8 +463,12 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
   if (G > 0) {
     int32_t* tile_offset = reinterpret_cast<int32_t*>(wsb + ws.tile_offset);
     const int mpt = kBM / g;
-    cascade_plan_kernel<<<1, 1024, 0, s>>>(groups->member_indptr, G, mpt, tile_offset);
-    ts_status st = cuda_check(cudaGetLastError(), "cascade plan launch");
+    ts_status st;
+    {
+      LaunchTrace trace("cascade_plan_kernel", s);
+      cascade_plan_kernel<<<1, 1024, 0, s>>>(groups->member_indptr, G, mpt, tile_offset);
+      st = cuda_check(cudaGetLastError(), "cascade plan launch");
+    }
     if (st != TS_OK) return st;
     CUtensorMap kmap, vmap;
     st = make_page_map(&kmap, k_pool, num_pages, H_kv);
@@ -495,8 +499,11 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
     if (st != TS_OK) return st;
     // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
     const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);
-    cascade_prefix_kernel<<<dim3(tiles, H_kv), kThreadsPfx, kSmemPfx, s>>>(pp, kmap, vmap);
-    st = cuda_check(cudaGetLastError(), "cascade prefix launch");
+    {
+      LaunchTrace trace("cascade_prefix_kernel", s);
+      cascade_prefix_kernel<<<dim3(tiles, H_kv), kThreadsPfx, kSmemPfx, s>>>(pp, kmap, vmap);
+      st = cuda_check(cudaGetLastError(), "cascade prefix launch");
+    }
     if (st != TS_OK) return st;
   }
   PrefixInputs pre;

@@ -1,8 +1,12 @@
 // Status strings, error details, device-property cache and the error-word reader.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "ts_common.cuh"
 
@@ -33,6 +37,53 @@ int current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   return dev;
+}
+
+namespace {
+struct TraceRecord {
+  const char* kernel;
+  cudaEvent_t begin, end;
+  int device;
+};
+std::atomic<bool> g_trace_on{false};
+std::mutex g_trace_mutex;
+std::vector<TraceRecord> g_trace;                      // recorded, not yet collected
+std::vector<std::pair<int, cudaEvent_t>> g_free_events;  // (device, event) for reuse
+
+cudaEvent_t take_event(int device) {  // caller holds g_trace_mutex
+  for (size_t i = 0; i < g_free_events.size(); ++i)
+    if (g_free_events[i].first == device) {
+      cudaEvent_t e = g_free_events[i].second;
+      g_free_events.erase(g_free_events.begin() + static_cast<long>(i));
+      return e;
+    }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+LaunchTrace::LaunchTrace(const char* kernel, cudaStream_t stream) : kernel_(kernel), stream_(stream) {
+  if (!g_trace_on.load(std::memory_order_relaxed)) return;
+  device_ = current_device();
+  std::lock_guard<std::mutex> lock(g_trace_mutex);
+  begin_ = take_event(device_);
+  if (begin_ && cudaEventRecord(begin_, stream_) != cudaSuccess) {
+    g_free_events.emplace_back(device_, begin_);
+    begin_ = nullptr;
+  }
+}
+
+LaunchTrace::~LaunchTrace() {
+  if (!begin_) return;
+  std::lock_guard<std::mutex> lock(g_trace_mutex);
+  cudaEvent_t end = take_event(device_);
+  if (end && cudaEventRecord(end, stream_) == cudaSuccess) {
+    g_trace.push_back({kernel_, begin_, end, device_});
+  } else {
+    g_free_events.emplace_back(device_, begin_);
+    if (end) g_free_events.emplace_back(device_, end);
+  }
 }
 
 int device_sm_count() {
@@ -66,6 +117,44 @@ const char* ts_status_string(int status) {
 const char* ts_last_error_detail(void) { return ts::g_detail.c_str(); }
 
 const char* ts_version(void) { return "ts_attn 0.1 (sm_103a)"; }
+
+ts_status ts_trace_enable(int32_t on) {
+  ts::g_trace_on.store(on != 0);
+  return TS_OK;
+}
+
+int32_t ts_trace_collect(ts_launch_record* out, int32_t capacity) {
+  std::vector<ts::TraceRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(ts::g_trace_mutex);
+    recs.swap(ts::g_trace);
+  }
+  int32_t n = 0;
+  bool failed = false;
+  for (const ts::TraceRecord& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.end) != cudaSuccess || cudaEventElapsedTime(&ms, r.begin, r.end) != cudaSuccess)
+      failed = true;
+    if (out != nullptr && n < capacity) {
+      std::memset(out[n].kernel, 0, sizeof(out[n].kernel));
+      std::strncpy(out[n].kernel, r.kernel, sizeof(out[n].kernel) - 1);
+      out[n].ms = ms;
+    }
+    ++n;
+  }
+  {
+    std::lock_guard<std::mutex> lock(ts::g_trace_mutex);
+    for (const ts::TraceRecord& r : recs) {
+      ts::g_free_events.emplace_back(r.device, r.begin);
+      ts::g_free_events.emplace_back(r.device, r.end);
+    }
+  }
+  if (failed) {
+    ts::fail(TS_ERR_CUDA, "ts_trace_collect: reading an event failed");
+    return -1;
+  }
+  return n;
+}
 
 ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream) {
   if (workspace == nullptr || error_bits == nullptr)

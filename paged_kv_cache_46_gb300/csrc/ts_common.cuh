@@ -43,6 +43,23 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
 size_t paged_decode_workspace_bytes(int B, int H_q, int D);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch trace: while ts_trace_enable(1) is in force, a LaunchTrace scope
+// records one CUDA event on `stream` when it opens and one when it closes
+// (put exactly one kernel launch inside); ts_trace_collect reads them back.
+class LaunchTrace {
+ public:
+  LaunchTrace(const char* kernel, cudaStream_t stream);
+  ~LaunchTrace();
+  LaunchTrace(const LaunchTrace&) = delete;
+  LaunchTrace& operator=(const LaunchTrace&) = delete;
+
+ private:
+  const char* kernel_;
+  cudaStream_t stream_;
+  cudaEvent_t begin_ = nullptr;
+  int device_ = -1;
+};
+
 // ---------------------------------------------------------------------------
 // Device side
 // ---------------------------------------------------------------------------

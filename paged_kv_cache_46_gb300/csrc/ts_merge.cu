@@ -95,6 +95,7 @@ extern "C" ts_status ts_merge_states(const void* o_a, const float* lse_a, const 
   const int64_t threads = rows * 32;
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchTrace trace("merge_states_kernel", s);
   if (dtype == TS_F32)
     merge_states_kernel<float><<<blocks, 256, 0, s>>>(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, D);
   else

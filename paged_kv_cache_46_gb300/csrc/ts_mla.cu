@@ -734,7 +734,10 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, mla_decode_kernel, prm, kvmap), "mla decode launch");
+  {
+    LaunchTrace trace("mla_decode_kernel", s);
+    st = cuda_check(cudaLaunchKernelEx(&cfg, mla_decode_kernel, prm, kvmap), "mla decode launch");
+  }
   if (st != TS_OK) return st;
   cudaLaunchAttribute pattr[1];
   pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -746,5 +749,6 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   mcfg.stream = s;
   mcfg.attrs = pattr;
   mcfg.numAttrs = 1;
+  LaunchTrace trace("mla_merge_kernel", s);
   return cuda_check(cudaLaunchKernelEx(&mcfg, mla_merge_kernel, prm), "mla merge launch");
 }

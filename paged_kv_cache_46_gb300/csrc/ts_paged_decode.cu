@@ -863,7 +863,10 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, fn, prm), "paged decode launch");
+  {
+    LaunchTrace trace("paged_decode_kernel", stream);
+    st = cuda_check(cudaLaunchKernelEx(&cfg, fn, prm), "paged decode launch");
+  }
   if (st != TS_OK) return st;
 
   const long long warps = static_cast<long long>(B) * H_q;
@@ -874,6 +877,7 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
+  LaunchTrace trace("split_merge_kernel", stream);
   if (dtype == TS_BF16)
     st = cuda_check(cudaLaunchKernelEx(&mcfg,
                                        pre ? split_merge_kernel<__nv_bfloat16, true>

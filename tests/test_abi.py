@@ -78,3 +78,12 @@ def test_python_binding_requires_int32_metadata():
     with pytest.raises(TypeError):
         ts.ts_paged_decode_attn(q, torch.zeros(2, 16, 2, 64), torch.zeros(2, 16, 2, 64),
                                 torch.zeros(1, 1, dtype=torch.int64), torch.zeros(1, dtype=torch.int32), 1.0)
+
+
+def test_launch_trace_toggles_without_a_gpu(lib):
+    """Enabling, disabling and collecting the launch trace touches no device
+    when nothing was launched: an empty collect returns 0 records."""
+    assert lib.ts_trace_enable(1) == ts.TS_OK
+    assert lib.ts_trace_enable(0) == ts.TS_OK
+    assert lib.ts_trace_collect(None, 0) == 0
+    assert ts.ts_trace_collect() == []

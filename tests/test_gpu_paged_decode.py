@@ -181,3 +181,24 @@ def test_merge_states(dtype):
         compare(o, o_ref, "f32", l, l_ref, "merge f32")
     else:
         compare(o, o_ref, "bf16", l, l_ref, "merge bf16")
+
+
+def test_launch_trace_records_each_kernel_of_a_call():
+    """With the launch trace on, one append + one decode call record the
+    append kernel, the split-KV kernel and the merge kernel, in launch order,
+    each with a positive device time; results stay correct."""
+    case = workloads.tiny_gqa_append(device=DEV)
+    k0, v0 = case.k_pool.clone(), case.v_pool.clone()
+    ts.ts_trace_collect()
+    ts.ts_trace_enable(True)
+    try:
+        _append(case)
+        out, lse, _ = _run_decode(case)
+    finally:
+        ts.ts_trace_enable(False)
+    recs = ts.ts_trace_collect()
+    assert [r[0] for r in recs] == ["kv_append_kernel", "paged_decode_kernel", "split_merge_kernel"]
+    assert all(ms > 0 for _, ms in recs)
+    o_ref, l_ref = oracle_decode(case, k_pool=k0, v_pool=v0)
+    compare(out, o_ref, "f32", lse, l_ref, "traced tiny append")
+    assert ts.ts_trace_collect() == []
