@@ -519,7 +519,7 @@ def run_ours(args):
     source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu"}.get(
         dom, "ts_paged_decode.cu")
     hbm_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(f"{args.workload}.md", source)
+    traffic = kernel_traffic(f"{dom}__{args.workload}.md", source)
     if case.mla:
         tflops = dom_flops / (dom_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
