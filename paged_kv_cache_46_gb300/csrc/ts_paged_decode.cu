@@ -99,6 +99,7 @@ struct PagedParams {
   uint32_t stages_off;   // offset of the first stage in dynamic shared memory
   uint32_t page_bytes;   // bytes of one full page of K (or V), all kv heads
   int32_t chunk_rows;    // token rows per stage (a page, or a contiguous part of one)
+  int32_t seq_units;     // work units a sequence costs beyond its pages (its q load and epilogue)
   uint32_t kv_area;      // chunk_rows * row_bytes: K (and V) area of a stage
   uint32_t row_bytes;    // bytes of one token row of K (or V), all kv heads
   uint32_t q_bytes;      // bytes of one sequence's query rows
@@ -216,11 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int B = p.B;
   const int chunk = (B + blockDim.x - 1) / blockDim.x;
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
+  // Work units: a sequence with np > 0 own pages counts np + seq_units, the
+  // first seq_units standing for its fixed cost (query load, epilogue); they
+  // carry no page. The units of the batch are cut evenly across the CTAs.
+  const int A = p.seq_units;
   long long mine = 0;
   for (int b = lo; b < hi; ++b) {
     const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
     if (L > 0)
-      mine += (L + ps - 1) / ps;
+      mine += (L + ps - 1) / ps + A;
     else if (b % G_ctas == k)
       write_empty_sequence<T, kPfx>(p, D, b, k);
   }
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     long long off = excl;
     for (int b = lo; b < hi; ++b) {
       const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
-      const long long np = L > 0 ? (L + ps - 1) / ps : 0;
+      const long long np = L > 0 ? (L + ps - 1) / ps + A : 0;
       if (start < off + np) {
         s_start[0] = b;
         s_start[1] = static_cast<int>(start - off);
@@ -268,96 +273,168 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     bool aborted = false;
     if (start < end && s_start[0] >= 0) {
       const uint64_t pol = policy_evict_first();
-      long long g = start;
-      int b = s_start[0];
-      int pg = s_start[1];
+      // The range is walked in chunks of up to 32 pages of one sequence. The
+      // metadata of the next chunk (sequence lengths, 32 lengths per warp load,
+      // and the chunk's block-table entries, one per lane) is loaded while the
+      // current chunk's pages are issued, so a sequence boundary costs no
+      // dependent global-load latency in the copy stream.
+      long long g = start;   // global index of the next work unit
+      int b = s_start[0];    // sequence of the next unit
+      int pg = s_start[1];   // its unit index within the sequence (pages start at unit A;
+                             // within a segment pg counts pages)
       bool first_seg = true;
-      while (g < end && !aborted && b < B) {
-        const int pre = prefix_tokens<kPfx>(p, b);
-        const int L = max(p.seq_lens[b] - pre, 0);
-        const int np = (L + ps - 1) / ps;
-        if (np == 0 || pg >= np) {
-          ++b;
-          pg = 0;
-          continue;
-        }
-        const int n_here = static_cast<int>(min(static_cast<long long>(np - pg), end - g));
-        const bool complete = (pg == 0) && (n_here == np);
-        const int out_slot = complete ? -1 : (first_seg ? 2 * k : 2 * k + 1);
-        if (pg == 0 && lane == 0) {
-          const long long last = g + np - 1;  // global index of the sequence's last page
-          const long long big = r_pages * (q_pages + 1);
-          const int k1 = static_cast<int>(last < big ? last / (q_pages + 1)
-                                                     : r_pages + (last - big) / max(q_pages, 1ll));
-          const int nparts = k1 - k + 1;
-          p.split_info[b] = make_int2(k, (nparts << 1) | (first_seg ? 0 : 1));
-        }
-        const int pre_pages = pre / ps;  // prefix pages come first in the row
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride + pre_pages + pg;
-        for (int base = 0; base < n_here && !aborted; base += 32) {
-          const int cnt = min(32, n_here - base);
-          // entries past the row (length inconsistent with bt_stride) count as bad pages
-          int pid = -1;
-          if (lane < cnt && pre_pages + pg + base + lane < p.bt_stride) pid = bt_row[base + lane];
-          for (int i = 0; i < cnt; ++i) {
-            const int page = __shfl_sync(0xffffffffu, pid, i);
-            const int pidx = pg + base + i;
-            const bool ok = page >= 0 && page < p.num_pages;
-            const int rows = ok ? ((pidx == np - 1) ? (L - pidx * ps) : ps) : 0;
-            const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
-            for (int c = 0; c < nchunks; ++c) {
-              if (lane == 0) {
-                const int s = it % S;
-                if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
-                  set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
-                  aborted = true;
-                } else {
-                  const int r0 = c * p.chunk_rows;
-                  const int valid = max(0, min(rows - r0, p.chunk_rows));
-                  uint32_t flags = (base + i == 0 && c == 0 ? kFlagFirst : 0u) |
-                                   (base + i == n_here - 1 && c == nchunks - 1 ? kFlagLast : 0u);
-                  if (!ok) {
-                    flags |= kFlagBadPage;
-                    set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
-                  }
-                  StageDesc d;
-                  d.b = b;
-                  d.valid = valid;
-                  d.flags = flags;
-                  d.out_slot = out_slot;
-                  desc[s] = d;
-                  const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
-                  const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
-                  const uint32_t full_bar = smem_u32(&full[s]);
-                  mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
-                  const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-                  if (bytes) {
-                    const size_t off = static_cast<size_t>(page) * p.page_bytes +
-                                       static_cast<size_t>(r0) * p.row_bytes;
-                    bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
-                    bulk_g2s_hint(st + p.kv_area, static_cast<const char*>(p.v_pool) + off, bytes,
-                                  full_bar, pol);
-                  }
-                  if (qb)
-                    bulk_g2s(st + 2 * p.kv_area,
-                             static_cast<const char*>(p.q) + static_cast<size_t>(b) * p.q_bytes, qb,
-                             full_bar);
-                }
-              }
-              aborted = __shfl_sync(0xffffffffu, aborted, 0);
-              if (aborted) break;
-              ++it;
+      int seg_left = 0, seg_L = 0, seg_np = 0, seg_pre = 0, seg_slot = -1;
+      int wb = b;                                   // lengths window: sequences wb .. wb+31
+      auto load_len = [&](int base, int& pre_out) {  // this lane's sequence base+lane
+        const int bb = base + lane;
+        pre_out = 0;
+        if (bb >= B) return -1;
+        pre_out = prefix_tokens<kPfx>(p, bb);
+        return max(p.seq_lens[bb] - pre_out, 0);
+      };
+      int win_pre, nxt_pre;
+      int win_len = load_len(wb, win_pre);
+      int nxt_len = load_len(wb + 32, nxt_pre);
+      // a chunk: `cnt` pages pg0.. of sequence b (own length L), partial slot
+      // `slot`, chunk flags, and the split_info value to write (-1: none)
+      constexpr int kSegFirst = 1, kSegLast = 2;
+      struct Chunk {
+        int b, pg0, cnt, L, slot, flags, split;
+      };
+      // entries past the row (length inconsistent with bt_stride) count as bad pages
+      auto load_pid = [&](const Chunk& c, int pre) {
+        const int idx = pre / ps + c.pg0 + lane;  // prefix pages come first in the row
+        if (lane < c.cnt && idx < p.bt_stride)
+          return p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + idx];
+        return -1;
+      };
+      // fills c with the next chunk of the range (c.cnt == 0 at its end) and
+      // returns this lane's block-table entry of it
+      auto next_chunk = [&](Chunk& c) {
+        c.cnt = 0;
+        if (g >= end) return -1;
+        if (seg_left == 0) {
+          while (true) {
+            if (b >= B) return -1;
+            while (b >= wb + 32) {  // slide the lengths window
+              win_len = nxt_len;
+              win_pre = nxt_pre;
+              wb += 32;
+              nxt_len = load_len(wb + 32, nxt_pre);
             }
-            if (aborted) break;
+            const int L = __shfl_sync(0xffffffffu, win_len, b - wb);
+            const int np = (L + ps - 1) / ps;
+            if (np == 0 || pg >= np + A) {
+              ++b;
+              pg = 0;
+              continue;
+            }
+            if (pg < A) {  // the sequence's overhead units: no page
+              const int skip = static_cast<int>(min(static_cast<long long>(A - pg), end - g));
+              g += skip;
+              pg += skip;
+              if (g >= end) return -1;
+            }
+            pg -= A;  // from here on: page index
+            seg_L = L;
+            seg_np = np;
+            seg_pre = __shfl_sync(0xffffffffu, win_pre, b - wb);
+            break;
           }
+          const int n_here = static_cast<int>(min(static_cast<long long>(seg_np - pg), end - g));
+          const bool complete = (pg == 0) && (n_here == seg_np);
+          seg_slot = complete ? -1 : (first_seg ? 2 * k : 2 * k + 1);
+          c.split = -1;
+          if (pg == 0) {  // the sequence starts here: record how many CTAs hold its pages
+            const long long last = g + seg_np - 1;  // global unit of its last page
+            const long long big = r_pages * (q_pages + 1);
+            const int k1 = static_cast<int>(last < big ? last / (q_pages + 1)
+                                                       : r_pages + (last - big) / max(q_pages, 1ll));
+            c.split = ((k1 - k + 1) << 1) | (first_seg ? 0 : 1);
+          }
+          first_seg = false;
+          seg_left = n_here;
+          c.flags = kSegFirst;
+        } else {
+          c.flags = 0;
+          c.split = -1;
         }
-        g += n_here;
-        pg += n_here;
-        if (pg >= np) {
+        c.b = b;
+        c.pg0 = pg;
+        c.cnt = min(32, seg_left);
+        c.L = seg_L;
+        c.slot = seg_slot;
+        seg_left -= c.cnt;
+        if (seg_left == 0) c.flags |= kSegLast;
+        pg += c.cnt;
+        g += c.cnt;
+        // inside a segment pg is a page index; a segment ends at the sequence's
+        // end (next sequence, unit 0) or at the range's end (walk over)
+        if (seg_left == 0 && pg >= seg_np) {
           ++b;
           pg = 0;
         }
-        first_seg = false;
+        return load_pid(c, seg_pre);
+      };
+      Chunk cur, nxt;
+      int pid = next_chunk(cur);
+      while (cur.cnt > 0 && !aborted) {
+        const int pid_nxt = next_chunk(nxt);
+        if (cur.split >= 0 && lane == 0) p.split_info[cur.b] = make_int2(k, cur.split);
+        const int np_cur = (cur.L + ps - 1) / ps;
+        for (int i = 0; i < cur.cnt; ++i) {
+          const int page = __shfl_sync(0xffffffffu, pid, i);
+          const int pidx = cur.pg0 + i;
+          const bool ok = page >= 0 && page < p.num_pages;
+          const int rows = ok ? ((pidx == np_cur - 1) ? (cur.L - pidx * ps) : ps) : 0;
+          const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
+          for (int c = 0; c < nchunks; ++c) {
+            if (lane == 0) {
+              const int s = it % S;
+              if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
+                set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+                aborted = true;
+              } else {
+                const int r0 = c * p.chunk_rows;
+                const int valid = max(0, min(rows - r0, p.chunk_rows));
+                uint32_t flags = ((cur.flags & kSegFirst) && i == 0 && c == 0 ? kFlagFirst : 0u) |
+                                 ((cur.flags & kSegLast) && i == cur.cnt - 1 && c == nchunks - 1 ? kFlagLast : 0u);
+                if (!ok) {
+                  flags |= kFlagBadPage;
+                  set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
+                }
+                StageDesc d;
+                d.b = cur.b;
+                d.valid = valid;
+                d.flags = flags;
+                d.out_slot = cur.slot;
+                desc[s] = d;
+                const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
+                const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
+                const uint32_t full_bar = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
+                const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
+                if (bytes) {
+                  const size_t off = static_cast<size_t>(page) * p.page_bytes +
+                                     static_cast<size_t>(r0) * p.row_bytes;
+                  bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
+                  bulk_g2s_hint(st + p.kv_area, static_cast<const char*>(p.v_pool) + off, bytes,
+                                full_bar, pol);
+                }
+                if (qb)
+                  bulk_g2s(st + 2 * p.kv_area,
+                           static_cast<const char*>(p.q) + static_cast<size_t>(cur.b) * p.q_bytes, qb,
+                           full_bar);
+              }
+            }
+            aborted = __shfl_sync(0xffffffffu, aborted, 0);
+            if (aborted) break;
+            ++it;
+          }
+          if (aborted) break;
+        }
+        cur = nxt;
+        pid = pid_nxt;
       }
     }
     if (lane == 0) {
@@ -449,14 +526,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         uint4 kv[C::kNV];
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v) kv[v] = lds128(ra + lane_off[v]);
+        float2 kf[C::kPairsPL];  // the row widened once, used by all G heads
+#pragma unroll
+        for (int v = 0; v < C::kNV; ++v)
+#pragma unroll
+          for (int w = 0; w < Elem<T>::kPairs; ++w) kf[v * Elem<T>::kPairs + w] = Elem<T>::pair(kv[v], w);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-            for (int w = 0; w < Elem<T>::kPairs; ++w)
-              a = __ffma2_rn(qv[hh][v * Elem<T>::kPairs + w], Elem<T>::pair(kv[v], w), a);
+          for (int x = 0; x < C::kPairsPL; ++x) a = __ffma2_rn(qv[hh][x], kf[x], a);
           sc[i][hh] = a.x + a.y;
         }
       }
@@ -517,105 +596,158 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         uint4 vv[C::kNV];
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v) vv[v] = lds128(ra + lane_off[v]);
+        float2 vf[C::kPairsPL];
+#pragma unroll
+        for (int v = 0; v < C::kNV; ++v)
+#pragma unroll
+          for (int w = 0; w < Elem<T>::kPairs; ++w) vf[v * Elem<T>::kPairs + w] = Elem<T>::pair(vv[v], w);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
 #pragma unroll
-          for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-            for (int w = 0; w < Elem<T>::kPairs; ++w)
-              acc[hh][v * Elem<T>::kPairs + w] =
-                  __ffma2_rn(p2, Elem<T>::pair(vv[v], w), acc[hh][v * Elem<T>::kPairs + w]);
+          for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __ffma2_rn(p2, vf[x], acc[hh][x]);
         }
       }
     }
 
     if (d.flags & kFlagLast) {
-      // Merge the NG token groups of this warp by LSE (lanes with equal l).
+      // Merge the NG token groups of this warp (lanes with equal l hold the
+      // same dims of different token groups) by LSE, as a reduce-scatter:
+      // weights first (group max M, w_j = 2^(m_j - M), total l), then each
+      // butterfly step hands half of the still-shared values to the partner,
+      // so after log2(NG) steps every lane owns NT/NG finished values and
+      // all 32 lanes write the output.
+      constexpr int P = C::kPairsPL;     // float2 per lane per head
+      constexpr int NT = G * P;          // float2 per lane
+      constexpr int NF = NT / C::kNG;    // float2 each lane owns at the end
+      static_assert(NT % C::kNG == 0 && NF >= 1, "reduce-scatter split");
+      static_assert((G & (G - 1)) == 0, "heads per kv head: a power of two");
+      float M[G], Lt[G];
+      float2 r[NT];
 #pragma unroll
-      for (int o = C::kLPT; o < 32; o <<= 1) {
+      for (int hh = 0; hh < G; ++hh) {
+        float mx = m[hh];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float mo = __shfl_xor_sync(0xffffffffu, m[hh], o);
-          const float lo_ = __shfl_xor_sync(0xffffffffu, lsum[hh], o);
-          const float mn = fmaxf(m[hh], mo);
-          const float ms = mn == -INFINITY ? 0.f : mn;
-          const float wa = fast_exp2(m[hh] - ms), wb = fast_exp2(mo - ms);
-          lsum[hh] = lsum[hh] * wa + lo_ * wb;
-          m[hh] = mn;
-          const float2 wa2 = make_float2(wa, wa), wb2 = make_float2(wb, wb);
+        for (int o = C::kLPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ms = mx == -INFINITY ? 0.f : mx;
+        const float w = fast_exp2(m[hh] - ms);  // 0 for a group that saw no token
+        float lw = lsum[hh] * w;
 #pragma unroll
-          for (int x = 0; x < C::kPairsPL; ++x) {
-            float2 other;
-            other.x = __shfl_xor_sync(0xffffffffu, acc[hh][x].x, o);
-            other.y = __shfl_xor_sync(0xffffffffu, acc[hh][x].y, o);
-            acc[hh][x] = __ffma2_rn(acc[hh][x], wa2, __fmul2_rn(other, wb2));
+        for (int o = C::kLPT; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        M[hh] = mx;
+        Lt[hh] = lw;
+        const float2 w2 = make_float2(w, w);
+#pragma unroll
+        for (int x = 0; x < P; ++x) r[hh * P + x] = __fmul2_rn(acc[hh][x], w2);
+      }
+      int own = 0;  // flattened index (head * P + pair) of r[0] after the steps
+#pragma unroll
+      for (int st = 0; (C::kLPT << st) < 32; ++st) {
+        const int o = C::kLPT << st;
+        const int half = (NT >> st) / 2;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float2 send = up ? r[i] : r[i + half];
+          const float2 keep = up ? r[i + half] : r[i];
+          float2 recv;
+          recv.x = __shfl_xor_sync(0xffffffffu, send.x, o);
+          recv.y = __shfl_xor_sync(0xffffffffu, send.y, o);
+          r[i] = make_float2(keep.x + recv.x, keep.y + recv.y);
+        }
+        own += up ? half : 0;
+      }
+      // r[i] now holds flattened value own + i: head (own + i) / P, pair
+      // (own + i) % P of this lane's dims. Finish them per whole 16-byte
+      // vector when the share allows it.
+      constexpr int U = (NF % Elem<T>::kPairs == 0) ? Elem<T>::kPairs : 1;
+      auto pick = [&](const float (&a)[G], int hh) {
+        float v = a[0];
+#pragma unroll
+        for (int q = 1; q < G; ++q) v = hh == q ? a[q] : v;
+        return v;
+      };
+      bool grouped = false;
+      if constexpr (kPfx) grouped = p.group_of[d.b] >= 0;
+      const int64_t row0 = static_cast<int64_t>(d.b) * p.H_q + h * G;  // first query head of the warp
+      // normaliser c_s of the own-token state and weight c_p of the prefix
+      // state (0 outside prefix mode), and the row's final LSE (log2 units)
+      auto finish = [&](int hh, float& cs, float& cp, float& lse2) {
+        const float Mh = pick(M, hh), Lh = pick(Lt, hh);
+        cs = Lh > 0.f ? __fdividef(1.0f, Lh) : 0.f;
+        cp = 0.f;
+        lse2 = Lh > 0.f ? Mh + __log2f(Lh) : -INFINITY;
+        if (kPfx && grouped && d.out_slot < 0) {
+          const float lp2 = p.prefix_lse[row0 + hh] * kLog2e;
+          const float Mx = fmaxf(lse2, lp2);
+          const float ws = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - Mx);
+          const float wp = lp2 == -INFINITY ? 0.f : fast_exp2(lp2 - Mx);
+          const float den = ws + wp;
+          const float iden = den > 0.f ? __fdividef(1.0f, den) : 0.f;
+          cs *= ws * iden;
+          cp = wp * iden;
+          lse2 = den > 0.f ? Mx + __log2f(den) : -INFINITY;
+        }
+      };
+#pragma unroll
+      for (int c = 0; c < NF; c += U) {
+        const int xf = own + c;
+        const int hh = xf / P, x = xf % P;
+        const int dim = (x / Elem<T>::kPairs) * (D / C::kNV) + C::kVE * l + 2 * (x % Elem<T>::kPairs);
+        float cs, cp, lse2;
+        finish(hh, cs, cp, lse2);
+        float2 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) val[u] = make_float2(r[c + u].x * cs, r[c + u].y * cs);
+        if (d.out_slot < 0) {
+          if (cp != 0.f) {
+            const float* po = p.prefix_o + (row0 + hh) * D + dim;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const float2 pv = *reinterpret_cast<const float2*>(po + 2 * u);
+              val[u] = make_float2(val[u].x + pv.x * cp, val[u].y + pv.y * cp);
+            }
+          }
+          T* o = static_cast<T*>(p.out) + (row0 + hh) * D + dim;
+          if constexpr (sizeof(T) == 2) {
+            if constexpr (U == 4) {
+              *reinterpret_cast<uint4*>(o) =
+                  make_uint4(float2_to_bf16x2(val[0].x, val[0].y), float2_to_bf16x2(val[1].x, val[1].y),
+                             float2_to_bf16x2(val[2].x, val[2].y), float2_to_bf16x2(val[3].x, val[3].y));
+            } else {
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                *reinterpret_cast<uint32_t*>(o + 2 * u) = float2_to_bf16x2(val[u].x, val[u].y);
+            }
+          } else {
+            if constexpr (U == 2) {
+              *reinterpret_cast<float4*>(o) = make_float4(val[0].x, val[0].y, val[1].x, val[1].y);
+            } else {
+#pragma unroll
+              for (int u = 0; u < U; ++u) *reinterpret_cast<float2*>(o + 2 * u) = val[u];
+            }
+          }
+        } else {
+          float* o = p.part_o + (static_cast<int64_t>(d.out_slot) * p.H_q + h * G + hh) * D + dim;
+          if constexpr (U % 2 == 0) {
+#pragma unroll
+            for (int u = 0; u < U; u += 2)
+              *reinterpret_cast<float4*>(o + 2 * u) = make_float4(val[u].x, val[u].y, val[u + 1].x, val[u + 1].y);
+          } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) *reinterpret_cast<float2*>(o + 2 * u) = val[u];
           }
         }
       }
-      if (j == 0) {
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const int hq = h * G + hh;
-          const float ls = lsum[hh];
-          float inv = ls > 0.f ? 1.0f / ls : 0.f;
-          float lse2 = ls > 0.f ? m[hh] + log2f(ls) : -INFINITY;
+      {  // lane q < G writes head q's LSE (every lane computes one, no divergence)
+        const int q = lane & (G - 1);
+        float cs, cp, lse2;
+        finish(q, cs, cp, lse2);
+        if (lane < G) {
           if (d.out_slot < 0) {
-            T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(d.b) * p.H_q + hq) * D;
-            if constexpr (kPfx) {
-              if (p.group_of[d.b] >= 0) {
-                // merge the shared-prefix state: weights by LSE (log2 domain)
-                const int64_t row = static_cast<int64_t>(d.b) * p.H_q + hq;
-                const float lp2 = p.prefix_lse[row] * kLog2e;
-                const float M = fmaxf(lse2, lp2);
-                const float ws = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - M);
-                const float wp = lp2 == -INFINITY ? 0.f : fast_exp2(lp2 - M);
-                const float den = ws + wp;
-                const float cs = den > 0.f ? inv * ws / den : 0.f;
-                const float cp = den > 0.f ? wp / den : 0.f;
-                const float* po = p.prefix_o + row * D;
-#pragma unroll
-                for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-                  for (int w = 0; w < Elem<T>::kPairs; ++w) {
-                    const float2 pv2 = *reinterpret_cast<const float2*>(po + dim_off[v] + 2 * w);
-                    float2& a = acc[hh][v * Elem<T>::kPairs + w];
-                    a = make_float2(a.x * cs + pv2.x * cp, a.y * cs + pv2.y * cp);
-                  }
-                inv = 1.0f;  // the merged rows are already normalised
-                lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
-              }
-            }
-#pragma unroll
-            for (int v = 0; v < C::kNV; ++v) {
-              if constexpr (sizeof(T) == 2) {
-                uint4 pk;
-                const float2* a = &acc[hh][v * 4];
-                pk.x = float2_to_bf16x2(a[0].x * inv, a[0].y * inv);
-                pk.y = float2_to_bf16x2(a[1].x * inv, a[1].y * inv);
-                pk.z = float2_to_bf16x2(a[2].x * inv, a[2].y * inv);
-                pk.w = float2_to_bf16x2(a[3].x * inv, a[3].y * inv);
-                *reinterpret_cast<uint4*>(o + dim_off[v]) = pk;
-              } else {
-                const float2* a = &acc[hh][v * 2];
-                *reinterpret_cast<float4*>(o + dim_off[v]) =
-                    make_float4(a[0].x * inv, a[0].y * inv, a[1].x * inv, a[1].y * inv);
-              }
-            }
-            if (l == 0 && p.lse) p.lse[static_cast<int64_t>(d.b) * p.H_q + hq] = lse2 * kLn2;
+            if (p.lse) p.lse[row0 + q] = lse2 * kLn2;
           } else {
-            float* o = p.part_o + (static_cast<int64_t>(d.out_slot) * p.H_q + hq) * D;
-#pragma unroll
-            for (int v = 0; v < C::kNV; ++v) {
-#pragma unroll
-              for (int w = 0; w < Elem<T>::kPairs; w += 2) {
-                const float2 a0 = acc[hh][v * Elem<T>::kPairs + w];
-                const float2 a1 = acc[hh][v * Elem<T>::kPairs + w + 1];
-                *reinterpret_cast<float4*>(o + dim_off[v] + 2 * w) =
-                    make_float4(a0.x * inv, a0.y * inv, a1.x * inv, a1.y * inv);
-              }
-            }
-            if (l == 0) p.part_lse[static_cast<int64_t>(d.out_slot) * p.H_q + hq] = lse2 * kLn2;
+            p.part_lse[static_cast<int64_t>(d.out_slot) * p.H_q + h * G + q] = lse2 * kLn2;
           }
         }
       }
@@ -829,6 +961,19 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
          (kSmemBudget - kHeaderBytes - align_up(prm.row_bytes, 128)) / stage_of(chunk_rows) < 2)
     chunk_rows = (chunk_rows + 1) / 2;
   prm.chunk_rows = chunk_rows;
+  // A sequence's fixed cost (query load, epilogue) measured on GB300 is about
+  // what its consumers spend on 16 to 24 token rows; one 16-row page came out
+  // best in a sweep of 0..8 units (mixed lengths at head dim 64, Llama-3-8B
+  // layer at 128). TS_PAGED_DECODE_SEQ_UNITS overrides (tuning).
+  {
+    const int rows = 16;
+    int units = std::max(1, (rows + page_size / 2) / page_size);
+    if (const char* env = getenv("TS_PAGED_DECODE_SEQ_UNITS")) {
+      const int v = atoi(env);
+      if (v >= 0 && v <= 1024) units = v;
+    }
+    prm.seq_units = units;
+  }
   prm.kv_area = static_cast<uint32_t>(chunk_rows) * prm.row_bytes;
   prm.stage_bytes = stage_of(chunk_rows);
   prm.stages_off = static_cast<uint32_t>(kHeaderBytes + align_up(prm.row_bytes, 128));
