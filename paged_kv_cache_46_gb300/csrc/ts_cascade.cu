@@ -16,12 +16,13 @@
 //                          the prefix state by LSE into the final output.
 //
 // Prefix kernel roles (192 threads): warps 0-3 own one query row per thread
-// (Q load, softmax, epilogue), warp 4 lane 0 issues the TMA loads of K and V
-// page boxes (128-byte swizzle), warp 5 lane 0 issues the MMAs. TMEM holds
-// S (128 fp32 columns) and O (64 columns). K and V each have one buffer: the
-// K tile is refilled as soon as S's MMA has read it, the V tile as soon as
-// PV's MMA has, so loads overlap the softmax. P goes through shared memory in
-// the MMA's K-major 128-byte-swizzled layout.
+// (Q load, softmax, epilogue), warp 4 issues the TMA loads of K and V page
+// boxes (128-byte swizzle; its lanes hold the page ids of the next key tile),
+// warp 5 lane 0 issues the MMAs, S(j+1) or P V(j), whichever is ready first.
+// TMEM holds S (128 fp32 columns) and O (64 columns). K and V tiles are
+// double-buffered, so a tile's load latency hides behind the previous tile's
+// softmax and products. P goes through shared memory in the MMA's K-major
+// 128-byte-swizzled layout. Two CTAs share an SM.
 #include <cmath>
 #include <mutex>
 
@@ -43,13 +44,16 @@ constexpr float kLn2C = 0.6931471805599453f;
 constexpr float kSlack = 8.0f;
 
 // Shared memory (offsets from a 1024-aligned base).
-constexpr int kOffQ = 0;          // [128 x 64] bf16, SW128 K-major      16 KB
-constexpr int kOffK = 16384;      // [128 keys x 64] bf16, SW128          16 KB
-constexpr int kOffV = 32768;      // [128 keys x 64] bf16, SW128          16 KB
-constexpr int kOffP = 49152;      // 2 x [128 x 64 keys] bf16, SW128      32 KB
-constexpr int kOffBar = 81920;    // mbarriers
+constexpr int kOffQ = 0;          // [128 x 64] bf16, SW128 K-major              16 KB
+constexpr int kTileKV = 16384;    // one K or V tile: [128 keys x 64] bf16, SW128
+constexpr int kOffK = 16384;      // K tiles, 2 buffers                           32 KB
+constexpr int kOffV = 49152;      // V tiles, 2 buffers                           32 KB
+constexpr int kOffP = 81920;      // 2 x [128 x 64 keys] bf16, SW128              32 KB
+constexpr int kOffBar = kOffP + 32768;  // mbarriers
 constexpr int kOffTmem = kOffBar + 128;
-constexpr int kSmemPfx = kOffTmem + 16 + 1024;  // + alignment slack
+constexpr int kSmemPfx = kOffTmem + 16;
+// Two CTAs share an SM: their shared memory plus the 1 KB each reserves fits.
+static_assert(2 * (kSmemPfx + 1024) <= 233472, "two prefix CTAs per SM");
 
 struct PrefixParams {
   const __nv_bfloat16* q;  // [B, H_q, 64]
@@ -105,11 +109,16 @@ __global__ void __launch_bounds__(1024) cascade_plan_kernel(const int32_t* membe
 __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
     const PrefixParams p, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // no room to realign two CTAs' worth: the swizzled tiles need a 1024-byte
+  // aligned base, which the declaration asks for and the check confirms
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x, h = blockIdx.y;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) set_device_error(p.err_word, TS_DEVERR_SMEM_ALIGN);
+    return;
+  }
   const int n_tiles_total = p.tile_offset[p.num_groups];
   if (t >= n_tiles_total) return;
   // group of this tile: largest gi with tile_offset[gi] <= t
@@ -127,19 +136,25 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
   const int n_kt = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  const uint32_t b_kfull = smem_u32(&bars[0]), b_vfull = smem_u32(&bars[1]);
-  const uint32_t b_kempty = smem_u32(&bars[2]), b_vempty = smem_u32(&bars[3]);
-  const uint32_t b_sfull = smem_u32(&bars[4]), b_sfree = smem_u32(&bars[5]);
-  const uint32_t b_pfull = smem_u32(&bars[6]), b_pvdone = smem_u32(&bars[7]);
+  // K and V tiles are double-buffered: tile j lives in buffer j % 2 and is
+  // the (j / 2)-th phase of that buffer's full / empty barrier
+  auto b_kfull = [&](int buf) { return smem_u32(&bars[0 + buf]); };
+  auto b_vfull = [&](int buf) { return smem_u32(&bars[2 + buf]); };
+  auto b_kempty = [&](int buf) { return smem_u32(&bars[4 + buf]); };
+  auto b_vempty = [&](int buf) { return smem_u32(&bars[6 + buf]); };
+  const uint32_t b_sfull = smem_u32(&bars[8]), b_sfree = smem_u32(&bars[9]);
+  const uint32_t b_pfull = smem_u32(&bars[10]), b_pvdone = smem_u32(&bars[11]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK);
   const uint32_t sV = smem_u32(smem + kOffV), sP = smem_u32(smem + kOffP);
 
   if (tid == 0) {
-    mbar_init(b_kfull, 1);
-    mbar_init(b_vfull, 1);
-    mbar_init(b_kempty, 1);
-    mbar_init(b_vempty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_kfull(i), 1);
+      mbar_init(b_vfull(i), 1);
+      mbar_init(b_kempty(i), 1);
+      mbar_init(b_vempty(i), 1);
+    }
     mbar_init(b_sfull, 1);
     mbar_init(b_sfree, 4);
     mbar_init(b_pfull, 4);
@@ -180,61 +195,83 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
   bool ok = true;
 
   if (warp == 4) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
-      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
-        mbar_arrive_expect_tx(bar, kBN * kHD * 2);
-        for (int i = 0; i < kPagesPerTile; ++i) {
-          const int pi = j * kPagesPerTile + i;
-          int row = oob;
-          if (pi < n_pages) {
-            const int page = p.prefix_pages[pp0 + pi];
-            row = (page >= 0 && page < p.num_pages) ? page * kPS : oob;
-            if (!(page >= 0 && page < p.num_pages)) set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
-          }
-          tma_load_3d(dst + i * (kPS * 128), map, 0, h, row, bar);
-        }
-      };
-      for (int j = 0; j < n_kt && ok; ++j) {
-        if (j > 0 && !mbar_wait(b_kempty, (j - 1) & 1)) ok = false;
-        if (ok) load_tile(&kmap, sK, b_kfull, j);
-        if (ok && j > 0 && !mbar_wait(b_vempty, (j - 1) & 1)) ok = false;
-        if (ok) load_tile(&vmap, sV, b_vfull, j);
+    // ---------------- TMA producer (lane 0 issues; lane i < 8 holds page i) ----
+    const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
+    auto tile_rows = [&](int j) {       // this lane's page of key tile j, as a pool row
+      const int pi = j * kPagesPerTile + lane;
+      int row = oob;
+      if (lane < kPagesPerTile && pi < n_pages) {
+        const int page = p.prefix_pages[pp0 + pi];
+        if (page >= 0 && page < p.num_pages)
+          row = page * kPS;
+        else
+          set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
       }
-      if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+      return row;
+    };
+    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int rows) {
+      if (lane == 0) mbar_arrive_expect_tx(bar, kBN * kHD * 2);
+#pragma unroll
+      for (int i = 0; i < kPagesPerTile; ++i) {
+        const int row = __shfl_sync(0xffffffffu, rows, i);
+        if (lane == 0) tma_load_3d(dst + i * (kPS * 128), map, 0, h, row, bar);
+      }
+    };
+    int rows = n_kt > 0 ? tile_rows(0) : oob;
+    for (int j = 0; j < n_kt && ok; ++j) {
+      const int rows_next = j + 1 < n_kt ? tile_rows(j + 1) : oob;  // page ids one tile ahead
+      const int buf = j & 1, ph = ((j >> 1) - 1) & 1;  // buffer; phase of its previous use
+      ok = __shfl_sync(0xffffffffu, lane == 0 && j >= 2 ? mbar_wait(b_kempty(buf), ph) : true, 0);
+      if (!ok) break;
+      load_tile(&kmap, sK + buf * kTileKV, b_kfull(buf), rows);
+      ok = __shfl_sync(0xffffffffu, lane == 0 && j >= 2 ? mbar_wait(b_vempty(buf), ph) : true, 0);
+      if (!ok) break;
+      load_tile(&vmap, sV + buf * kTileKV, b_vfull(buf), rows);
+      rows = rows_next;
     }
+    if (!ok && lane == 0) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
+    // Whichever is ready first: S(js) (the softmax has read S(js-1), K(js)
+    // landed) or P V(j) (P(j) written, V(j) landed). A late K tile then no
+    // longer holds back P V, nor a late P the next S.
     if (lane == 0) {
       constexpr uint32_t iS = idesc_bf16(kBM, kBN, 0);
       constexpr uint32_t iO = idesc_bf16(kBM, kHD, 1);
-      auto issue_s = [&](int j) {
-        if (!mbar_wait(b_kfull, j & 1)) return false;
+      auto issue_s = [&](int js) {
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kHD / 16; ++ks)
-          mma_bf16(tmem, desc_sw128(sQ + ks * 32), desc_sw128(sK + ks * 32), iS, ks > 0);
+          mma_bf16(tmem, desc_sw128(sQ + ks * 32), desc_sw128(sK + (js & 1) * kTileKV + ks * 32), iS, ks > 0);
         mma_commit(b_sfull);
-        mma_commit(b_kempty);
-        return true;
+        mma_commit(b_kempty(js & 1));
       };
-      ok = n_kt > 0 ? issue_s(0) : true;
+      int js = 0;
+      if (n_kt > 0) {
+        ok = mbar_wait(b_kfull(0), 0);
+        if (ok) issue_s(js++);
+      }
       for (int j = 0; j < n_kt && ok; ++j) {
-        // S(j + 1) once the softmax has read S(j)
-        if (j + 1 < n_kt) {
-          ok = mbar_wait(b_sfree, j & 1) && issue_s(j + 1);
-          if (!ok) break;
+        const int buf = j & 1;
+        const unsigned long long t0 = globaltimer_ns();
+        while (true) {
+          if (js < n_kt && mbar_test(b_sfree, (js - 1) & 1) && mbar_test(b_kfull(js & 1), (js >> 1) & 1))
+            issue_s(js++);
+          if (mbar_test(b_pfull, j & 1) && mbar_test(b_vfull(buf), (j >> 1) & 1)) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
         }
-        ok = mbar_wait(b_pfull, j & 1) && mbar_wait(b_vfull, j & 1);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t sVj = sV + buf * kTileKV;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
           mma_bf16(tmem + kTmemO, desc_sw128(sP + (ks >> 2) * 16384 + (ks & 3) * 32),
-                   desc_sw128(sV + ks * 2048), iO, (j > 0 || ks > 0) ? 1u : 0u);
+                   desc_sw128(sVj + ks * 2048), iO, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(b_pvdone);
-        mma_commit(b_vempty);
+        mma_commit(b_vempty(buf));
       }
       if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
     }
@@ -266,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
         s[c] = key0 + c < plen ? s[c] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[c]);
       }
-      // the previous PV must be done before P and O are touched
+      // the previous P V must be done before P and O are touched
       if (j > 0) {
         ok = mbar_wait(b_pvdone, (j - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -496,6 +533,11 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
     st = cuda_check(cudaFuncSetAttribute(cascade_prefix_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
                     "prefix smem attribute");
+    if (st != TS_OK) return st;
+    // all of the SM's unified L1/shared memory as shared memory: two CTAs per SM
+    st = cuda_check(cudaFuncSetAttribute(cascade_prefix_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         static_cast<int>(cudaSharedmemCarveoutMaxShared)),
+                    "prefix carveout attribute");
     if (st != TS_OK) return st;
     // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
     const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);
