@@ -32,6 +32,7 @@
 //     with programmatic dependent launch, reduces the split sequences.
 #include <cmath>
 #include <cstdlib>
+#include <type_traits>
 
 #include "ts_common.cuh"
 
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     if (warp != 0) return;
     // ======================= producer warp ================================
     int it = 0;
+    int ps_stage = 0, ps_phase = 0;  // it % S and (it / S) & 1, kept incrementally
     bool aborted = false;
     if (start < end && s_start[0] >= 0) {
       const uint64_t pol = policy_evict_first();
@@ -390,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
           const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
           for (int c = 0; c < nchunks; ++c) {
             if (lane == 0) {
-              const int s = it % S;
-              if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
+              const int s = ps_stage;
+              if (it >= S && !mbar_wait(smem_u32(&empty[s]), ps_phase ^ 1)) {
                 set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
                 aborted = true;
               } else {
@@ -430,6 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
             aborted = __shfl_sync(0xffffffffu, aborted, 0);
             if (aborted) break;
             ++it;
+            if (++ps_stage == S) {
+              ps_stage = 0;
+              ps_phase ^= 1;
+            }
           }
           if (aborted) break;
         }
@@ -481,10 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   float2 acc[G][C::kPairsPL];
   float m[G], lsum[G];
 
-  int it = 0;
+  int it = 0, s = 0, phase = 0;  // s = it % S, phase = (it / S) & 1
   while (true) {
-    const int s = it % S;
-    if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1)) {
+    if (!mbar_wait(smem_u32(&full[s]), phase)) {
       set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
       break;
     }
@@ -513,16 +518,33 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     }
 
     const int valid = d.valid;
+    // A full stage (every row valid, passes cover it exactly) needs no row
+    // clamping and no score masking: the common case gets its own copy.
+    auto run_passes = [&](auto full_tag) {
+    constexpr bool kFull = decltype(full_tag)::value;
     for (int pass = 0; pass < npass; ++pass) {
       const int t0 = pass * tokens_per_pass + j * C::kTPG;
       // Rows past `valid` read the last valid row (their scores are masked and
       // their weights are 0); a unit with no valid row reads the zero row. So the
       // token loop has no branches and its dependency chains interleave freely.
       float sc[C::kTPG][G];
+      // V rows are read together with the K rows, so their shared-memory
+      // latency hides behind the scores and the softmax
+      uint4 vv[C::kTPG][C::kNV];
+      uint32_t row_off[C::kTPG];
+#pragma unroll
+      for (int i = 0; i < C::kTPG; ++i)
+        row_off[i] = kFull ? (t0 + i) * row_stride
+                           : (valid > 0 ? min(t0 + i, valid - 1) * row_stride : 0xffffffffu);
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
-        const int t = t0 + i;
-        const uint32_t ra = valid > 0 ? kbase + min(t, valid - 1) * row_stride : zero_row;
+        const uint32_t ra = row_off[i] != 0xffffffffu ? vbase + row_off[i] : zero_row;
+#pragma unroll
+        for (int v = 0; v < C::kNV; ++v) vv[i][v] = lds128(ra + lane_off[v]);
+      }
+#pragma unroll
+      for (int i = 0; i < C::kTPG; ++i) {
+        const uint32_t ra = row_off[i] != 0xffffffffu ? kbase + row_off[i] : zero_row;
         uint4 kv[C::kNV];
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v) kv[v] = lds128(ra + lane_off[v]);
@@ -547,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
           for (int hh = 0; hh < G; ++hh) sc[i][hh] += __shfl_xor_sync(0xffffffffu, sc[i][hh], o);
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
-        const bool in = t0 + i < valid;
+        const bool in = kFull || t0 + i < valid;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) sc[i][hh] = in ? sc[i][hh] : -INFINITY;
       }
@@ -591,16 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       }
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
-        const int t = t0 + i;
-        const uint32_t ra = valid > 0 ? vbase + min(t, valid - 1) * row_stride : zero_row;
-        uint4 vv[C::kNV];
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v) vv[v] = lds128(ra + lane_off[v]);
         float2 vf[C::kPairsPL];
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v)
 #pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) vf[v * Elem<T>::kPairs + w] = Elem<T>::pair(vv[v], w);
+          for (int w = 0; w < Elem<T>::kPairs; ++w) vf[v * Elem<T>::kPairs + w] = Elem<T>::pair(vv[i][v], w);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
@@ -609,6 +626,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         }
       }
     }
+    };
+    if (valid == p.chunk_rows && p.chunk_rows % tokens_per_pass == 0)
+      run_passes(std::integral_constant<bool, true>());
+    else
+      run_passes(std::integral_constant<bool, false>());
 
     if (d.flags & kFlagLast) {
       // Merge the NG token groups of this warp (lanes with equal l hold the
@@ -755,6 +777,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     ++it;
+    if (++s == S) {
+      s = 0;
+      phase ^= 1;
+    }
   }
 }
 
