@@ -165,8 +165,11 @@ def dist_setup(n_gpus: int):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:  # host-only ranks (tests of the multi-rank plumbing)
+            dist.init_process_group("gloo")
         return rank, world, local, dist
     return 0, 1, 0, None
 
