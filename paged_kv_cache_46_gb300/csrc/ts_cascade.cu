@@ -530,14 +530,15 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
     pp.prefix_o = prefix_o;
     pp.prefix_lse = prefix_lse;
     pp.err_word = reinterpret_cast<uint32_t*>(wsb);
-    st = cuda_check(cudaFuncSetAttribute(cascade_prefix_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
-                    "prefix smem attribute");
-    if (st != TS_OK) return st;
-    // all of the SM's unified L1/shared memory as shared memory: two CTAs per SM
-    st = cuda_check(cudaFuncSetAttribute(cascade_prefix_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         static_cast<int>(cudaSharedmemCarveoutMaxShared)),
-                    "prefix carveout attribute");
+    st = prepare_once(reinterpret_cast<const void*>(cascade_prefix_kernel), [](const void* k) {
+      ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
+                                "prefix smem attribute");
+      if (s2 != TS_OK) return s2;
+      // all of the SM's unified L1/shared memory as shared memory: two CTAs per SM
+      return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             static_cast<int>(cudaSharedmemCarveoutMaxShared)),
+                        "prefix carveout attribute");
+    });
     if (st != TS_OK) return st;
     // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
     const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);

@@ -86,6 +86,21 @@ LaunchTrace::~LaunchTrace() {
   }
 }
 
+namespace {
+std::mutex g_prep_mutex;
+std::vector<std::pair<const void*, int>> g_prepared;  // (kernel, device) prepared successfully
+}  // namespace
+
+ts_status prepare_once(const void* kernel, ts_status (*prepare)(const void*)) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_prep_mutex);
+  for (const auto& e : g_prepared)
+    if (e.first == kernel && e.second == dev) return TS_OK;
+  const ts_status st = prepare(kernel);
+  if (st == TS_OK) g_prepared.emplace_back(kernel, dev);
+  return st;
+}
+
 int device_sm_count() {
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return 0;

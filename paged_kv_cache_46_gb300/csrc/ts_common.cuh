@@ -43,6 +43,11 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
 size_t paged_decode_workspace_bytes(int B, int H_q, int D);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Runs `prepare` (function attributes, attribute queries) the first time a
+// kernel is launched on a device and remembers a success, so that later calls
+// (and calls captured into a CUDA graph) do no attribute work.
+ts_status prepare_once(const void* kernel, ts_status (*prepare)(const void*));
+
 // Launch trace: while ts_trace_enable(1) is in force, a LaunchTrace scope
 // records one CUDA event on `stream` when it opens and one when it closes
 // (put exactly one kernel launch inside); ts_trace_collect reads them back.

@@ -718,9 +718,10 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  ts_status st = cuda_check(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemMla),
-                            "mla smem attribute");
+  ts_status st = prepare_once(reinterpret_cast<const void*>(mla_decode_kernel), [](const void* k) {
+    return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMla),
+                      "mla smem attribute");
+  });
   if (st != TS_OK) return st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

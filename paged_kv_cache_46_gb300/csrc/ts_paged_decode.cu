@@ -1010,19 +1010,24 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   prm.num_stages = stages;
   const size_t smem = prm.stages_off + static_cast<size_t>(stages) * prm.stage_bytes;
 
-  ts_status st = cuda_check(
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)),
-      "set smem attribute");
+  // Once per kernel and device: allow the whole stage budget, and check that
+  // the kernel was compiled to launch with kLaunchRegs registers per thread
+  // (with fewer, the consumers' setmaxnreg.inc could never be satisfied).
+  ts_status st = prepare_once(reinterpret_cast<const void*>(fn), [](const void* k) {
+    ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget),
+                              "set smem attribute");
+    if (s2 != TS_OK) return s2;
+    cudaFuncAttributes fa;
+    s2 = cuda_check(cudaFuncGetAttributes(&fa, k), "query kernel attributes");
+    if (s2 != TS_OK) return s2;
+    if (fa.numRegs < kLaunchRegs)
+      return fail(TS_ERR_UNSUPPORTED, "paged decode kernel compiled with %d registers/thread, the register split "
+                  "needs %d", fa.numRegs, kLaunchRegs);
+    return TS_OK;
+  });
   if (st != TS_OK) return st;
-  // The producer/consumer register split assumes the kernel was compiled to
-  // launch with kLaunchRegs registers per thread; with fewer, the consumers'
-  // setmaxnreg.inc could never be satisfied. Refuse to launch in that case.
-  cudaFuncAttributes fa;
-  st = cuda_check(cudaFuncGetAttributes(&fa, fn), "query kernel attributes");
-  if (st != TS_OK) return st;
-  if (fa.numRegs < kLaunchRegs)
-    return fail(TS_ERR_UNSUPPORTED, "%s: kernel compiled with %d registers/thread, the register split needs %d",
-                who, fa.numRegs, kLaunchRegs);
+  if (smem > static_cast<size_t>(kSmemBudget))
+    return fail(TS_ERR_UNSUPPORTED, "%s: shared memory plan %zu B exceeds %d B", who, smem, kSmemBudget);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

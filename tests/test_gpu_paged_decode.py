@@ -202,3 +202,50 @@ def test_launch_trace_records_each_kernel_of_a_call():
     o_ref, l_ref = oracle_decode(case, k_pool=k0, v_pool=v0)
     compare(out, o_ref, "f32", lse, l_ref, "traced tiny append")
     assert ts.ts_trace_collect() == []
+
+
+def test_decode_step_replays_from_a_cuda_graph():
+    """One decode step (append + split-KV attention + merge) captured once in a
+    CUDA graph and replayed with new inputs written in place: new queries and
+    new K/V rows, then shorter lengths. The split plan is computed on the
+    device from seq_lens at every launch, so the replays need no host work."""
+    case = workloads.llama3_8b_layer(device=DEV, B=8, lo=100, hi=900)
+    k0, v0 = case.k_pool.clone(), case.v_pool.clone()
+    bt, lens, pos = device_metadata(case)
+    q, kn, vn = case.q.clone(), case.k_new.clone(), case.v_new.clone()
+    out = torch.empty_like(q)
+    lse = torch.empty(case.B, case.H_q, dtype=torch.float32, device=DEV)
+    ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D))
+    stream = torch.cuda.Stream()
+
+    def step():
+        ts.ts_kv_append(kn, vn, case.k_pool, case.v_pool, bt, pos, stream=stream)
+        ts.ts_paged_decode_attn(q, case.k_pool, case.v_pool, bt, lens, case.scale, out=out, lse=lse,
+                                workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()  # warm-up outside the capture (function attributes, tensor maps)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    gen = torch.Generator(device=DEV).manual_seed(123)
+    for attempt, shorten in ((0, False), (1, False), (2, True)):
+        q.copy_(torch.randn(q.shape, generator=gen, device=DEV).to(q.dtype))
+        kn.copy_(torch.randn(kn.shape, generator=gen, device=DEV).to(kn.dtype))
+        vn.copy_(torch.randn(vn.shape, generator=gen, device=DEV).to(vn.dtype))
+        new_lens = case.attn_lens.copy()
+        if shorten:
+            new_lens = np.maximum(new_lens // 3, 1).astype(np.int32)
+        lens.copy_(torch.from_numpy(new_lens))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert ts.ts_read_device_error(ws) == 0
+        view = workloads.oracle_view(case, k_pool=k0, v_pool=v0)
+        view["q"] = as_f64(q)
+        view["k_new"], view["v_new"] = as_f64(kn), as_f64(vn)
+        kp, vp = oracle.kv_append(view["k_pool"], view["v_pool"], view["k_new"], view["v_new"],
+                                  view["block_table"], view["positions"], case.page_size)
+        o_ref, l_ref = oracle.decode_attention(view["q"], kp, vp, view["block_table"],
+                                               new_lens.astype(np.int64), case.scale)
+        compare(out, o_ref, "bf16", lse, l_ref, f"graph replay {attempt}")
