@@ -297,12 +297,31 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(b_sfree);
       const int key0 = j * kBN;
-      float mx = -INFINITY;
+      // With a positive scale (the usual case) the scores stay unscaled: the
+      // row max is taken on raw scores (three-input max) and the scale is
+      // folded into the exponent's FFMA. Keys past the prefix are masked only
+      // in its last, partial tile.
+      const float sl = p.scale_log2;
+      float mx;
+      if (sl > 0.f) {
+        if (key0 + kBN > plen) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = key0 + c < plen ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < kBN; ++c) s[c] = key0 + c < plen ? s[c] : -INFINITY;
+        }
+        float mr = fmax3(s[0], s[1], s[2]);
+#pragma unroll
+        for (int c = 3; c + 1 < kBN; c += 2) mr = fmax3(mr, s[c], s[c + 1]);
+        mr = fmaxf(mr, s[kBN - 1]);
+        mx = mr * sl;
+      } else {
+        mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          s[c] = key0 + c < plen ? s[c] * sl : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
       }
+      const float sx = sl > 0.f ? sl : 1.f;  // factor still to apply to s[] in the exponent
       // the previous P V must be done before P and O are touched
       if (j > 0) {
         ok = mbar_wait(b_pvdone, (j - 1) & 1);
@@ -329,15 +348,14 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
         tmem_wait_st();
       }
       const float ms = m == -INFINITY ? 0.f : m;
-      float ls = 0.f;
+      float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kBN; c += 8) {
         float e[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          e[x] = fast_exp2(s[c + x] - ms);
-          ls += e[x];
-        }
+        for (int x = 0; x < 8; ++x) e[x] = fast_exp2(fmaf(s[c + x], sx, -ms));
+#pragma unroll
+        for (int x = 0; x < 8; x += 2) ls2 = __fadd2_rn(ls2, make_float2(e[x], e[x + 1]));
         uint4 pk;
         pk.x = float2_to_bf16x2(e[0], e[1]);
         pk.y = float2_to_bf16x2(e[2], e[3]);
@@ -345,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
         pk.w = float2_to_bf16x2(e[6], e[7]);
         *reinterpret_cast<uint4*>(smem + kOffP + (c >> 6) * 16384 + sw128_off(r, (c & 63) >> 3)) = pk;
       }
-      l += ls;
+      l += ls2.x + ls2.y;
       fence_async_smem();
       tc_fence_before();
       __syncwarp();

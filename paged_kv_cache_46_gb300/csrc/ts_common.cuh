@@ -184,6 +184,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Maximum of three floats in one instruction (NaN inputs are ignored, as fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // bf16 pair in one 32-bit word -> two floats (exact widening).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
