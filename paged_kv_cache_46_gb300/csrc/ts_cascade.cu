@@ -19,10 +19,10 @@
 // (Q load, softmax, epilogue), warp 4 issues the TMA loads of K and V page
 // boxes (128-byte swizzle; its lanes hold the page ids of the next key tile),
 // warp 5 lane 0 issues the MMAs, S(j+1) or P V(j), whichever is ready first.
-// TMEM holds S (128 fp32 columns) and O (64 columns). K and V tiles are
-// double-buffered, so a tile's load latency hides behind the previous tile's
-// softmax and products. P goes through shared memory in the MMA's K-major
-// 128-byte-swizzled layout. Two CTAs share an SM.
+// TMEM holds S (128 fp32 columns), O (64 columns) and P (64 columns of bf16
+// pairs, the P V product's A operand). K and V tiles are double-buffered, so
+// a tile's load latency hides behind the previous tile's softmax and
+// products. Two CTAs share an SM.
 #include <cmath>
 #include <mutex>
 
@@ -37,8 +37,9 @@ constexpr int kBN = 128;           // keys per tile
 constexpr int kPS = 16;            // page size of the prefix path
 constexpr int kPagesPerTile = kBN / kPS;
 constexpr int kThreadsPfx = 192;
-constexpr uint32_t kTmemCols = 256;  // S: [0, 128), O: [128, 192)
+constexpr uint32_t kTmemCols = 256;  // S: [0, 128), O: [128, 192), P: [192, 256)
 constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemP = 192;     // P as bf16 pairs: key k of row r at column k / 2 of lane r
 constexpr float kLog2eC = 1.4426950408889634f;
 constexpr float kLn2C = 0.6931471805599453f;
 constexpr float kSlack = 8.0f;
@@ -48,8 +49,7 @@ constexpr int kOffQ = 0;          // [128 x 64] bf16, SW128 K-major             
 constexpr int kTileKV = 16384;    // one K or V tile: [128 keys x 64] bf16, SW128
 constexpr int kOffK = 16384;      // K tiles, 2 buffers                           32 KB
 constexpr int kOffV = 49152;      // V tiles, 2 buffers                           32 KB
-constexpr int kOffP = 81920;      // 2 x [128 x 64 keys] bf16, SW128              32 KB
-constexpr int kOffBar = kOffP + 32768;  // mbarriers
+constexpr int kOffBar = 81920;    // mbarriers
 constexpr int kOffTmem = kOffBar + 128;
 constexpr int kSmemPfx = kOffTmem + 16;
 // Two CTAs share an SM: their shared memory plus the 1 KB each reserves fits.
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
   const uint32_t b_pfull = smem_u32(&bars[10]), b_pvdone = smem_u32(&bars[11]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK);
-  const uint32_t sV = smem_u32(smem + kOffV), sP = smem_u32(smem + kOffP);
+  const uint32_t sV = smem_u32(smem + kOffV);
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
         const uint32_t sVj = sV + buf * kTileKV;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_bf16(tmem + kTmemO, desc_sw128(sP + (ks >> 2) * 16384 + (ks & 3) * 32),
+          mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + ks * 8,
                    desc_sw128(sVj + ks * 2048), iO, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(b_pvdone);
         mma_commit(b_vempty(buf));
@@ -349,22 +349,21 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
       }
       const float ms = m == -INFINITY ? 0.f : m;
       float2 ls2 = make_float2(0.f, 0.f);
+      // P straight into TMEM (the P V MMA reads its A operand there)
 #pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
-        float e[8];
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) e[x] = fast_exp2(fmaf(s[c + x], sx, -ms));
-#pragma unroll
-        for (int x = 0; x < 8; x += 2) ls2 = __fadd2_rn(ls2, make_float2(e[x], e[x + 1]));
-        uint4 pk;
-        pk.x = float2_to_bf16x2(e[0], e[1]);
-        pk.y = float2_to_bf16x2(e[2], e[3]);
-        pk.z = float2_to_bf16x2(e[4], e[5]);
-        pk.w = float2_to_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(smem + kOffP + (c >> 6) * 16384 + sw128_off(r, (c & 63) >> 3)) = pk;
+        for (int x = 0; x < 32; x += 2) {
+          const float e0 = fast_exp2(fmaf(s[c + x], sx, -ms));
+          const float e1 = fast_exp2(fmaf(s[c + x + 1], sx, -ms));
+          ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+          pk[x / 2] = float2_to_bf16x2(e0, e1);
+        }
+        tmem_st16(trow + kTmemP + c / 2, pk);
       }
+      tmem_wait_st();
       l += ls2.x + ls2.y;
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
