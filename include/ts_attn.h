@@ -30,6 +30,15 @@
  *   - Errors: argument errors are returned before anything is enqueued; a
  *     failed launch returns TS_ERR_CUDA. ts_last_error_detail() describes the
  *     last non-OK status of the calling thread.
+ *   - Overlap with the previous kernel (programmatic dependent launch): the
+ *     append and paged-attention kernels may start while the previous kernel
+ *     of the stream is still running, if that kernel allows it (a kernel that
+ *     does not use programmatic dependent launch never does). Before waiting
+ *     for it, ts_paged_decode_attn reads only seq_lens, the block table and,
+ *     in cascade mode, the group descriptors; so a kernel that triggers its
+ *     dependents early must not write those. Every other input is read, and
+ *     every output written, after the wait. The library's own kernels follow
+ *     this rule, so back-to-back calls are safe.
  */
 #ifndef TS_ATTN_H_
 #define TS_ATTN_H_

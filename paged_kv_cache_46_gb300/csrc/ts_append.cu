@@ -21,6 +21,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         const int32_t* __restrict__ positions,
                                                         int32_t page_size, int32_t num_pages,
                                                         int32_t row_vecs) {
+  // Programmatic dependent launch: wait for the previous kernel of the stream
+  // before reading anything, and let the next one (the attention, which reads
+  // only lengths and block tables before its own wait) start its prologue.
+  pdl_wait_primary();
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int pos = positions[b];
   if (pos < 0) return;
@@ -65,10 +70,19 @@ extern "C" ts_status ts_kv_append(const void* k_new, const void* v_new, void* k_
       return fail(TS_ERR_INVALID_ARG, "ts_kv_append: tensors must be 16-byte aligned");
   const int row_vecs = static_cast<int>(row_bytes / 16);
   const int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
-  LaunchTrace trace("kv_append_kernel", static_cast<cudaStream_t>(stream));
-  kv_append_kernel<<<B, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, bt_stride, positions,
-      page_size, num_pages, row_vecs);
-  return cuda_check(cudaGetLastError(), "ts_kv_append: launch");
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  LaunchTrace trace("kv_append_kernel", cfg.stream);
+  return cuda_check(cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<const uint4*>(k_new),
+                                       static_cast<const uint4*>(v_new), static_cast<uint4*>(k_pool),
+                                       static_cast<uint4*>(v_pool), block_table, bt_stride, positions,
+                                       page_size, num_pages, row_vecs),
+                    "ts_kv_append: launch");
 }

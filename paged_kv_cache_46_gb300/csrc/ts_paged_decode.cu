@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
   unsigned char* stages = smem + p.stages_off;
 
-  pdl_wait_primary();
+  // Programmatic dependent launch: this kernel may start while the previous
+  // kernel of the stream finishes. Until griddepcontrol.wait it only reads
+  // seq_lens, the block table and the prefix-group metadata; every other read
+  // and every global write comes after the wait.
   pdl_launch_dependents();
 
   if (tid == 0) {
@@ -223,12 +226,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   // carry no page. The units of the batch are cut evenly across the CTAs.
   const int A = p.seq_units;
   long long mine = 0;
+  bool has_empty = false;
   for (int b = lo; b < hi; ++b) {
     const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
     if (L > 0)
       mine += (L + ps - 1) / ps + A;
     else if (b % G_ctas == k)
-      write_empty_sequence<T, kPfx>(p, D, b, k);
+      has_empty = true;
+  }
+  if (has_empty) {  // sequences with no own tokens are written here, after the wait
+    pdl_wait_primary();
+    for (int b = lo; b < hi; ++b)
+      if (p.seq_lens[b] - prefix_tokens<kPfx>(p, b) <= 0 && b % G_ctas == k)
+        write_empty_sequence<T, kPfx>(p, D, b, k);
   }
   long long incl = mine;
 #pragma unroll
@@ -380,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       };
       Chunk cur, nxt;
       int pid = next_chunk(cur);
+      pdl_wait_primary();  // the metadata of the first chunk is loaded; copies and writes follow
       while (cur.cnt > 0 && !aborted) {
         const int pid_nxt = next_chunk(nxt);
         if (cur.split >= 0 && lane == 0) p.split_info[cur.b] = make_int2(k, cur.split);
@@ -464,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<G>::kConsumer));
   if (warp - kFirstConsumerWarp >= n_consumer) return;
+  pdl_wait_primary();  // before the consumers' global reads (prefix state) and writes
 
   // ========================= consumer warps ================================
   const int h = warp - kFirstConsumerWarp;  // kv head of this warp
@@ -791,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 template <typename T, bool kPfx>
 __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, int D) {
   pdl_wait_primary();
+  pdl_launch_dependents();  // a following PDL-aware kernel may start its prologue
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int b = warp / p.H_q, hq = warp % p.H_q;
