@@ -225,10 +225,11 @@ def ts_group_prefixes(block_table: np.ndarray, seq_lens: np.ndarray, page_size: 
     cap_g = max(1, B // max(2, min_group))
     caps = np.maximum(0, (lens.astype(np.int64) - 1) // page_size)
     cap_pages = max(1, int(min(int(caps.sum()), cap_g * bt.shape[1])))
+    # the library writes every entry it reports; nothing needs clearing
     arrays = {
-        "prefix_indptr": np.zeros(cap_g + 1, np.int32), "prefix_pages": np.zeros(cap_pages, np.int32),
-        "prefix_len": np.zeros(cap_g, np.int32), "member_indptr": np.zeros(cap_g + 1, np.int32),
-        "member_ids": np.zeros(max(1, B), np.int32), "group_of": np.zeros(max(1, B), np.int32),
+        "prefix_indptr": np.empty(cap_g + 1, np.int32), "prefix_pages": np.empty(cap_pages, np.int32),
+        "prefix_len": np.empty(cap_g, np.int32), "member_indptr": np.empty(cap_g + 1, np.int32),
+        "member_ids": np.empty(max(1, B), np.int32), "group_of": np.empty(max(1, B), np.int32),
     }
     c = PrefixGroupsC(0, *[arrays[k].ctypes.data for k in
                            ("prefix_indptr", "prefix_pages", "prefix_len", "member_indptr", "member_ids",

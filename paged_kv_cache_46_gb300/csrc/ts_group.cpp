@@ -17,10 +17,11 @@
 //   * siblings are visited in increasing page id; members are listed in
 //     increasing sequence index.
 // Unary stretches of the trie (every member continues with the same page) are
-// crossed in one scan, so the cost is about sum of shared pages plus a sort per
-// branching node.
+// crossed in one pass along each member's row (contiguous memory), so the cost
+// is about the sum of shared pages plus a sort per branching node.
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <utility>
 #include <vector>
 
@@ -43,46 +44,68 @@ struct Grouper {
 
   // Returns the members of the subtree rooted at (S, d) left ungrouped.
   std::vector<int32_t> visit(std::vector<int32_t> S, int d) {
-    // cross the unary stretch: every member may go deeper and shares page d
-    while (true) {
-      bool extend = true;
-      for (int32_t s : S)
-        if (cap[s] <= d) {
-          extend = false;
-          break;
+    // cross the unary stretch (every member may go deeper and shares the
+    // page) in one pass along each member's row: it ends at the smallest cap
+    // or at the first page where some row differs from the first member's
+    {
+      int32_t lim = cap[S[0]];
+      for (int32_t s : S) lim = std::min(lim, cap[s]);
+      if (lim > d) {
+        const int32_t* r0 = bt + static_cast<int64_t>(S[0]) * stride;
+        int32_t e = lim;
+        for (size_t i = 1; i < S.size() && e > d; ++i) {
+          const int32_t* rs = bt + static_cast<int64_t>(S[i]) * stride;
+          if (std::memcmp(rs + d, r0 + d, static_cast<size_t>(e - d) * sizeof(int32_t)) == 0) continue;
+          int32_t t = d;
+          while (t < e && rs[t] == r0[t]) ++t;
+          e = t;
         }
-      if (!extend) break;
-      const int32_t p0 = page(S[0], d);
-      for (int32_t s : S)
-        if (page(s, d) != p0) {
-          extend = false;
-          break;
-        }
-      if (!extend) break;
-      ++d;
-    }
-    std::vector<int32_t> left;
-    std::vector<std::pair<int32_t, int32_t>> next;  // (page at depth d, sequence)
-    for (int32_t s : S) {
-      if (cap[s] <= d)
-        left.push_back(s);
-      else
-        next.emplace_back(page(s, d), s);
-    }
-    std::sort(next.begin(), next.end());
-    for (size_t i = 0; i < next.size();) {
-      size_t j = i;
-      while (j < next.size() && next[j].first == next[i].first) ++j;
-      std::vector<int32_t> child;
-      child.reserve(j - i);
-      for (size_t t = i; t < j; ++t) child.push_back(next[t].second);
-      if (static_cast<int>(child.size()) >= min_group) {
-        std::vector<int32_t> rest = visit(std::move(child), d + 1);
-        left.insert(left.end(), rest.begin(), rest.end());
-      } else {
-        left.insert(left.end(), child.begin(), child.end());
+        d = e;
       }
-      i = j;
+    }
+    // Branch on the page at depth d. Pages are counted in a hash table first,
+    // so only pages held by at least min_group members become children
+    // (visited in increasing page id); all others stay with this node.
+    std::vector<int32_t> left;
+    size_t cap2 = 16;
+    while (cap2 < 2 * S.size()) cap2 <<= 1;
+    std::vector<int32_t> key(cap2, 0), cnt(cap2, 0), child_of(cap2, -1);
+    std::vector<uint8_t> used(cap2, 0);
+    auto slot = [&](int32_t pg) {  // any int32 is a valid key (bad page ids included)
+      size_t h = (static_cast<uint32_t>(pg) * 2654435761u) & (cap2 - 1);
+      while (used[h] && key[h] != pg) h = (h + 1) & (cap2 - 1);
+      return h;
+    };
+    for (int32_t s : S) {
+      if (cap[s] <= d) continue;
+      const size_t h = slot(page(s, d));
+      used[h] = 1;
+      key[h] = page(s, d);
+      ++cnt[h];
+    }
+    std::vector<std::pair<int32_t, size_t>> kids;  // (page, table slot) of children
+    for (size_t h = 0; h < cap2; ++h)
+      if (used[h] && cnt[h] >= min_group) kids.emplace_back(key[h], h);
+    std::sort(kids.begin(), kids.end());
+    std::vector<std::vector<int32_t>> members(kids.size());
+    for (size_t c = 0; c < kids.size(); ++c) {
+      child_of[kids[c].second] = static_cast<int32_t>(c);
+      members[c].reserve(cnt[kids[c].second]);
+    }
+    for (int32_t s : S) {  // S is in increasing sequence order, and so are the children
+      if (cap[s] <= d) {
+        left.push_back(s);
+        continue;
+      }
+      const int32_t c = child_of[slot(page(s, d))];
+      if (c >= 0)
+        members[c].push_back(s);
+      else
+        left.push_back(s);
+    }
+    for (size_t c = 0; c < kids.size(); ++c) {
+      std::vector<int32_t> rest = visit(std::move(members[c]), d + 1);
+      left.insert(left.end(), rest.begin(), rest.end());
     }
     if (d >= 1 && static_cast<int>(left.size()) >= min_group) {
       std::sort(left.begin(), left.end());
