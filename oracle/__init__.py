@@ -24,6 +24,8 @@ docstring names the pins that tie it to something other than itself.
 from .attention import (
     gather_sequence,
     decode_attention,
+    fold_sq_factor,
+    multi_query_decode_attention,
     mla_decode_attention,
     merge_states,
     merge_states_many,
@@ -34,6 +36,8 @@ from .prefix_groups import check_prefix_groups, PrefixGroups
 __all__ = [
     "gather_sequence",
     "decode_attention",
+    "fold_sq_factor",
+    "multi_query_decode_attention",
     "mla_decode_attention",
     "merge_states",
     "merge_states_many",

@@ -103,6 +103,79 @@ def decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale):
     return out, lse
 
 
+def fold_sq_factor(num_heads: int, q_len: int, tile_rows: int = 128) -> int:
+    """Number of query tokens folded into the head (row) dimension of a tile.
+
+    TokenSpeed deep dive, section 7.2: ``F`` is the largest factor with
+    ``q_len % F == 0`` and ``num_heads * F <= tile_rows``; the kernel then sees
+    ``H_eff = num_heads * F`` rows per query step and ``q_len / F`` steps. A
+    head count that alone exceeds the tile folds nothing (``F = 1``).
+
+    Pinned by: the page's worked example (64 heads, 4 query tokens, 128-row
+    tile: F = 2, H_eff = 128, 2 steps; ``tests/golden/fold_sq_factor_example.json``)
+    and hand-checked values for prime, non-power-of-two and oversized cases.
+    """
+    if num_heads <= 0 or q_len <= 0 or tile_rows <= 0:
+        raise ValueError("num_heads, q_len and tile_rows must be positive")
+    best = 1
+    for f in range(1, q_len + 1):
+        if q_len % f == 0 and num_heads * f <= tile_rows:
+            best = f
+    return best
+
+
+def multi_query_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale):
+    """Decode with several new query tokens per sequence (speculative verify).
+
+    ``q`` holds ``q_len`` consecutive query tokens per sequence whose K/V rows
+    are already in the cache: ``seq_lens[b]`` counts them. Query token ``j``
+    sits at position ``L_b - q_len + j`` and attends tokens ``0 .. L_b - q_len + j``
+    (causal among the new tokens); each (token, head) row is otherwise the
+    single-query GQA decode of :func:`decode_attention`.
+
+    TokenSpeed deep dive, section 7 fig. 3 and 7.2 (decode over ``q_seqlen``
+    query tokens per sequence, the workspace sized by ``H * q_len`` rows);
+    the causal placement of the new tokens at the end of the context is the
+    reading listed in the design notes.
+
+    Args:
+        q: [B, q_len, H_q, D]; pools and block table as :func:`decode_attention`;
+        seq_lens: [B] context lengths including the q_len new tokens (>= q_len).
+
+    Returns:
+        (O [B, q_len, H_q, D] float64, LSE [B, q_len, H_q] float64).
+
+    Pinned by: q_len = 1 equals :func:`decode_attention`; every row equals
+    :func:`decode_attention` of that one query over the shortened context;
+    torch's fp64 scaled_dot_product_attention with an explicit causal mask on
+    the unpaged K/V; rows unaffected by K/V rows after their position.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, q_len, H_q, D = q.shape
+    page_size, H_kv = k_pool.shape[1], k_pool.shape[2]
+    if H_q % H_kv != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
+    g = H_q // H_kv
+    Dv = v_pool.shape[3]
+    out = np.zeros((B, q_len, H_q, Dv), dtype=np.float64)
+    lse = np.full((B, q_len, H_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L < q_len:
+            raise ValueError("seq_lens must count the q_len new tokens")
+        K = gather_sequence(k_pool, block_table[b], L, page_size).astype(np.float64)
+        V = gather_sequence(v_pool, block_table[b], L, page_size).astype(np.float64)
+        for j in range(q_len):
+            Lj = L - q_len + 1 + j
+            for kh in range(H_kv):
+                heads = slice(kh * g, (kh + 1) * g)
+                scores = scale * (q[b, j, heads] @ K[:Lj, kh, :].T)  # [g, Lj]
+                o, l = _softmax_attend(scores, V[:Lj, kh, :])
+                out[b, j, heads] = o
+                lse[b, j, heads] = l
+    return out, lse
+
+
 def mla_decode_attention(q, kv_pool, block_table, seq_lens, scale, d_v):
     """Absorbed-MLA decode: every query head attends one shared latent head.
 

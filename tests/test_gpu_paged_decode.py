@@ -109,6 +109,31 @@ def test_result_independent_of_split_pattern(ctas):
     assert np.all(as_f64(out[0]) == 0) and np.all(np.isneginf(as_f64(lse[0])))
 
 
+@pytest.mark.parametrize("ctas", [7, None])
+def test_one_workspace_serves_calls_with_different_cuts(ctas):
+    """The per-CTA records of cut sequences are rewritten by every call, so a
+    workspace reused across calls whose lengths cut the batch differently
+    (and leave some CTAs without a cut sequence) gives each call's result."""
+    lens_sets = [[700, 2049, 5, 64, 300, 17], [16, 33, 2049, 1, 800, 0], [4000, 3, 3, 3, 90, 512],
+                 [1, 1, 1, 1, 1, 1]]
+    ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(6, 32, 64))
+    for i, lens in enumerate(lens_sets):
+        case = workloads.build_case(f"reuse_{i}", 51 + i, B=6, H_q=32, H_kv=8, D=64, page_size=16,
+                                    seq_lens=lens, dtype="bf16", scale=0.125, device=DEV)
+        bt, dlens, _ = device_metadata(case)
+        if ctas is not None:
+            os.environ["TS_PAGED_DECODE_CTAS"] = str(ctas)
+        try:
+            out, lse = ts.ts_paged_decode_attn(case.q, case.k_pool, case.v_pool, bt, dlens, case.scale,
+                                               workspace=ws, return_lse=True)
+            torch.cuda.synchronize()
+        finally:
+            os.environ.pop("TS_PAGED_DECODE_CTAS", None)
+        assert ts.ts_read_device_error(ws) == 0
+        o_ref, l_ref = oracle_decode(case)
+        compare(out, o_ref, "bf16", lse, l_ref, f"reuse call {i} ctas={ctas}")
+
+
 @pytest.mark.parametrize("dtype,D,H_q,H_kv,ps", [
     ("f32", 64, 8, 2, 16), ("f32", 128, 8, 8, 16), ("bf16", 64, 8, 8, 16), ("bf16", 64, 16, 2, 32),
     ("bf16", 128, 64, 8, 16), ("bf16", 128, 8, 1, 8), ("bf16", 64, 4, 4, 16), ("f32", 64, 16, 8, 32),

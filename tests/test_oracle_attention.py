@@ -281,6 +281,94 @@ def test_kv_bytes_model_matches_worked_example():
     assert g["kv_bytes"] == g["per_request_mib"] * 2 ** 20
 
 
+def test_fold_sq_factor_matches_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "fold_sq_factor_example.json")))
+    f = oracle.fold_sq_factor(g["num_heads"], g["q_seqlen"], g["tile_rows"])
+    assert f == g["F"]
+    assert g["num_heads"] * f == g["H_eff"] and g["q_seqlen"] // f == g["q_seqlen_eff"]
+
+
+@pytest.mark.parametrize("H,q_len,tile,F_expected", [
+    (128, 4, 128, 1),   # the head count alone fills the tile
+    (32, 4, 128, 4),    # all four tokens fit
+    (64, 3, 128, 1),    # 3 is prime and 64 * 3 > 128
+    (16, 6, 128, 6),    # a non-power-of-two factor
+    (48, 4, 128, 2),    # 48 * 4 > 128 >= 48 * 2
+    (200, 2, 128, 1),   # more heads than tile rows
+    (4, 8, 8, 2),       # an 8-row tile
+    (1, 7, 8, 7),
+])
+def test_fold_sq_factor_hand_values(H, q_len, tile, F_expected):
+    assert oracle.fold_sq_factor(H, q_len, tile) == F_expected
+
+
+def _causal_sdpa_reference(q, K, V, lens, scale, g):
+    """torch fp64 SDPA with an explicit boolean mask: query j of sequence b
+    sees keys 0 .. L_b - q_len + j (test-side code)."""
+    B, q_len, H_q, D = q.shape
+    out = np.zeros((B, q_len, H_q, V.shape[3]))
+    for b in range(B):
+        L = int(lens[b])
+        k = torch.from_numpy(K[b, :L]).permute(1, 0, 2).repeat_interleave(g, dim=0)  # [H_q, L, D]
+        v = torch.from_numpy(V[b, :L]).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        qq = torch.from_numpy(q[b]).permute(1, 0, 2)  # [H_q, q_len, D]
+        pos = torch.arange(L)[None, :]
+        last = (L - q_len + torch.arange(q_len))[:, None]
+        mask = pos <= last  # [q_len, L]
+        o = F.scaled_dot_product_attention(qq[None], k[None], v[None], attn_mask=mask, scale=scale)
+        out[b] = o[0].permute(1, 0, 2).numpy()
+    return out
+
+
+def _multi_query_problem(seed, q_len, B=4, H_q=8, H_kv=2, D=16, page_size=4, Lmax=29):
+    rng, q1, K, V, lens = _random_problem(seed, B=B, H_q=H_q, H_kv=H_kv, D=D, page_size=page_size, Lmax=Lmax)
+    lens = np.maximum(lens, q_len)
+    lens[1] = q_len  # the new tokens are the whole context
+    q = rng.standard_normal((B, q_len, H_q, D))
+    kp, vp, bt = _paged_from_contiguous(rng, K, V, lens, page_size)
+    return q, K, V, lens, kp, vp, bt
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4])
+def test_multi_query_matches_causal_torch_sdpa(q_len):
+    q, K, V, lens, kp, vp, bt = _multi_query_problem(40 + q_len, q_len)
+    o, lse = oracle.multi_query_decode_attention(q, kp, vp, bt, lens, 0.41)
+    ref = _causal_sdpa_reference(q, K, V, lens, 0.41, 4)
+    np.testing.assert_allclose(o, ref, atol=1e-12, rtol=0)
+    # LSE of row j: scipy over the scores of its visible keys
+    for b in range(len(lens)):
+        for j in range(q_len):
+            Lj = int(lens[b]) - q_len + 1 + j
+            for h in range(q.shape[2]):
+                s = 0.41 * K[b, :Lj, h // 4] @ q[b, j, h]
+                assert abs(lse[b, j, h] - logsumexp(s)) < 1e-12
+
+
+def test_multi_query_rows_are_single_queries_over_shortened_contexts():
+    q_len = 3
+    q, K, V, lens, kp, vp, bt = _multi_query_problem(47, q_len)
+    o, lse = oracle.multi_query_decode_attention(q, kp, vp, bt, lens, 0.29)
+    for j in range(q_len):
+        o1, l1 = oracle.decode_attention(q[:, j], kp, vp, bt, lens - q_len + 1 + j, 0.29)
+        np.testing.assert_array_equal(o[:, j], o1)
+        np.testing.assert_array_equal(lse[:, j], l1)
+
+
+def test_multi_query_rows_ignore_later_keys():
+    q_len = 4
+    q, K, V, lens, kp, vp, bt = _multi_query_problem(48, q_len)
+    o, _ = oracle.multi_query_decode_attention(q, kp, vp, bt, lens, 0.3)
+    b, L = 0, int(lens[0])
+    last_pos = L - 1
+    page, row = bt[b, last_pos // 4], last_pos % 4
+    kp2, vp2 = kp.copy(), vp.copy()
+    kp2[page, row] += 5.0
+    vp2[page, row] -= 3.0
+    o2, _ = oracle.multi_query_decode_attention(q, kp2, vp2, bt, lens, 0.3)
+    np.testing.assert_array_equal(o2[b, :q_len - 1], o[b, :q_len - 1])  # earlier tokens cannot see it
+    assert not np.allclose(o2[b, q_len - 1], o[b, q_len - 1])
+
+
 # ---------------------------------------------------------------------------
 # Mutation checks: a plausible mistake planted in the oracle must fail a pin.
 # ---------------------------------------------------------------------------
@@ -332,3 +420,21 @@ def test_mutation_merge_sign_error_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "merge_states", wrong)
     with pytest.raises(AssertionError):
         test_cascade_prefix_suffix_merge_equals_flat()
+
+
+def test_mutation_causal_off_by_one_is_caught(monkeypatch):
+    real = oa.multi_query_decode_attention
+
+    def shifted(q, k_pool, v_pool, block_table, seq_lens, scale):
+        # every query token also sees the next token (limit one too far)
+        q_len = q.shape[1]
+        o = np.zeros(q.shape[:3] + (v_pool.shape[3],))
+        l = np.zeros(q.shape[:3])
+        for j in range(q_len):
+            lens_j = np.minimum(np.asarray(seq_lens) - q_len + 2 + j, np.asarray(seq_lens))
+            oj, lj = oracle.decode_attention(q[:, j], k_pool, v_pool, block_table, lens_j, scale)
+            o[:, j], l[:, j] = oj, lj
+        return o, l
+    monkeypatch.setattr(oracle, "multi_query_decode_attention", shifted)
+    with pytest.raises(AssertionError):
+        test_multi_query_matches_causal_torch_sdpa(3)
