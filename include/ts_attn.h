@@ -178,6 +178,54 @@ TS_API ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_pool,
                                               ts_dtype dtype, void* out, float* lse, void* stream);
 
 /*
+ * ts_fold_sq_factor - query tokens folded into the rows of one tile.
+ *
+ * TokenSpeed deep dive, section 7.2 (fold_sq_factor): the largest F with
+ * q_len % F == 0 and num_heads * F <= tile_rows, so that a tile holds
+ * num_heads * F rows and a sequence's q_len tokens take q_len / F tiles
+ * (64 heads, 4 tokens, 128-row tile: F = 2). Returns 0 if an argument is not
+ * positive. Host only.
+ */
+TS_API int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t tile_rows);
+
+/*
+ * ts_paged_decode_multi_workspace_size - workspace bytes for
+ * ts_paged_decode_multi_attn (B sequences of q_len query tokens). Returns 0 on
+ * invalid arguments.
+ */
+TS_API size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q, int32_t D);
+
+/*
+ * ts_paged_decode_multi_attn - decode with q_len new query tokens per sequence
+ * (speculative or multi-token verification).
+ *
+ * The q_len tokens' K/V rows are already in the cache (ts_kv_append once per
+ * token) and seq_lens counts them. Query token j of sequence b sits at
+ * position seq_lens[b] - q_len + j and attends tokens 0 .. that position
+ * (causal among the new tokens); each (token, head) row is otherwise the
+ * single-query decode of ts_paged_decode_attn. Tokens are folded into the
+ * kernel's per-kv-head rows (TokenSpeed deep dive, section 7.2): F of them
+ * with the g heads of a kv head when g * F is 1, 2, 4 or 8 (the largest such
+ * factor F of q_len); the others run as separate passes over the pages.
+ *
+ *   q             device [B, q_len, H_q, D] of dtype
+ *   out           device [B, q_len, H_q, D] of dtype (written)
+ *   lse           device float32 [B, q_len, H_q] (written) or NULL
+ *   seq_lens      device int32 [B], each >= q_len (rows of a token whose
+ *                 position would be negative get O = 0, LSE = -inf)
+ *   workspace     >= ts_paged_decode_multi_workspace_size(B, q_len, H_q, D)
+ *   other arguments, support and errors as in ts_paged_decode_attn;
+ *   q_len >= 1 (q_len == 1 gives exactly ts_paged_decode_attn's result).
+ */
+TS_API ts_status ts_paged_decode_multi_attn(const void* q, const void* k_pool, const void* v_pool,
+                                            const int32_t* block_table, int32_t bt_stride,
+                                            const int32_t* seq_lens, int32_t B, int32_t q_len,
+                                            int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                                            int32_t num_pages, float scale, ts_dtype dtype, void* out,
+                                            float* lse, void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/*
  * ts_merge_states - merge two attention states over disjoint key sets.
  *
  * Per row r: m = max(lse_a, lse_b), w_a = exp(lse_a - m), w_b = exp(lse_b - m),

@@ -69,6 +69,10 @@ _SIGNATURES = {
                                             _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
     "ts_paged_decode_attn_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32,
                                                     _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP]),
+    "ts_paged_decode_multi_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "ts_paged_decode_multi_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
+                                                  _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
+    "ts_fold_sq_factor": (_I32, [_I32, _I32, _I32]),
     "ts_merge_states": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, ctypes.c_int, _VP]),
     "ts_group_prefixes": (ctypes.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, ctypes.POINTER(PrefixGroupsC)]),
     "ts_cascade_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
@@ -202,6 +206,36 @@ def ts_paged_decode_attn_noalloc(q, k_pool, v_pool, block_table, seq_lens, scale
     _check(lib().ts_paged_decode_attn_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                               block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, ps, P,
                                               float(scale), _dt(q), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def ts_paged_decode_multi_workspace_size(B: int, q_len: int, H_q: int, D: int) -> int:
+    return int(lib().ts_paged_decode_multi_workspace_size(B, q_len, H_q, D))
+
+
+def ts_fold_sq_factor(num_heads: int, q_len: int, tile_rows: int = 128) -> int:
+    """Query tokens folded into a tile's rows (see include/ts_attn.h)."""
+    return int(lib().ts_fold_sq_factor(num_heads, q_len, tile_rows))
+
+
+def ts_paged_decode_multi_attn(q, k_pool, v_pool, block_table, seq_lens, scale: float, out=None, lse=None,
+                               workspace=None, stream=None, return_lse: bool = False):
+    """Decode with q_len query tokens per sequence, q [B, q_len, H_q, D]; seq_lens count
+    the new tokens (already appended). Returns ``out`` [B, q_len, H_q, D] (and ``lse``)."""
+    _require_i32(block_table, seq_lens)
+    B, q_len, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, q_len, H_q, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(ts_paged_decode_multi_workspace_size(B, q_len, H_q, D), q.device)
+    _check(lib().ts_paged_decode_multi_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                            block_table.shape[1], _ptr(seq_lens), B, q_len, H_q, H_kv, D,
+                                            ps, P, float(scale), _dt(q), _ptr(out), _ptr(lse),
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            _stream(stream)))
+    return (out, lse) if return_lse else out
 
 
 def ts_merge_states(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):

@@ -25,776 +25,21 @@
 //     memory is used g times. Dot products use packed fp32 FMA (FFMA2) and
 //     are reduced across the LPT lanes with warp shuffles; softmax runs in
 //     the log2 domain (scale * log2 e folded into q).
+//   * Several query tokens per sequence (speculative verify, q_len > 1) are
+//     folded into the rows of a warp (TokenSpeed deep dive, section 7.2,
+//     fold_sq_factor): F tokens x g heads = G rows per kv head, and a
+//     sequence becomes q_len / F "virtual sequences" of F tokens each. Row
+//     (f, head) of virtual sequence t attends the tokens before position
+//     L - q_len + t F + f + 1; only the last F - 1 tokens need a per-row mask.
 //   * At the end of a sequence's segment the groups merge by LSE with shuffles
 //     and lane group 0 writes either the final output (segment = whole
 //     sequence) or an fp32 partial state into one of the CTA's two workspace
 //     slots (first / last segment of its range). The merge kernel, launched
 //     with programmatic dependent launch, reduces the split sequences.
-#include <cmath>
-#include <cstdlib>
-#include <type_traits>
-
-#include "ts_common.cuh"
+#include "ts_paged_decode_kernel.cuh"
 
 namespace ts {
 namespace {
-
-constexpr int kMaxConsumerWarps = 8;
-// Three warp groups: group 0 holds the producer (warp 0; warps 1-3 leave after
-// the prologue), groups 1-2 hold the consumer warps (warp 4 + kv head).
-// Register split: launched at kLaunchRegs per thread; the producer group gives
-// registers back (setmaxnreg.dec, RegSplit) and the consumer groups take
-// them (setmaxnreg.inc): 128*56 + 256*224 == 384*168, or
-// 128*40 + 256*232 == 384*168 for group size 8.
-constexpr int kThreads = 384;
-constexpr int kFirstConsumerWarp = 4;
-constexpr int kLaunchRegs = 168;
-// Group size 8 keeps twice the query/accumulator registers per lane pair and
-// takes the larger consumer share.
-template <int G>
-struct RegSplit {
-  static constexpr int kProducer = G >= 8 ? 40 : 56;
-  static constexpr int kConsumer = G >= 8 ? 232 : 224;
-  static_assert(128 * kProducer + 256 * kConsumer <= kThreads * kLaunchRegs,
-                "register split exceeds the launch allocation");
-};
-constexpr int kMaxStages = 8;
-constexpr int kHeaderBytes = 1024;
-constexpr int kZeroRowOff = kHeaderBytes;  // one zeroed token row (<= 4 KB)
-constexpr uint32_t kFlagFirst = 1u, kFlagLast = 2u, kFlagEnd = 4u, kFlagBadPage = 8u;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-// Largest score excess over the reference max (log2 units) before the
-// accumulators are rescaled: unnormalised weights stay <= 2^8.
-constexpr float kRescaleSlack = 8.0f;
-
-struct StageDesc {
-  int32_t b;         // sequence
-  int32_t valid;     // tokens present in this page
-  uint32_t flags;    // kFlag*
-  int32_t out_slot;  // -1: write the final output; else partial slot index
-};
-
-struct PagedParams {
-  const void* q;
-  const void* k_pool;
-  const void* v_pool;
-  const int32_t* block_table;
-  const int32_t* seq_lens;
-  int32_t bt_stride, B, H_q, H_kv, page_size, num_pages;
-  float scale_log2;  // scale * log2(e)
-  void* out;
-  float* lse;
-  uint32_t* err_word;
-  int2* split_info;  // per sequence: {first CTA, (parts << 1) | slot of first part}
-  float* part_o;     // [2 * gridDim.x, H_q, D]
-  float* part_lse;   // [2 * gridDim.x, H_q]
-  // Shared-prefix (cascade) mode: a grouped sequence's own pages start after
-  // its group's prefix pages, and the prefix attention state is merged in.
-  const int32_t* group_of;    // [B] group or -1
-  const int32_t* prefix_len;  // [groups] shared tokens (whole pages)
-  const float* prefix_o;      // [B, H_q, D] normalised prefix output (fp32)
-  const float* prefix_lse;    // [B, H_q] prefix LSE (natural log)
-  int32_t num_stages;
-  uint32_t stage_bytes;  // bytes per stage (K rows + V rows + q rows, aligned)
-  uint32_t stages_off;   // offset of the first stage in dynamic shared memory
-  uint32_t page_bytes;   // bytes of one full page of K (or V), all kv heads
-  int32_t chunk_rows;    // token rows per stage (a page, or a contiguous part of one)
-  int32_t seq_units;     // work units a sequence costs beyond its pages (its q load and epilogue)
-  uint32_t kv_area;      // chunk_rows * row_bytes: K (and V) area of a stage
-  uint32_t row_bytes;    // bytes of one token row of K (or V), all kv heads
-  uint32_t q_bytes;      // bytes of one sequence's query rows
-};
-
-template <typename T>
-struct Elem;
-template <>
-struct Elem<float> {
-  static constexpr int kVE = 4;  // elements per 16-byte vector
-  // Converts word pair w (of a 16-byte vector) to a float2.
-  __device__ static __forceinline__ float2 pair(const uint4& v, int w) {
-    const uint32_t a = w == 0 ? v.x : v.z;
-    const uint32_t b = w == 0 ? v.y : v.w;
-    return make_float2(__uint_as_float(a), __uint_as_float(b));
-  }
-  static constexpr int kPairs = 2;  // float2 pairs per vector
-};
-template <>
-struct Elem<__nv_bfloat16> {
-  static constexpr int kVE = 8;
-  __device__ static __forceinline__ float2 pair(const uint4& v, int w) {
-    const uint32_t x = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
-    return bf16x2_to_float2(x);
-  }
-  static constexpr int kPairs = 4;
-};
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-template <typename T, int D, int G>
-struct Cfg {
-  static constexpr int kES = sizeof(T);
-  static constexpr int kVE = Elem<T>::kVE;
-  static constexpr int kDPL = (G <= 4) ? 16 : 8;        // dims per lane
-  static constexpr int kNV = kDPL / kVE;                // 16-byte vectors per lane
-  static constexpr int kLPT = D / kDPL;                 // lanes per token
-  static constexpr int kNG = 32 / kLPT;                 // token groups per warp
-  static constexpr int kTPG0 = 16 / kNG;
-  static constexpr int kTPG = (kTPG0 * G > 16) ? (16 / G) : kTPG0;  // tokens per group per pass
-  static constexpr int kPairsPL = kDPL / 2;             // float2 per lane per head
-  static_assert(kLPT >= 2 && kLPT <= 32 && (32 % kLPT) == 0, "lane split");
-  static_assert(kTPG >= 1, "tokens per group");
-};
-
-// Tokens of sequence b covered by its group's shared prefix (prefix mode).
-template <bool kPfx>
-__device__ __forceinline__ int prefix_tokens(const PagedParams& p, int b) {
-  if constexpr (kPfx) {
-    const int g = p.group_of[b];
-    return g >= 0 ? p.prefix_len[g] : 0;
-  } else {
-    return 0;
-  }
-}
-
-// Writes the output of a sequence with no own tokens: O = 0, LSE = -inf, or
-// the prefix state alone in prefix mode.
-template <typename T, bool kPfx>
-__device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k) {
-  const bool grouped = kPfx && p.group_of[b] >= 0;
-  T* out = static_cast<T*>(p.out) + static_cast<int64_t>(b) * p.H_q * D;
-  const float* po = grouped ? p.prefix_o + static_cast<int64_t>(b) * p.H_q * D : nullptr;
-  for (int i = 0; i < p.H_q * D; ++i) out[i] = static_cast<T>(grouped ? po[i] : 0.0f);
-  if (p.lse)
-    for (int h = 0; h < p.H_q; ++h)
-      p.lse[static_cast<int64_t>(b) * p.H_q + h] =
-          grouped ? p.prefix_lse[static_cast<int64_t>(b) * p.H_q + h] : -INFINITY;
-  p.split_info[b] = make_int2(k, 0);
-}
-
-template <typename T, int D, int G, bool kPfx>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedParams p) {
-  using C = Cfg<T, D, G>;
-  extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int n_consumer = p.H_kv;  // one consumer warp per kv head
-  const int nwarps = blockDim.x >> 5;
-  const int k = blockIdx.x;
-  const int G_ctas = gridDim.x;
-  const int ps = p.page_size;
-  const int S = p.num_stages;
-
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + 64);
-  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + 128);
-  long long* warp_tot = reinterpret_cast<long long*>(smem + 512);
-  int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
-  unsigned char* stages = smem + p.stages_off;
-
-  // Programmatic dependent launch: this kernel may start while the previous
-  // kernel of the stream finishes. Until griddepcontrol.wait it only reads
-  // seq_lens, the block table and the prefix-group metadata; every other read
-  // and every global write comes after the wait.
-  pdl_launch_dependents();
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), n_consumer);
-    }
-    s_start[0] = -1;
-    s_start[1] = 0;
-    fence_mbar_init();
-  }
-  // A row of zeros that masked rows of empty units read instead of the stage.
-  for (int i = tid; i < static_cast<int>(p.row_bytes / 4); i += blockDim.x)
-    reinterpret_cast<uint32_t*>(smem + kZeroRowOff)[i] = 0u;
-
-  // ---- prologue: total pages T and this CTA's range [start, end) ----------
-  const int B = p.B;
-  const int chunk = (B + blockDim.x - 1) / blockDim.x;
-  const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
-  // Work units: a sequence with np > 0 own pages counts np + seq_units, the
-  // first seq_units standing for its fixed cost (query load, epilogue); they
-  // carry no page. The units of the batch are cut evenly across the CTAs.
-  const int A = p.seq_units;
-  long long mine = 0;
-  bool has_empty = false;
-  for (int b = lo; b < hi; ++b) {
-    const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
-    if (L > 0)
-      mine += (L + ps - 1) / ps + A;
-    else if (b % G_ctas == k)
-      has_empty = true;
-  }
-  if (has_empty) {  // sequences with no own tokens are written here, after the wait
-    pdl_wait_primary();
-    for (int b = lo; b < hi; ++b)
-      if (p.seq_lens[b] - prefix_tokens<kPfx>(p, b) <= 0 && b % G_ctas == k)
-        write_empty_sequence<T, kPfx>(p, D, b, k);
-  }
-  long long incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  long long wbase = 0, total = 0;
-  for (int w = 0; w < nwarps; ++w) {
-    const long long v = warp_tot[w];
-    if (w < warp) wbase += v;
-    total += v;
-  }
-  const long long excl = wbase + incl - mine;
-  // Balanced cut: the first (total % G) CTAs take one page more. Non-empty
-  // ranges are contiguous, so a sequence's pages always lie in consecutive
-  // non-empty CTAs (the merge relies on it).
-  const long long q_pages = total / G_ctas, r_pages = total % G_ctas;
-  const long long start = k * q_pages + min(static_cast<long long>(k), r_pages);
-  const long long end = start + q_pages + (k < r_pages ? 1 : 0);
-  if (start < end && excl <= start && start < excl + mine) {
-    long long off = excl;
-    for (int b = lo; b < hi; ++b) {
-      const int L = p.seq_lens[b] - prefix_tokens<kPfx>(p, b);
-      const long long np = L > 0 ? (L + ps - 1) / ps + A : 0;
-      if (start < off + np) {
-        s_start[0] = b;
-        s_start[1] = static_cast<int>(start - off);
-        break;
-      }
-      off += np;
-    }
-  }
-  __syncthreads();
-
-  if (warp < kFirstConsumerWarp) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<G>::kProducer));
-    if (warp != 0) return;
-    // ======================= producer warp ================================
-    int it = 0;
-    int ps_stage = 0, ps_phase = 0;  // it % S and (it / S) & 1, kept incrementally
-    bool aborted = false;
-    if (start < end && s_start[0] >= 0) {
-      const uint64_t pol = policy_evict_first();
-      // The range is walked in chunks of up to 32 pages of one sequence. The
-      // metadata of the next chunk (sequence lengths, 32 lengths per warp load,
-      // and the chunk's block-table entries, one per lane) is loaded while the
-      // current chunk's pages are issued, so a sequence boundary costs no
-      // dependent global-load latency in the copy stream.
-      long long g = start;   // global index of the next work unit
-      int b = s_start[0];    // sequence of the next unit
-      int pg = s_start[1];   // its unit index within the sequence (pages start at unit A;
-                             // within a segment pg counts pages)
-      bool first_seg = true;
-      int seg_left = 0, seg_L = 0, seg_np = 0, seg_pre = 0, seg_slot = -1;
-      int wb = b;                                   // lengths window: sequences wb .. wb+31
-      auto load_len = [&](int base, int& pre_out) {  // this lane's sequence base+lane
-        const int bb = base + lane;
-        pre_out = 0;
-        if (bb >= B) return -1;
-        pre_out = prefix_tokens<kPfx>(p, bb);
-        return max(p.seq_lens[bb] - pre_out, 0);
-      };
-      int win_pre, nxt_pre;
-      int win_len = load_len(wb, win_pre);
-      int nxt_len = load_len(wb + 32, nxt_pre);
-      // a chunk: `cnt` pages pg0.. of sequence b (own length L), partial slot
-      // `slot`, chunk flags, and the split_info value to write (-1: none)
-      constexpr int kSegFirst = 1, kSegLast = 2;
-      struct Chunk {
-        int b, pg0, cnt, L, slot, flags, split;
-      };
-      // entries past the row (length inconsistent with bt_stride) count as bad pages
-      auto load_pid = [&](const Chunk& c, int pre) {
-        const int idx = pre / ps + c.pg0 + lane;  // prefix pages come first in the row
-        if (lane < c.cnt && idx < p.bt_stride)
-          return p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + idx];
-        return -1;
-      };
-      // fills c with the next chunk of the range (c.cnt == 0 at its end) and
-      // returns this lane's block-table entry of it
-      auto next_chunk = [&](Chunk& c) {
-        c.cnt = 0;
-        if (g >= end) return -1;
-        if (seg_left == 0) {
-          while (true) {
-            if (b >= B) return -1;
-            while (b >= wb + 32) {  // slide the lengths window
-              win_len = nxt_len;
-              win_pre = nxt_pre;
-              wb += 32;
-              nxt_len = load_len(wb + 32, nxt_pre);
-            }
-            const int L = __shfl_sync(0xffffffffu, win_len, b - wb);
-            const int np = (L + ps - 1) / ps;
-            if (np == 0 || pg >= np + A) {
-              ++b;
-              pg = 0;
-              continue;
-            }
-            if (pg < A) {  // the sequence's overhead units: no page
-              const int skip = static_cast<int>(min(static_cast<long long>(A - pg), end - g));
-              g += skip;
-              pg += skip;
-              if (g >= end) return -1;
-            }
-            pg -= A;  // from here on: page index
-            seg_L = L;
-            seg_np = np;
-            seg_pre = __shfl_sync(0xffffffffu, win_pre, b - wb);
-            break;
-          }
-          const int n_here = static_cast<int>(min(static_cast<long long>(seg_np - pg), end - g));
-          const bool complete = (pg == 0) && (n_here == seg_np);
-          seg_slot = complete ? -1 : (first_seg ? 2 * k : 2 * k + 1);
-          c.split = -1;
-          if (pg == 0) {  // the sequence starts here: record how many CTAs hold its pages
-            const long long last = g + seg_np - 1;  // global unit of its last page
-            const long long big = r_pages * (q_pages + 1);
-            const int k1 = static_cast<int>(last < big ? last / (q_pages + 1)
-                                                       : r_pages + (last - big) / max(q_pages, 1ll));
-            c.split = ((k1 - k + 1) << 1) | (first_seg ? 0 : 1);
-          }
-          first_seg = false;
-          seg_left = n_here;
-          c.flags = kSegFirst;
-        } else {
-          c.flags = 0;
-          c.split = -1;
-        }
-        c.b = b;
-        c.pg0 = pg;
-        c.cnt = min(32, seg_left);
-        c.L = seg_L;
-        c.slot = seg_slot;
-        seg_left -= c.cnt;
-        if (seg_left == 0) c.flags |= kSegLast;
-        pg += c.cnt;
-        g += c.cnt;
-        // inside a segment pg is a page index; a segment ends at the sequence's
-        // end (next sequence, unit 0) or at the range's end (walk over)
-        if (seg_left == 0 && pg >= seg_np) {
-          ++b;
-          pg = 0;
-        }
-        return load_pid(c, seg_pre);
-      };
-      Chunk cur, nxt;
-      int pid = next_chunk(cur);
-      pdl_wait_primary();  // the metadata of the first chunk is loaded; copies and writes follow
-      while (cur.cnt > 0 && !aborted) {
-        const int pid_nxt = next_chunk(nxt);
-        if (cur.split >= 0 && lane == 0) p.split_info[cur.b] = make_int2(k, cur.split);
-        const int np_cur = (cur.L + ps - 1) / ps;
-        for (int i = 0; i < cur.cnt; ++i) {
-          const int page = __shfl_sync(0xffffffffu, pid, i);
-          const int pidx = cur.pg0 + i;
-          const bool ok = page >= 0 && page < p.num_pages;
-          const int rows = ok ? ((pidx == np_cur - 1) ? (cur.L - pidx * ps) : ps) : 0;
-          const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
-          for (int c = 0; c < nchunks; ++c) {
-            if (lane == 0) {
-              const int s = ps_stage;
-              if (it >= S && !mbar_wait(smem_u32(&empty[s]), ps_phase ^ 1)) {
-                set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
-                aborted = true;
-              } else {
-                const int r0 = c * p.chunk_rows;
-                const int valid = max(0, min(rows - r0, p.chunk_rows));
-                uint32_t flags = ((cur.flags & kSegFirst) && i == 0 && c == 0 ? kFlagFirst : 0u) |
-                                 ((cur.flags & kSegLast) && i == cur.cnt - 1 && c == nchunks - 1 ? kFlagLast : 0u);
-                if (!ok) {
-                  flags |= kFlagBadPage;
-                  set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
-                }
-                StageDesc d;
-                d.b = cur.b;
-                d.valid = valid;
-                d.flags = flags;
-                d.out_slot = cur.slot;
-                desc[s] = d;
-                const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
-                const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
-                const uint32_t full_bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
-                const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-                if (bytes) {
-                  const size_t off = static_cast<size_t>(page) * p.page_bytes +
-                                     static_cast<size_t>(r0) * p.row_bytes;
-                  bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
-                  bulk_g2s_hint(st + p.kv_area, static_cast<const char*>(p.v_pool) + off, bytes,
-                                full_bar, pol);
-                }
-                if (qb)
-                  bulk_g2s(st + 2 * p.kv_area,
-                           static_cast<const char*>(p.q) + static_cast<size_t>(cur.b) * p.q_bytes, qb,
-                           full_bar);
-              }
-            }
-            aborted = __shfl_sync(0xffffffffu, aborted, 0);
-            if (aborted) break;
-            ++it;
-            if (++ps_stage == S) {
-              ps_stage = 0;
-              ps_phase ^= 1;
-            }
-          }
-          if (aborted) break;
-        }
-        cur = nxt;
-        pid = pid_nxt;
-      }
-    }
-    if (lane == 0) {
-      if (!aborted) {
-        const int s = it % S;
-        if (it >= S && !mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1)) {
-          set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
-          aborted = true;
-        } else {
-          desc[s].flags = kFlagEnd;
-          mbar_arrive(smem_u32(&full[s]));
-        }
-      }
-      if (aborted) {
-        // Let any copy already issued land before the CTA's shared memory is released.
-        for (int j = max(0, it - S); j < it; ++j)
-          mbar_wait(smem_u32(&full[j % S]), (j / S) & 1);
-      }
-    }
-    return;
-  }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<G>::kConsumer));
-  if (warp - kFirstConsumerWarp >= n_consumer) return;
-  pdl_wait_primary();  // before the consumers' global reads (prefix state) and writes
-
-  // ========================= consumer warps ================================
-  const int h = warp - kFirstConsumerWarp;  // kv head of this warp
-  const int j = lane / C::kLPT;
-  const int l = lane % C::kLPT;
-  const int tokens_per_pass = C::kNG * C::kTPG;
-  const int npass = (p.chunk_rows + tokens_per_pass - 1) / tokens_per_pass;
-  const int H_kv = p.H_kv;
-
-  int dim_off[C::kNV];
-  uint32_t lane_off[C::kNV];  // byte offset of this lane's vectors within a token row
-#pragma unroll
-  for (int v = 0; v < C::kNV; ++v) {
-    dim_off[v] = v * (D / C::kNV) + C::kVE * l;
-    lane_off[v] = static_cast<uint32_t>((h * D + dim_off[v]) * C::kES);
-  }
-  const uint32_t zero_row = smem_u32(smem + kZeroRowOff);
-  const uint32_t row_stride = p.row_bytes;
-
-  float2 qv[G][C::kPairsPL];
-  float2 acc[G][C::kPairsPL];
-  float m[G], lsum[G];
-
-  int it = 0, s = 0, phase = 0;  // s = it % S, phase = (it / S) & 1
-  while (true) {
-    if (!mbar_wait(smem_u32(&full[s]), phase)) {
-      set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
-      break;
-    }
-    const StageDesc d = desc[s];
-    if (d.flags & kFlagEnd) break;
-    const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-    const uint32_t kbase = st, vbase = st + p.kv_area, qbase = st + 2 * p.kv_area;
-
-    if (d.flags & kFlagFirst) {
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        m[hh] = -INFINITY;
-        lsum[hh] = 0.f;
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v) {
-          const uint4 raw =
-              lds128(qbase + ((h * G + hh) * D + dim_off[v]) * C::kES);
-#pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) {
-            const float2 f = Elem<T>::pair(raw, w);
-            qv[hh][v * Elem<T>::kPairs + w] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-            acc[hh][v * Elem<T>::kPairs + w] = make_float2(0.f, 0.f);
-          }
-        }
-      }
-    }
-
-    const int valid = d.valid;
-    // A full stage (every row valid, passes cover it exactly) needs no row
-    // clamping and no score masking: the common case gets its own copy.
-    auto run_passes = [&](auto full_tag) {
-    constexpr bool kFull = decltype(full_tag)::value;
-    for (int pass = 0; pass < npass; ++pass) {
-      const int t0 = pass * tokens_per_pass + j * C::kTPG;
-      // Rows past `valid` read the last valid row (their scores are masked and
-      // their weights are 0); a unit with no valid row reads the zero row. So the
-      // token loop has no branches and its dependency chains interleave freely.
-      float sc[C::kTPG][G];
-      // V rows are read together with the K rows, so their shared-memory
-      // latency hides behind the scores and the softmax
-      uint4 vv[C::kTPG][C::kNV];
-      uint32_t row_off[C::kTPG];
-#pragma unroll
-      for (int i = 0; i < C::kTPG; ++i)
-        row_off[i] = kFull ? (t0 + i) * row_stride
-                           : (valid > 0 ? min(t0 + i, valid - 1) * row_stride : 0xffffffffu);
-#pragma unroll
-      for (int i = 0; i < C::kTPG; ++i) {
-        const uint32_t ra = row_off[i] != 0xffffffffu ? vbase + row_off[i] : zero_row;
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v) vv[i][v] = lds128(ra + lane_off[v]);
-      }
-#pragma unroll
-      for (int i = 0; i < C::kTPG; ++i) {
-        const uint32_t ra = row_off[i] != 0xffffffffu ? kbase + row_off[i] : zero_row;
-        uint4 kv[C::kNV];
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v) kv[v] = lds128(ra + lane_off[v]);
-        float2 kf[C::kPairsPL];  // the row widened once, used by all G heads
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) kf[v * Elem<T>::kPairs + w] = Elem<T>::pair(kv[v], w);
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int x = 0; x < C::kPairsPL; ++x) a = __ffma2_rn(qv[hh][x], kf[x], a);
-          sc[i][hh] = a.x + a.y;
-        }
-      }
-#pragma unroll
-      for (int o = 1; o < C::kLPT; o <<= 1)
-#pragma unroll
-        for (int i = 0; i < C::kTPG; ++i)
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) sc[i][hh] += __shfl_xor_sync(0xffffffffu, sc[i][hh], o);
-#pragma unroll
-      for (int i = 0; i < C::kTPG; ++i) {
-        const bool in = kFull || t0 + i < valid;
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) sc[i][hh] = in ? sc[i][hh] : -INFINITY;
-      }
-
-      // Online softmax with a lazily moved reference max: m[] only moves when a
-      // score exceeds it by more than kRescaleSlack (log2 units), so p <= 2^slack
-      // and the accumulators are rescaled only a few times per sequence. The
-      // decision is made warp-uniform so the rescale branch never diverges.
-      float mx[G];
-      bool need = false;
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        mx[hh] = sc[0][hh];
-#pragma unroll
-        for (int i = 1; i < C::kTPG; ++i) mx[hh] = fmaxf(mx[hh], sc[i][hh]);
-        need |= mx[hh] > m[hh] + kRescaleSlack;
-      }
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float mnew = fmaxf(m[hh], mx[hh]);
-          const float alpha = m[hh] == -INFINITY ? 0.f : fast_exp2(m[hh] - mnew);
-          m[hh] = mnew;
-          lsum[hh] *= alpha;
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __fmul2_rn(acc[hh][x], a2);
-        }
-      }
-      float pr[C::kTPG][G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float msafe = m[hh] == -INFINITY ? 0.f : m[hh];
-        float ls = lsum[hh];
-#pragma unroll
-        for (int i = 0; i < C::kTPG; ++i) {
-          pr[i][hh] = fast_exp2(sc[i][hh] - msafe);
-          ls += pr[i][hh];
-        }
-        lsum[hh] = ls;
-      }
-#pragma unroll
-      for (int i = 0; i < C::kTPG; ++i) {
-        float2 vf[C::kPairsPL];
-#pragma unroll
-        for (int v = 0; v < C::kNV; ++v)
-#pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) vf[v * Elem<T>::kPairs + w] = Elem<T>::pair(vv[i][v], w);
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
-#pragma unroll
-          for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __ffma2_rn(p2, vf[x], acc[hh][x]);
-        }
-      }
-    }
-    };
-    if (valid == p.chunk_rows && p.chunk_rows % tokens_per_pass == 0)
-      run_passes(std::integral_constant<bool, true>());
-    else
-      run_passes(std::integral_constant<bool, false>());
-
-    if (d.flags & kFlagLast) {
-      // Merge the NG token groups of this warp (lanes with equal l hold the
-      // same dims of different token groups) by LSE, as a reduce-scatter:
-      // weights first (group max M, w_j = 2^(m_j - M), total l), then each
-      // butterfly step hands half of the still-shared values to the partner,
-      // so after log2(NG) steps every lane owns NT/NG finished values and
-      // all 32 lanes write the output.
-      constexpr int P = C::kPairsPL;     // float2 per lane per head
-      constexpr int NT = G * P;          // float2 per lane
-      constexpr int NF = NT / C::kNG;    // float2 each lane owns at the end
-      static_assert(NT % C::kNG == 0 && NF >= 1, "reduce-scatter split");
-      static_assert((G & (G - 1)) == 0, "heads per kv head: a power of two");
-      float M[G], Lt[G];
-      float2 r[NT];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float mx = m[hh];
-#pragma unroll
-        for (int o = C::kLPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float ms = mx == -INFINITY ? 0.f : mx;
-        const float w = fast_exp2(m[hh] - ms);  // 0 for a group that saw no token
-        float lw = lsum[hh] * w;
-#pragma unroll
-        for (int o = C::kLPT; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-        M[hh] = mx;
-        Lt[hh] = lw;
-        const float2 w2 = make_float2(w, w);
-#pragma unroll
-        for (int x = 0; x < P; ++x) r[hh * P + x] = __fmul2_rn(acc[hh][x], w2);
-      }
-      int own = 0;  // flattened index (head * P + pair) of r[0] after the steps
-#pragma unroll
-      for (int st = 0; (C::kLPT << st) < 32; ++st) {
-        const int o = C::kLPT << st;
-        const int half = (NT >> st) / 2;
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-          const float2 send = up ? r[i] : r[i + half];
-          const float2 keep = up ? r[i + half] : r[i];
-          float2 recv;
-          recv.x = __shfl_xor_sync(0xffffffffu, send.x, o);
-          recv.y = __shfl_xor_sync(0xffffffffu, send.y, o);
-          r[i] = make_float2(keep.x + recv.x, keep.y + recv.y);
-        }
-        own += up ? half : 0;
-      }
-      // r[i] now holds flattened value own + i: head (own + i) / P, pair
-      // (own + i) % P of this lane's dims. Finish them per whole 16-byte
-      // vector when the share allows it.
-      constexpr int U = (NF % Elem<T>::kPairs == 0) ? Elem<T>::kPairs : 1;
-      auto pick = [&](const float (&a)[G], int hh) {
-        float v = a[0];
-#pragma unroll
-        for (int q = 1; q < G; ++q) v = hh == q ? a[q] : v;
-        return v;
-      };
-      bool grouped = false;
-      if constexpr (kPfx) grouped = p.group_of[d.b] >= 0;
-      const int64_t row0 = static_cast<int64_t>(d.b) * p.H_q + h * G;  // first query head of the warp
-      // normaliser c_s of the own-token state and weight c_p of the prefix
-      // state (0 outside prefix mode), and the row's final LSE (log2 units)
-      auto finish = [&](int hh, float& cs, float& cp, float& lse2) {
-        const float Mh = pick(M, hh), Lh = pick(Lt, hh);
-        cs = Lh > 0.f ? __fdividef(1.0f, Lh) : 0.f;
-        cp = 0.f;
-        lse2 = Lh > 0.f ? Mh + __log2f(Lh) : -INFINITY;
-        if (kPfx && grouped && d.out_slot < 0) {
-          const float lp2 = p.prefix_lse[row0 + hh] * kLog2e;
-          const float Mx = fmaxf(lse2, lp2);
-          const float ws = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - Mx);
-          const float wp = lp2 == -INFINITY ? 0.f : fast_exp2(lp2 - Mx);
-          const float den = ws + wp;
-          const float iden = den > 0.f ? __fdividef(1.0f, den) : 0.f;
-          cs *= ws * iden;
-          cp = wp * iden;
-          lse2 = den > 0.f ? Mx + __log2f(den) : -INFINITY;
-        }
-      };
-#pragma unroll
-      for (int c = 0; c < NF; c += U) {
-        const int xf = own + c;
-        const int hh = xf / P, x = xf % P;
-        const int dim = (x / Elem<T>::kPairs) * (D / C::kNV) + C::kVE * l + 2 * (x % Elem<T>::kPairs);
-        float cs, cp, lse2;
-        finish(hh, cs, cp, lse2);
-        float2 val[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) val[u] = make_float2(r[c + u].x * cs, r[c + u].y * cs);
-        if (d.out_slot < 0) {
-          if (cp != 0.f) {
-            const float* po = p.prefix_o + (row0 + hh) * D + dim;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const float2 pv = *reinterpret_cast<const float2*>(po + 2 * u);
-              val[u] = make_float2(val[u].x + pv.x * cp, val[u].y + pv.y * cp);
-            }
-          }
-          T* o = static_cast<T*>(p.out) + (row0 + hh) * D + dim;
-          if constexpr (sizeof(T) == 2) {
-            if constexpr (U == 4) {
-              *reinterpret_cast<uint4*>(o) =
-                  make_uint4(float2_to_bf16x2(val[0].x, val[0].y), float2_to_bf16x2(val[1].x, val[1].y),
-                             float2_to_bf16x2(val[2].x, val[2].y), float2_to_bf16x2(val[3].x, val[3].y));
-            } else {
-#pragma unroll
-              for (int u = 0; u < U; ++u)
-                *reinterpret_cast<uint32_t*>(o + 2 * u) = float2_to_bf16x2(val[u].x, val[u].y);
-            }
-          } else {
-            if constexpr (U == 2) {
-              *reinterpret_cast<float4*>(o) = make_float4(val[0].x, val[0].y, val[1].x, val[1].y);
-            } else {
-#pragma unroll
-              for (int u = 0; u < U; ++u) *reinterpret_cast<float2*>(o + 2 * u) = val[u];
-            }
-          }
-        } else {
-          float* o = p.part_o + (static_cast<int64_t>(d.out_slot) * p.H_q + h * G + hh) * D + dim;
-          if constexpr (U % 2 == 0) {
-#pragma unroll
-            for (int u = 0; u < U; u += 2)
-              *reinterpret_cast<float4*>(o + 2 * u) = make_float4(val[u].x, val[u].y, val[u + 1].x, val[u + 1].y);
-          } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u) *reinterpret_cast<float2*>(o + 2 * u) = val[u];
-          }
-        }
-      }
-      {  // lane q < G writes head q's LSE (every lane computes one, no divergence)
-        const int q = lane & (G - 1);
-        float cs, cp, lse2;
-        finish(q, cs, cp, lse2);
-        if (lane < G) {
-          if (d.out_slot < 0) {
-            if (p.lse) p.lse[row0 + q] = lse2 * kLn2;
-          } else {
-            p.part_lse[static_cast<int64_t>(d.out_slot) * p.H_q + h * G + q] = lse2 * kLn2;
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    ++it;
-    if (++s == S) {
-      s = 0;
-      phase ^= 1;
-    }
-  }
-}
 
 // Reduces the partial states of sequences cut across CTAs (one warp per
 // (sequence, query head)); sequences written whole by the main kernel are
@@ -806,19 +51,19 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
   pdl_launch_dependents();  // a following PDL-aware kernel may start its prologue
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = warp / p.H_q, hq = warp % p.H_q;
+  const int b = warp / p.rows, hq = warp % p.rows;  // virtual sequence, query row
   if (b >= p.B) return;
   const int2 info = p.split_info[b];
   const int nparts = info.y >> 1;
   if (nparts <= 1) return;
   const int k0 = info.x, slot0 = info.y & 1;
-  const int64_t row = static_cast<int64_t>(b) * p.H_q + hq;
+  const int64_t row = static_cast<int64_t>(b) * p.rows + hq;
   const bool grouped = kPfx && p.group_of[b] >= 0;
   const float lse_pre = grouped ? p.prefix_lse[row] : -INFINITY;
   float mx = lse_pre;
   for (int i = 0; i < nparts; ++i) {
     const int slot = i == 0 ? 2 * k0 + slot0 : 2 * (k0 + i);
-    mx = fmaxf(mx, p.part_lse[static_cast<int64_t>(slot) * p.H_q + hq]);
+    mx = fmaxf(mx, p.part_lse[static_cast<int64_t>(slot) * p.rows + hq]);
   }
   const float ms = mx == -INFINITY ? 0.f : mx;
   float wsum = 0.f;
@@ -827,9 +72,9 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
     wsum = 0.f;
     for (int i = 0; i < nparts; ++i) {
       const int slot = i == 0 ? 2 * k0 + slot0 : 2 * (k0 + i);
-      const float w = __expf(p.part_lse[static_cast<int64_t>(slot) * p.H_q + hq] - ms);
+      const float w = __expf(p.part_lse[static_cast<int64_t>(slot) * p.rows + hq] - ms);
       const float4 o =
-          *reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(slot) * p.H_q + hq) * D + d0);
+          *reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(slot) * p.rows + hq) * D + d0);
       a.x += w * o.x;
       a.y += w * o.y;
       a.z += w * o.z;
@@ -846,7 +91,7 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, i
       wsum += w;
     }
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-    T* out = static_cast<T*>(p.out) + (static_cast<int64_t>(b) * p.H_q + hq) * D + d0;
+    T* out = static_cast<T*>(p.out) + row * D + d0;
     if constexpr (sizeof(T) == 2) {
       uint2 pk;
       pk.x = float2_to_bf16x2(a.x * inv, a.y * inv);
@@ -864,10 +109,10 @@ using KernelFn = void (*)(const PagedParams);
 template <typename T, int D, bool kPfx>
 KernelFn pick_g(int g) {
   switch (g) {
-    case 1: return paged_decode_kernel<T, D, 1, kPfx>;
-    case 2: return paged_decode_kernel<T, D, 2, kPfx>;
-    case 4: return paged_decode_kernel<T, D, 4, kPfx>;
-    case 8: return paged_decode_kernel<T, D, 8, kPfx>;
+    case 1: return paged_decode_kernel<T, D, 1, kPfx, false>;
+    case 2: return paged_decode_kernel<T, D, 2, kPfx, false>;
+    case 4: return paged_decode_kernel<T, D, 4, kPfx, false>;
+    case 8: return paged_decode_kernel<T, D, 8, kPfx, false>;
     default: return nullptr;
   }
 }
@@ -915,19 +160,34 @@ WsLayout workspace_layout(int B, int H_q, int D, int n_ctas) {
 
 }  // namespace
 
-// Launches the paged split-KV kernel pair; `pre` non-null selects prefix
-// (cascade) mode.
-ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void* v_pool,
-                                   const int32_t* block_table, int32_t bt_stride,
-                                   const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
-                                   int32_t D, int32_t page_size, int32_t num_pages, float scale,
-                                   ts_dtype dtype, void* out, float* lse, void* workspace,
-                                   size_t workspace_bytes, cudaStream_t stream, const char* who,
-                                   const PrefixInputs* pre) {
+// Query tokens folded into one warp's rows for q_len tokens and g query heads
+// per kv head: the page's fold_sq_factor rule (largest factor F of q_len with
+// g F rows in the tile, TokenSpeed deep dive section 7.2) for an 8-row tile,
+// restricted to the row counts the kernel is compiled for (g F in 1, 2, 4, 8).
+int gqa_fold(int g, int q_len) {
+  for (int f = q_len; f >= 1; --f) {
+    const int r = g * f;
+    if (q_len % f == 0 && r <= 8 && (r & (r - 1)) == 0) return f;
+  }
+  return 1;
+}
+
+// Launches the paged split-KV kernel pair for q_len query tokens per
+// sequence; `pre` non-null selects prefix (cascade) mode (q_len 1 only).
+ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                            int32_t B, int32_t q_len, int32_t H_q, int32_t H_kv, int32_t D,
+                            int32_t page_size, int32_t num_pages, float scale, ts_dtype dtype,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream, const char* who, const PrefixInputs* pre) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
       bt_stride <= 0)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
                 who, B, H_q, H_kv, D, page_size, num_pages, bt_stride);
+  if (q_len < 1 || (pre != nullptr && q_len != 1) ||
+      static_cast<long long>(B) * q_len > INT32_MAX / 2)
+    return fail(TS_ERR_INVALID_ARG, "%s: q_len=%d (>= 1; 1 with shared prefixes; B * q_len < 2^30)",
+                who, q_len);
   if (H_q % H_kv != 0)
     return fail(TS_ERR_INVALID_ARG, "%s: H_q=%d not a multiple of H_kv=%d", who, H_q, H_kv);
   if (dtype != TS_F32 && dtype != TS_BF16)
@@ -941,17 +201,24 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
     return fail(TS_ERR_UNSUPPORTED, "%s: H_kv=%d (supported 1, 2, 4, 8)", who, H_kv);
   if (page_size != 8 && page_size != 16 && page_size != 32)
     return fail(TS_ERR_UNSUPPORTED, "%s: page_size=%d (supported 8, 16, 32)", who, page_size);
-  KernelFn fn = pick_kernel(dtype, D, g, pre != nullptr);
+  const int fold = (g & (g - 1)) == 0 ? gqa_fold(g, q_len) : 1;
+  const int steps = q_len / fold;
+  const int Bv = B * steps;           // virtual sequences
+  const int rows = fold * H_q;        // query rows of a virtual sequence
+  KernelFn fn = q_len == 1 ? pick_kernel(dtype, D, g, pre != nullptr)
+                           : pick_paged_multi_kernel(dtype, D, g * fold);
   if (!fn)
     return fail(TS_ERR_UNSUPPORTED, "%s: D=%d, group size %d (supported D 64/128, g 1/2/4/8)", who,
                 D, g);
+  int g_shift = 0;
+  while ((1 << g_shift) < g) ++g_shift;
   const size_t es = dtype == TS_F32 ? 4 : 2;
   for (const void* ptr : {q, k_pool, v_pool, static_cast<const void*>(out)})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
       return fail(TS_ERR_INVALID_ARG, "%s: q, pools and out must be 16-byte aligned", who);
   const int n_ctas = paged_decode_ctas();
   if (n_ctas <= 0) return fail(TS_ERR_CUDA, "%s: cannot query the SM count", who);
-  const WsLayout ws = workspace_layout(B, H_q, D, n_ctas);
+  const WsLayout ws = workspace_layout(Bv, rows, D, n_ctas);
   if (!workspace || workspace_bytes < ws.total)
     return fail(TS_ERR_WORKSPACE, "%s: workspace %zu B < %zu B needed", who, workspace_bytes,
                 ws.total);
@@ -965,8 +232,13 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.bt_stride = bt_stride;
-  prm.B = B;
+  prm.B = Bv;
   prm.H_q = H_q;
+  prm.q_len = q_len;
+  prm.fold = fold;
+  prm.steps = steps;
+  prm.rows = rows;
+  prm.g_shift = g_shift;
   prm.H_kv = H_kv;
   prm.page_size = page_size;
   prm.num_pages = num_pages;
@@ -984,7 +256,7 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   prm.row_bytes = static_cast<uint32_t>(H_kv * D * es);
   prm.page_bytes = static_cast<uint32_t>(page_size) * prm.row_bytes;
-  prm.q_bytes = static_cast<uint32_t>(H_q * D * es);
+  prm.q_bytes = static_cast<uint32_t>(rows * D * es);
   // A stage holds chunk_rows token rows of one page (all kv heads, K and V)
   // plus room for one sequence's query rows. Whole pages when two stages fit,
   // else halves, quarters... TS_PAGED_DECODE_CHUNK_ROWS overrides (tuning).
@@ -1058,7 +330,7 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   }
   if (st != TS_OK) return st;
 
-  const long long warps = static_cast<long long>(B) * H_q;
+  const long long warps = static_cast<long long>(Bv) * rows;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
   mcfg.blockDim = dim3(256);
@@ -1079,6 +351,18 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
   return st;
 }
 
+ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                   int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                   ts_dtype dtype, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream, const char* who,
+                                   const PrefixInputs* pre) {
+  return paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, 1, H_q, H_kv, D,
+                           page_size, num_pages, scale, dtype, out, lse, workspace, workspace_bytes,
+                           stream, who, pre);
+}
+
 ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_table, int32_t bt_stride,
                               const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
@@ -1094,6 +378,16 @@ size_t paged_decode_workspace_bytes(int B, int H_q, int D) {
   const int n = paged_decode_ctas();
   if (n <= 0 || B < 0 || H_q <= 0 || D <= 0) return 0;
   return workspace_layout(B, H_q, D, n).total;
+}
+
+// Upper bound over the fold: at most B * q_len virtual sequences of at most
+// q_len * H_q rows.
+size_t paged_decode_multi_workspace_bytes(int B, int q_len, int H_q, int D) {
+  const int n = paged_decode_ctas();
+  if (n <= 0 || B < 0 || q_len < 1 || H_q <= 0 || D <= 0 ||
+      static_cast<long long>(B) * q_len > INT32_MAX / 2)
+    return 0;
+  return workspace_layout(B * q_len, q_len * H_q, D, n).total;
 }
 
 }  // namespace ts
@@ -1113,4 +407,30 @@ extern "C" ts_status ts_paged_decode_attn(const void* q, const void* k_pool, con
                                  D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                  workspace_bytes, static_cast<cudaStream_t>(stream),
                                  "ts_paged_decode_attn");
+}
+
+extern "C" size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q, int32_t D) {
+  return ts::paged_decode_multi_workspace_bytes(B, q_len, H_q, D);
+}
+
+extern "C" ts_status ts_paged_decode_multi_attn(const void* q, const void* k_pool, const void* v_pool,
+                                                const int32_t* block_table, int32_t bt_stride,
+                                                const int32_t* seq_lens, int32_t B, int32_t q_len,
+                                                int32_t H_q, int32_t H_kv, int32_t D,
+                                                int32_t page_size, int32_t num_pages, float scale,
+                                                ts_dtype dtype, void* out, float* lse,
+                                                void* workspace, size_t workspace_bytes,
+                                                void* stream) {
+  return ts::paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, q_len, H_q,
+                               H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
+                               workspace_bytes, static_cast<cudaStream_t>(stream),
+                               "ts_paged_decode_multi_attn", nullptr);
+}
+
+extern "C" int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t tile_rows) {
+  if (num_heads <= 0 || q_len <= 0 || tile_rows <= 0) return 0;
+  int32_t best = 1;
+  for (int32_t f = 1; f <= q_len; ++f)
+    if (q_len % f == 0 && static_cast<long long>(num_heads) * f <= tile_rows) best = f;
+  return best;
 }

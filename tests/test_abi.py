@@ -87,3 +87,14 @@ def test_launch_trace_toggles_without_a_gpu(lib):
     assert lib.ts_trace_enable(0) == ts.TS_OK
     assert lib.ts_trace_collect(None, 0) == 0
     assert ts.ts_trace_collect() == []
+
+
+def test_fold_sq_factor_host_helper_matches_the_rule(lib):
+    """ts_fold_sq_factor is host logic: checked against the oracle's statement
+    of the page's rule over a grid, and 0 for non-positive arguments."""
+    import oracle
+    for H in (1, 4, 16, 48, 64, 100, 128, 200):
+        for q_len in range(1, 13):
+            for tile in (8, 64, 128):
+                assert lib.ts_fold_sq_factor(H, q_len, tile) == oracle.fold_sq_factor(H, q_len, tile)
+    assert lib.ts_fold_sq_factor(0, 4, 128) == 0 and lib.ts_fold_sq_factor(64, 0, 128) == 0

@@ -113,8 +113,12 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
                append: bool = False, mla: bool = False, Dv: Optional[int] = None,
                pool_factor: float = 1.25, shared_groups: Optional[List[np.ndarray]] = None,
                shared_pages: int = 0, device="cpu", rng: Optional[np.random.Generator] = None,
-               extra_pages: int = 1, num_pages: Optional[int] = None, values: bool = True) -> PagedCase:
+               extra_pages: int = 1, num_pages: Optional[int] = None, values: bool = True,
+               q_len: int = 1) -> PagedCase:
     """Build a case: lengths -> page need -> shuffled pool -> block tables -> values.
+
+    ``q_len`` > 1 draws ``q_len`` query tokens per sequence (q [B, q_len, H_q, D]);
+    ``seq_lens`` then already count them.
 
     ``shared_groups``: lists of sequence ids; each list shares its first
     ``shared_pages`` pages by physical id (the cascade workload).
@@ -177,7 +181,7 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
     else:
         k_pool = _randn((num_pages, page_size, H_kv, D), g, device, dtype)
         v_pool = _randn((num_pages, page_size, H_kv, Dv), g, device, dtype)
-    q = _randn((B, H_q, D), g, device, dtype)
+    q = _randn((B, H_q, D) if q_len == 1 else (B, q_len, H_q, D), g, device, dtype)
     k_new = v_new = None
     if append:
         k_new = _randn((B, H_kv, D), g, device, dtype)
