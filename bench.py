@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla"],
+    ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla",
+                                           "spec_verify_q2", "spec_verify_q4"],
                     default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -206,6 +207,8 @@ def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
                                                members=32 if small else 1024)
     if name == "mla":
         return workloads.absorbed_mla(device=device, B=2 if small else n(64))
+    if name.startswith("spec_verify_q"):
+        return workloads.speculative_verify(device=device, B=8 if small else n(64), q_len=int(name[13:]))
     raise ValueError(name)
 
 
@@ -245,6 +248,9 @@ def oracle_pass(view, case):
         return oracle.mla_decode_attention(view["q"], view["k_pool"], view["block_table"], view["seq_lens"],
                                            case.scale, case.Dv)
     kp, vp = view["k_pool"], view["v_pool"]
+    if case.q_len > 1:
+        return oracle.multi_query_decode_attention(view["q"], kp, vp, view["block_table"], view["seq_lens"],
+                                                   case.scale)
     if case.append:
         kp, vp = oracle.kv_append(kp, vp, view["k_new"], view["v_new"], view["block_table"],
                                   view["positions"], case.page_size)
@@ -283,14 +289,15 @@ def cpu_baseline(case, budget_s: float = 12.0):
     return {"value": nbytes / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{len(idx)} of {case.B} sequences ({int(case.attn_lens[idx].sum())} tokens) x {reps} passes, "
                       f"fp64 numpy, 1 BLAS thread; bytes counted flat (no prefix sharing)",
-            "query_tokens_per_s": len(idx) / sec}
+            "query_tokens_per_s": len(idx) * case.q_len / sec}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla"))
+    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla") or
+                          args.workload.startswith("spec_verify"))
     # size each step's sample so the whole run stays within ~2 minutes
     t1, _ = time_oracle(case, [0], 0.0)
     per_seq = max(t1, 1e-4)
@@ -336,8 +343,9 @@ class DeviceStep:
         self.bt = torch.from_numpy(c.block_table).to(dev)
         self.lens = torch.from_numpy(c.attn_lens).to(dev)
         self.pos = torch.from_numpy(c.positions).to(dev)
-        self.out = torch.empty(c.B, c.H_q, c.Dv, dtype=c.q.dtype, device=dev)
-        self.lse = torch.empty(c.B, c.H_q, dtype=torch.float32, device=dev)
+        rows = (c.B, c.H_q) if c.q_len == 1 else (c.B, c.q_len, c.H_q)
+        self.out = torch.empty(*rows, c.Dv, dtype=c.q.dtype, device=dev)
+        self.lse = torch.empty(*rows, dtype=torch.float32, device=dev)
         pools = [(c.k_pool, c.v_pool)]
         for _ in range(rotate - 1):
             pools.append((c.k_pool.clone(), c.v_pool.clone() if c.v_pool is not None else None))
@@ -352,6 +360,8 @@ class DeviceStep:
             ws_bytes = ts.ts_cascade_decode_workspace_size(c.B, c.H_q, c.D)
         elif c.mla:
             ws_bytes = ts.ts_mla_workspace_size(c.B, c.H_q, c.Dv)
+        elif c.q_len > 1:
+            ws_bytes = ts.ts_paged_decode_multi_workspace_size(c.B, c.q_len, c.H_q, c.D)
         else:
             ws_bytes = ts.ts_paged_decode_workspace_size(c.B, c.H_q, c.D)
         self.ws = ts.new_workspace(ws_bytes, dev)
@@ -368,6 +378,9 @@ class DeviceStep:
         elif c.mla:
             ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=self.out, lse=self.lse,
                                    workspace=self.ws, stream=stream)
+        elif c.q_len > 1:
+            ts.ts_paged_decode_multi_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse,
+                                          workspace=self.ws, stream=stream)
         else:
             ts.ts_paged_decode_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse, workspace=self.ws,
                                     stream=stream)
@@ -524,7 +537,8 @@ def run_ours(args):
         e2e_ms = max(max_over_ranks(s2.elapsed_time(e2), dist, dev) / n_e2e, wall_ms)
         e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
-               "query_tokens_per_s": world * case.B / (e2e_ms * 1e-3), "cuda_graph": graph is not None}
+               "query_tokens_per_s": world * case.B * case.q_len / (e2e_ms * 1e-3),
+               "cuda_graph": graph is not None}
         if host_group_ms:
             e2e["host_grouping_ms"] = statistics.median(host_group_ms)
 
@@ -568,10 +582,11 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D,
                    "Dv": case.Dv, "page_size": case.page_size, "tokens_attended": int(case.attn_lens.sum()),
-                   "kv_bytes_per_step": nbytes, "append": case.append, "parallelism": f"replicas x{world}",
+                   "kv_bytes_per_step": nbytes, "append": case.append, "q_len": case.q_len,
+                   "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {rotate} rotated pool cop{'y' if rotate == 1 else 'ies'} of "
                          f"{pool_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)"},
-        "query_tokens_per_s": world * case.B / (ms_step * 1e-3),
+        "query_tokens_per_s": world * case.B * case.q_len / (ms_step * 1e-3),
         "hbm_frac_of_8tbs": value / world / 8000.0,
         "roofline": roofline,
         "kernels": kernels,

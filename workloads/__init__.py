@@ -58,6 +58,7 @@ class PagedCase:
     k_new: Optional[torch.Tensor] = None
     v_new: Optional[torch.Tensor] = None
     groups_truth: Optional[List[np.ndarray]] = None  # cascade: members per constructed group
+    q_len: int = 1              # query tokens per sequence (q [B, q_len, H_q, D] when > 1)
     prefix_pages_truth: int = 0
     meta: Dict = field(default_factory=dict)
 
@@ -195,7 +196,7 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
                      page_size=page_size, num_pages=num_pages, dtype=dtype, scale=scale,
                      mla=mla, append=append, seq_lens=lens, block_table=bt,
                      sentinel_page=sentinel, q=q, k_pool=k_pool, v_pool=v_pool,
-                     k_new=k_new, v_new=v_new,
+                     k_new=k_new, v_new=v_new, q_len=q_len,
                      groups_truth=[np.asarray(m) for m in shared_groups] if shared_groups else None,
                      prefix_pages_truth=shared_pages if shared_groups else 0)
 
@@ -221,6 +222,18 @@ def llama3_8b_layer(device="cpu", seed: int = 2, B: int = 64, lo: int = 512, hi:
     return build_case(f"llama3_8b_layer_B{B}", seed, B=B, H_q=32, H_kv=8, D=128, page_size=16,
                       seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128),
                       append=append, device=device, rng=rng)
+
+
+def speculative_verify(device="cpu", seed: int = 6, B: int = 64, q_len: int = 4, lo: int = 512,
+                       hi: int = 4096) -> PagedCase:
+    """Llama-3-8B-shaped layer verifying q_len draft tokens per sequence:
+    32/8 heads, D=128, bf16, page 16, lens ~ U[lo, hi] counting the draft
+    tokens (their K/V already in the cache), pool 1.25x the need."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_case(f"speculative_verify_B{B}_q{q_len}", seed, B=B, H_q=32, H_kv=8, D=128,
+                      page_size=16, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128),
+                      device=device, rng=rng, q_len=q_len)
 
 
 def mixed_lengths(device="cpu", seed: int = 3, repeat: int = 32) -> PagedCase:
