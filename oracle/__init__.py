@@ -14,6 +14,8 @@ Each function restates the operation from the pages it cites:
   lengths): pages of fixed size addressed through a per-request block table.
 * TokenSpeed deep dive (wth2jhl.online), section 7 "MLA decode", fig. 3 and
   section 7.1: split-KV partial outputs carry a log-sum-exp and are reduced by it.
+* tokenspeed 딥다이브 (fiv.co.kr), section 6-4: fp8 token-group quantization
+  (scale = group max / fp8 max, clamp, cast; reconstruction = code * scale).
 * Tokasaurus blog (Stanford), "Dynamic prefix identification and exploration":
   shared-prefix (Hydragen / cascade) attention over greedily found shared prefixes.
 
@@ -32,6 +34,14 @@ from .attention import (
     kv_append,
 )
 from .prefix_groups import check_prefix_groups, PrefixGroups
+from .fp8 import (
+    e4m3_decode,
+    e4m3_encode,
+    quantize_token_groups,
+    dequantize,
+    kv_append_fp8,
+    decode_attention_fp8,
+)
 
 __all__ = [
     "gather_sequence",
@@ -43,5 +53,11 @@ __all__ = [
     "merge_states_many",
     "kv_append",
     "check_prefix_groups",
+    "e4m3_decode",
+    "e4m3_encode",
+    "quantize_token_groups",
+    "dequantize",
+    "kv_append_fp8",
+    "decode_attention_fp8",
     "PrefixGroups",
 ]
