@@ -57,7 +57,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla",
-                                           "spec_verify_q2", "spec_verify_q4"],
+                                           "spec_verify_q2", "spec_verify_q4", "llama3_8b_layer_fp8"],
                     default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -207,6 +207,8 @@ def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
                                                members=32 if small else 1024)
     if name == "mla":
         return workloads.absorbed_mla(device=device, B=2 if small else n(64))
+    if name == "llama3_8b_layer_fp8":
+        return workloads.llama3_8b_layer_fp8(device=device, B=8 if small else n(64))
     if name.startswith("spec_verify_q"):
         return workloads.speculative_verify(device=device, B=8 if small else n(64), q_len=int(name[13:]))
     raise ValueError(name)
@@ -222,6 +224,8 @@ def algorithmic(case, groups=None):
     tokens = int(case.attn_lens.astype(np.int64).sum())
     if case.mla:
         return tokens * case.D * es, tokens * case.H_q * (case.D + case.Dv) * 2
+    if case.kv_fp8:
+        return case.kv_bytes_read(), 0
     row = case.H_kv * (case.D + case.Dv) * es
     if groups is not None and groups["num_groups"] > 0:
         prefix_tokens = int(groups["prefix_len"].astype(np.int64).sum())
@@ -248,6 +252,13 @@ def oracle_pass(view, case):
         return oracle.mla_decode_attention(view["q"], view["k_pool"], view["block_table"], view["seq_lens"],
                                            case.scale, case.Dv)
     kp, vp = view["k_pool"], view["v_pool"]
+    if case.kv_fp8:
+        ks, vs = view["k_scale"], view["v_scale"]
+        if case.append:
+            kp, vp, ks, vs = oracle.kv_append_fp8(kp, vp, ks, vs, view["k_new"], view["v_new"], view["block_table"],
+                                                  view["positions"], case.page_size)
+        return oracle.decode_attention_fp8(view["q"], kp, vp, ks, vs, view["block_table"], view["seq_lens"],
+                                           case.scale)
     if case.q_len > 1:
         return oracle.multi_query_decode_attention(view["q"], kp, vp, view["block_table"], view["seq_lens"],
                                                    case.scale)
@@ -263,6 +274,8 @@ def sample_bytes(case, idx):
     tokens = int(case.attn_lens[idx].astype(np.int64).sum())
     if case.mla:
         return tokens * case.D * es
+    if case.kv_fp8:
+        return tokens * case.H_kv * (case.D + case.Dv) + tokens * case.H_kv * 2 * 4
     return tokens * case.H_kv * (case.D + case.Dv) * es
 
 
@@ -297,7 +310,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla") or
-                          args.workload.startswith("spec_verify"))
+                          args.workload.startswith("spec_verify") or args.workload.endswith("fp8"))
     # size each step's sample so the whole run stays within ~2 minutes
     t1, _ = time_oracle(case, [0], 0.0)
     per_seq = max(t1, 1e-4)
@@ -350,6 +363,9 @@ class DeviceStep:
         for _ in range(rotate - 1):
             pools.append((c.k_pool.clone(), c.v_pool.clone() if c.v_pool is not None else None))
         self.pools = pools
+        # fp8 caches: each rotated pool copy has its own scale arrays
+        self.scales = [(c.k_scale, c.v_scale)] + [(c.k_scale.clone(), c.v_scale.clone())
+                                                  for _ in range(rotate - 1)] if c.kv_fp8 else None
         self.groups = None
         self.gdev = None
         if c.name.startswith("cascade"):
@@ -381,6 +397,10 @@ class DeviceStep:
         elif c.q_len > 1:
             ts.ts_paged_decode_multi_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse,
                                           workspace=self.ws, stream=stream)
+        elif c.kv_fp8:
+            ks, vs = self.scales[i % len(self.scales)]
+            ts.ts_paged_decode_fp8_attn(q, kp, vp, ks, vs, bt, lens, c.scale, out=self.out, lse=self.lse,
+                                        workspace=self.ws, stream=stream)
         else:
             ts.ts_paged_decode_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse, workspace=self.ws,
                                     stream=stream)
@@ -389,7 +409,11 @@ class DeviceStep:
         ts, c = self.ts, self.case
         kp, vp = self.pools[i % len(self.pools)]
         inputs = inputs or {}
-        if c.append:
+        if c.append and c.kv_fp8:
+            ks, vs = self.scales[i % len(self.scales)]
+            ts.ts_kv_append_fp8(inputs.get("k_new", c.k_new), inputs.get("v_new", c.v_new), kp, vp, ks, vs,
+                                inputs.get("bt", self.bt), inputs.get("pos", self.pos), stream=stream)
+        elif c.append:
             ts.ts_kv_append(inputs.get("k_new", c.k_new), inputs.get("v_new", c.v_new), kp, vp,
                             inputs.get("bt", self.bt), inputs.get("pos", self.pos), stream=stream)
         if ev is not None:
@@ -578,7 +602,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if case.dtype == "bf16" else "f32", "accumulate": "f32",
+        "vs_baseline": None, "dtype": ("e4m3 K/V, bf16 q" if case.kv_fp8 else
+                                       "bf16" if case.dtype == "bf16" else "f32"), "accumulate": "f32",
         "data": "synthetic",
         "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D,
                    "Dv": case.Dv, "page_size": case.page_size, "tokens_attended": int(case.attn_lens.sum()),

@@ -226,6 +226,50 @@ TS_API ts_status ts_paged_decode_multi_attn(const void* q, const void* k_pool, c
                                             void* stream);
 
 /*
+ * ts_kv_append_fp8 - quantize one new token's K and V per sequence into an
+ * fp8 (e4m3fn) cache.
+ *
+ * Placement as ts_kv_append. Quantization per token group (tokenspeed
+ * 딥다이브, fiv.co.kr, section 6-4): a group is one (token, kv head) row of D
+ * values; scale = max(max |x|, 1e-10) / 448 and code = e4m3fn(clamp(x / scale,
+ * -448, 448)), the scale and the division in float32 rounded to nearest even,
+ * the cast rounded to nearest even. Bit-exact with that definition.
+ *
+ *   k_new, v_new    device [B, H_kv, D] of dtype (bf16 or f32)
+ *   k_pool, v_pool  device uint8 [num_pages, page_size, H_kv, D] e4m3fn codes (written)
+ *   k_scale,v_scale device float32 [num_pages, page_size, H_kv] (written)
+ *   block_table, positions, sizes as ts_kv_append. D in {64, 128}.
+ */
+TS_API ts_status ts_kv_append_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                  float* k_scale, float* v_scale, const int32_t* block_table,
+                                  int32_t bt_stride, const int32_t* positions, int32_t B, int32_t H_kv,
+                                  int32_t D, int32_t page_size, int32_t num_pages, ts_dtype dtype,
+                                  void* stream);
+
+/*
+ * ts_paged_decode_fp8_attn - ts_paged_decode_attn over an fp8 (e4m3fn) cache.
+ *
+ * Computes ts_paged_decode_attn's result over the cache's reconstruction
+ * K[t] = code * k_scale[t] (and the same for V), with bf16 queries and
+ * output: the kernel widens the codes exactly and applies each row's scale
+ * to its score (K) and to its softmax weight (V), in float32.
+ *
+ *   q               device bf16 [B, H_q, D];  out device bf16 [B, H_q, D]
+ *   k_pool, v_pool  device uint8 [num_pages, page_size, H_kv, D] e4m3fn codes
+ *   k_scale,v_scale device float32 [num_pages, page_size, H_kv], 16-byte aligned
+ *   workspace       >= ts_paged_decode_workspace_size(B, H_q, D)
+ *   other arguments as ts_paged_decode_attn. Supported: D in {64, 128},
+ *   H_q / H_kv in {1, 2, 4}, H_kv in {1, 2, 4, 8}, page_size in {8, 16, 32}.
+ */
+TS_API ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool, const void* v_pool,
+                                          const float* k_scale, const float* v_scale,
+                                          const int32_t* block_table, int32_t bt_stride,
+                                          const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                          int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
+/*
  * ts_merge_states - merge two attention states over disjoint key sets.
  *
  * Per row r: m = max(lse_a, lse_b), w_a = exp(lse_a - m), w_b = exp(lse_b - m),

@@ -73,6 +73,10 @@ _SIGNATURES = {
     "ts_paged_decode_multi_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
                                                   _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
     "ts_fold_sq_factor": (_I32, [_I32, _I32, _I32]),
+    "ts_kv_append_fp8": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32,
+                                        _I32, ctypes.c_int, _VP]),
+    "ts_paged_decode_fp8_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32,
+                                                _I32, _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_merge_states": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, ctypes.c_int, _VP]),
     "ts_group_prefixes": (ctypes.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, ctypes.POINTER(PrefixGroupsC)]),
     "ts_cascade_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
@@ -235,6 +239,46 @@ def ts_paged_decode_multi_attn(q, k_pool, v_pool, block_table, seq_lens, scale: 
                                             ps, P, float(scale), _dt(q), _ptr(out), _ptr(lse),
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def _require_fp8_cache(k_pool, v_pool, k_scale, v_scale):
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8:
+        raise TypeError("fp8 pools hold e4m3fn codes as uint8")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("fp8 scales are float32 [num_pages, page_size, H_kv]")
+    if tuple(k_scale.shape) != tuple(k_pool.shape[:3]) or tuple(v_scale.shape) != tuple(v_pool.shape[:3]):
+        raise ValueError("scales must be [num_pages, page_size, H_kv] of their pool")
+
+
+def ts_kv_append_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, block_table, positions,
+                     stream=None) -> None:
+    """Quantize k_new/v_new [B, H_kv, D] into fp8 pools and their scales (see ts_attn.h)."""
+    _require_i32(block_table, positions)
+    _require_fp8_cache(k_pool, v_pool, k_scale, v_scale)
+    B, H_kv, D = k_new.shape
+    _check(lib().ts_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(positions), B,
+                                  H_kv, D, k_pool.shape[1], k_pool.shape[0], _dt(k_new), _stream(stream)))
+
+
+def ts_paged_decode_fp8_attn(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, scale: float,
+                             out=None, lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Decode attention over an fp8 (e4m3fn) cache with bf16 queries; returns ``out`` (and ``lse``)."""
+    _require_i32(block_table, seq_lens)
+    _require_fp8_cache(k_pool, v_pool, k_scale, v_scale)
+    B, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, H_q, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(ts_paged_decode_workspace_size(B, H_q, D), q.device)
+    _check(lib().ts_paged_decode_fp8_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv,
+                                          D, ps, P, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
     return (out, lse) if return_lse else out
 
 

@@ -109,10 +109,10 @@ using KernelFn = void (*)(const PagedParams);
 template <typename T, int D, bool kPfx>
 KernelFn pick_g(int g) {
   switch (g) {
-    case 1: return paged_decode_kernel<T, D, 1, kPfx, false>;
-    case 2: return paged_decode_kernel<T, D, 2, kPfx, false>;
-    case 4: return paged_decode_kernel<T, D, 4, kPfx, false>;
-    case 8: return paged_decode_kernel<T, D, 8, kPfx, false>;
+    case 1: return paged_decode_kernel<T, D, 1, kPfx, false, false>;
+    case 2: return paged_decode_kernel<T, D, 2, kPfx, false, false>;
+    case 4: return paged_decode_kernel<T, D, 4, kPfx, false, false>;
+    case 8: return paged_decode_kernel<T, D, 8, kPfx, false, false>;
     default: return nullptr;
   }
 }
@@ -174,12 +174,19 @@ int gqa_fold(int g, int q_len) {
 
 // Launches the paged split-KV kernel pair for q_len query tokens per
 // sequence; `pre` non-null selects prefix (cascade) mode (q_len 1 only).
+// Group scales of an fp8 (e4m3fn) cache, [num_pages, page_size, H_kv] each.
+struct Fp8Scales {
+  const float* k_scale;
+  const float* v_scale;
+};
+
 ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                             int32_t B, int32_t q_len, int32_t H_q, int32_t H_kv, int32_t D,
                             int32_t page_size, int32_t num_pages, float scale, ts_dtype dtype,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream, const char* who, const PrefixInputs* pre) {
+                            cudaStream_t stream, const char* who, const PrefixInputs* pre,
+                            const Fp8Scales* f8 = nullptr) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
       bt_stride <= 0)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
@@ -205,8 +212,18 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   const int steps = q_len / fold;
   const int Bv = B * steps;           // virtual sequences
   const int rows = fold * H_q;        // query rows of a virtual sequence
-  KernelFn fn = q_len == 1 ? pick_kernel(dtype, D, g, pre != nullptr)
-                           : pick_paged_multi_kernel(dtype, D, g * fold);
+  if (f8 != nullptr) {
+    if (dtype != TS_BF16 || q_len != 1 || pre != nullptr || g > 4)
+      return fail(TS_ERR_UNSUPPORTED, "%s: fp8 cache takes bf16 queries, one per sequence, g <= 4", who);
+    if (!f8->k_scale || !f8->v_scale)
+      return fail(TS_ERR_INVALID_ARG, "%s: null scale array", who);
+    if (reinterpret_cast<uintptr_t>(f8->k_scale) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(f8->v_scale) % 16 != 0)
+      return fail(TS_ERR_INVALID_ARG, "%s: scale arrays must be 16-byte aligned", who);
+  }
+  KernelFn fn = f8 != nullptr ? pick_paged_fp8_kernel(D, g)
+                : q_len == 1  ? pick_kernel(dtype, D, g, pre != nullptr)
+                              : pick_paged_multi_kernel(dtype, D, g * fold);
   if (!fn)
     return fail(TS_ERR_UNSUPPORTED, "%s: D=%d, group size %d (supported D 64/128, g 1/2/4/8)", who,
                 D, g);
@@ -254,9 +271,12 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
   prm.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
-  prm.row_bytes = static_cast<uint32_t>(H_kv * D * es);
+  const size_t es_kv = f8 != nullptr ? 1 : es;  // K/V element bytes
+  prm.row_bytes = static_cast<uint32_t>(H_kv * D * es_kv);
   prm.page_bytes = static_cast<uint32_t>(page_size) * prm.row_bytes;
   prm.q_bytes = static_cast<uint32_t>(rows * D * es);
+  prm.k_scale = f8 != nullptr ? f8->k_scale : nullptr;
+  prm.v_scale = f8 != nullptr ? f8->v_scale : nullptr;
   // A stage holds chunk_rows token rows of one page (all kv heads, K and V)
   // plus room for one sequence's query rows. Whole pages when two stages fit,
   // else halves, quarters... TS_PAGED_DECODE_CHUNK_ROWS overrides (tuning).
@@ -265,8 +285,10 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
     const int v = atoi(env);
     if (v > 0 && v <= page_size) chunk_rows = v;
   }
+  // fp8: each stage also holds its rows' K and V group scales
+  auto scale_of = [&](int rows) { return f8 != nullptr ? static_cast<uint32_t>(rows * H_kv * 4) : 0u; };
   auto stage_of = [&](int rows) {
-    return static_cast<uint32_t>(align_up(2ull * rows * prm.row_bytes + prm.q_bytes, 128));
+    return static_cast<uint32_t>(align_up(2ull * rows * prm.row_bytes + 2ull * scale_of(rows) + prm.q_bytes, 128));
   };
   while (chunk_rows > 1 &&
          (kSmemBudget - kHeaderBytes - align_up(prm.row_bytes, 128)) / stage_of(chunk_rows) < 2)
@@ -286,6 +308,10 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
     prm.seq_units = units;
   }
   prm.kv_area = static_cast<uint32_t>(chunk_rows) * prm.row_bytes;
+  prm.scale_area = scale_of(chunk_rows);
+  if (prm.scale_area % 16 != 0)
+    return fail(TS_ERR_UNSUPPORTED, "%s: fp8 stage of %d rows x %d kv heads: scales not a multiple of 16 B",
+                who, chunk_rows, H_kv);
   prm.stage_bytes = stage_of(chunk_rows);
   prm.stages_off = static_cast<uint32_t>(kHeaderBytes + align_up(prm.row_bytes, 128));
   const int stages = std::min<int>(kMaxStages, (kSmemBudget - prm.stages_off) / prm.stage_bytes);
@@ -363,6 +389,18 @@ ts_status launch_paged_decode_impl(const void* q, const void* k_pool, const void
                            stream, who, pre);
 }
 
+ts_status launch_paged_decode_fp8(const void* q, const void* k_pool, const void* v_pool,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                  int32_t B, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                                  int32_t num_pages, float scale, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  const Fp8Scales f8{k_scale, v_scale};
+  return paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, 1, H_q, H_kv, D,
+                           page_size, num_pages, scale, TS_BF16, out, lse, workspace, workspace_bytes,
+                           stream, "ts_paged_decode_fp8_attn", nullptr, &f8);
+}
+
 ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_table, int32_t bt_stride,
                               const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
@@ -433,4 +471,16 @@ extern "C" int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t t
   for (int32_t f = 1; f <= q_len; ++f)
     if (q_len % f == 0 && static_cast<long long>(num_heads) * f <= tile_rows) best = f;
   return best;
+}
+
+extern "C" ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool, const void* v_pool,
+                                              const float* k_scale, const float* v_scale,
+                                              const int32_t* block_table, int32_t bt_stride,
+                                              const int32_t* seq_lens, int32_t B, int32_t H_q,
+                                              int32_t H_kv, int32_t D, int32_t page_size,
+                                              int32_t num_pages, float scale, void* out, float* lse,
+                                              void* workspace, size_t workspace_bytes, void* stream) {
+  return ts::launch_paged_decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,
+                                     seq_lens, B, H_q, H_kv, D, page_size, num_pages, scale, out, lse,
+                                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }

@@ -8,6 +8,9 @@
 #include <cstdlib>
 #include <type_traits>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "ts_common.cuh"
 
 namespace ts {
@@ -53,12 +56,21 @@ struct PagedParams {
   uint32_t kv_area;      // chunk_rows * row_bytes: K (and V) area of a stage
   uint32_t row_bytes;    // bytes of one token row of K (or V), all kv heads
   uint32_t q_bytes;      // bytes of one virtual sequence's query rows
+  // fp8 (e4m3fn) cache: one float32 scale per (page, row, kv head) for K and
+  // for V ([num_pages, page_size, H_kv]); a stage holds its rows' scales
+  // (scale_area bytes each) after the V rows. nullptr / 0 otherwise.
+  const float* k_scale;
+  const float* v_scale;
+  uint32_t scale_area;
 };
 
 using PagedKernelFn = void (*)(const PagedParams);
 // Kernel for several query tokens per sequence with G rows per kv head
 // (defined in ts_paged_decode_multi.cu); nullptr if not compiled.
 PagedKernelFn pick_paged_multi_kernel(ts_dtype dt, int D, int G);
+// Kernel for an fp8 (e4m3fn) cache with bf16 queries and G rows per kv head
+// (defined in ts_paged_decode_fp8.cu); nullptr if not compiled.
+PagedKernelFn pick_paged_fp8_kernel(int D, int G);
 
 namespace {
 
@@ -115,6 +127,25 @@ struct Elem<__nv_bfloat16> {
   }
   static constexpr int kPairs = 4;
 };
+// e4m3fn codes of an fp8 cache: pair w is bytes 2w, 2w+1, widened exactly
+// (e4m3 -> f16 -> f32 by the conversion instructions).
+template <>
+struct Elem<uint8_t> {
+  static constexpr int kVE = 16;
+  __device__ static __forceinline__ float2 pair(const uint4& v, int w) {
+    const uint32_t x = (w >> 1) == 0 ? v.x : ((w >> 1) == 1 ? v.y : ((w >> 1) == 2 ? v.z : v.w));
+    const __nv_fp8x2_storage_t c = static_cast<__nv_fp8x2_storage_t>((w & 1) ? (x >> 16) : (x & 0xffffu));
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+    return __half22float2(__half2(h));
+  }
+  static constexpr int kPairs = 8;
+};
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -185,10 +216,13 @@ __device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k) 
   p.split_info[b] = make_int2(k, 0);
 }
 
-template <typename T, int D, int G, bool kPfx, bool kMulti>
+template <typename T, int D, int G, bool kPfx, bool kMulti, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedParams p) {
   static_assert(!(kPfx && kMulti), "shared prefixes take one query token per sequence");
-  using C = Cfg<T, D, G>;
+  static_assert(!kFp8 || (G <= 4 && sizeof(T) == 2 && !kPfx), "fp8 cache: bf16 queries, up to 4 rows");
+  // K/V element type (the lane split follows it); T is the query / output type
+  using KV = std::conditional_t<kFp8, uint8_t, T>;
+  using C = Cfg<KV, D, G>;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -433,8 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
                 desc[s] = d;
                 const uint32_t bytes = static_cast<uint32_t>(valid) * p.row_bytes;
                 const uint32_t qb = (flags & kFlagFirst) ? p.q_bytes : 0u;
+                // fp8: the scales of the stage's chunk_rows rows (whole, in bounds
+                // of the page even past the valid rows)
+                const uint32_t sb = (kFp8 && bytes) ? p.scale_area : 0u;
                 const uint32_t full_bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(full_bar, 2 * bytes + qb);
+                mbar_arrive_expect_tx(full_bar, 2 * bytes + 2 * sb + qb);
                 const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
                 if (bytes) {
                   const size_t off = static_cast<size_t>(page) * p.page_bytes +
@@ -442,9 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
                   bulk_g2s_hint(st, static_cast<const char*>(p.k_pool) + off, bytes, full_bar, pol);
                   bulk_g2s_hint(st + p.kv_area, static_cast<const char*>(p.v_pool) + off, bytes,
                                 full_bar, pol);
+                  if (sb) {
+                    const size_t so = (static_cast<size_t>(page) * ps + r0) * p.H_kv;
+                    bulk_g2s_hint(st + 2 * p.kv_area, p.k_scale + so, sb, full_bar, pol);
+                    bulk_g2s_hint(st + 2 * p.kv_area + sb, p.v_scale + so, sb, full_bar, pol);
+                  }
                 }
                 if (qb)
-                  bulk_g2s(st + 2 * p.kv_area,
+                  bulk_g2s(st + 2 * (p.kv_area + (kFp8 ? p.scale_area : 0u)),
                            static_cast<const char*>(p.q) + static_cast<size_t>(cur.b) * p.q_bytes, qb,
                            full_bar);
               }
@@ -524,21 +566,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     const StageDesc d = desc[s];
     if (d.flags & kFlagEnd) break;
     const uint32_t st = smem_u32(stages + static_cast<size_t>(s) * p.stage_bytes);
-    const uint32_t kbase = st, vbase = st + p.kv_area, qbase = st + 2 * p.kv_area;
+    const uint32_t kbase = st, vbase = st + p.kv_area;
+    const uint32_t sarea = kFp8 ? p.scale_area : 0u;
+    const uint32_t ksbase = st + 2 * p.kv_area, vsbase = ksbase + sarea;  // fp8 scales
+    const uint32_t qbase = st + 2 * (p.kv_area + sarea);
 
     if (d.flags & kFlagFirst) {
+      // the lane's query dims are those of its K/V vectors; a K/V vector of
+      // fp8 codes spans two 16-byte vectors of bf16 queries
+      constexpr int kQV = C::kVE / Elem<T>::kVE;
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
         m[hh] = -INFINITY;
         lsum[hh] = 0.f;
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v) {
-          const uint4 raw = lds128(qbase + (qrow(hh) * D + dim_off[v]) * C::kES);
 #pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) {
-            const float2 f = Elem<T>::pair(raw, w);
-            qv[hh][v * Elem<T>::kPairs + w] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-            acc[hh][v * Elem<T>::kPairs + w] = make_float2(0.f, 0.f);
+          for (int u = 0; u < kQV; ++u) {
+            const uint4 raw =
+                lds128(qbase + (qrow(hh) * D + dim_off[v] + u * Elem<T>::kVE) * static_cast<int>(sizeof(T)));
+#pragma unroll
+            for (int w = 0; w < Elem<T>::kPairs; ++w) {
+              const float2 f = Elem<T>::pair(raw, w);
+              const int x = v * Elem<KV>::kPairs + u * Elem<T>::kPairs + w;
+              qv[hh][x] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+              acc[hh][x] = make_float2(0.f, 0.f);
+            }
           }
         }
       }
@@ -583,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v)
 #pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) kf[v * Elem<T>::kPairs + w] = Elem<T>::pair(kv[v], w);
+          for (int w = 0; w < Elem<KV>::kPairs; ++w) kf[v * Elem<KV>::kPairs + w] = Elem<KV>::pair(kv[v], w);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           float2 a = make_float2(0.f, 0.f);
@@ -598,6 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         for (int i = 0; i < C::kTPG; ++i)
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) sc[i][hh] += __shfl_xor_sync(0xffffffffu, sc[i][hh], o);
+      // fp8 cache: token i's scores take its K row's group scale, and its
+      // softmax weight its V row's (0 for rows past the valid ones, whose
+      // scale slots may hold anything)
+      float vsc[C::kTPG];
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int i = 0; i < C::kTPG; ++i) {
+          const int rix = kFull ? t0 + i : min(t0 + i, max(valid - 1, 0));
+          const uint32_t so = static_cast<uint32_t>((rix * p.H_kv + h) * 4);
+          const float ks = lds_f32(ksbase + so);
+          vsc[i] = (kFull || t0 + i < valid) ? lds_f32(vsbase + so) : 0.f;
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) sc[i][hh] *= ks;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < C::kTPG; ++i) {
         const bool in = kFull || t0 + i < valid;
@@ -649,10 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
 #pragma unroll
         for (int v = 0; v < C::kNV; ++v)
 #pragma unroll
-          for (int w = 0; w < Elem<T>::kPairs; ++w) vf[v * Elem<T>::kPairs + w] = Elem<T>::pair(vv[i][v], w);
+          for (int w = 0; w < Elem<KV>::kPairs; ++w) vf[v * Elem<KV>::kPairs + w] = Elem<KV>::pair(vv[i][v], w);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const float2 p2 = make_float2(pr[i][hh], pr[i][hh]);
+          const float pw = kFp8 ? pr[i][hh] * vsc[i] : pr[i][hh];
+          const float2 p2 = make_float2(pw, pw);
 #pragma unroll
           for (int x = 0; x < C::kPairsPL; ++x) acc[hh][x] = __ffma2_rn(p2, vf[x], acc[hh][x]);
         }
@@ -747,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       for (int c = 0; c < NF; c += U) {
         const int xf = own + c;
         const int hh = xf / P, x = xf % P;
-        const int dim = (x / Elem<T>::kPairs) * (D / C::kNV) + C::kVE * l + 2 * (x % Elem<T>::kPairs);
+        const int dim = (x / Elem<KV>::kPairs) * (D / C::kNV) + C::kVE * l + 2 * (x % Elem<KV>::kPairs);
         float cs, cp, lse2;
         finish(hh, cs, cp, lse2);
         float2 val[U];

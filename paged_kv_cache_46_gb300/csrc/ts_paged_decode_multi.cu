@@ -10,10 +10,10 @@ namespace {
 template <typename T, int D>
 PagedKernelFn pick_rows(int G) {
   switch (G) {
-    case 1: return paged_decode_kernel<T, D, 1, false, true>;
-    case 2: return paged_decode_kernel<T, D, 2, false, true>;
-    case 4: return paged_decode_kernel<T, D, 4, false, true>;
-    case 8: return paged_decode_kernel<T, D, 8, false, true>;
+    case 1: return paged_decode_kernel<T, D, 1, false, true, false>;
+    case 2: return paged_decode_kernel<T, D, 2, false, true, false>;
+    case 4: return paged_decode_kernel<T, D, 4, false, true, false>;
+    case 8: return paged_decode_kernel<T, D, 8, false, true, false>;
     default: return nullptr;
   }
 }

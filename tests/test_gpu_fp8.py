@@ -1,0 +1,116 @@
+"""GPU parity for the fp8 (e4m3fn) cache through the C ABI: the quantizing
+append is bit-exact with the oracle's token-group quantizer, and decode over
+the codes matches the fp64 oracle on the float32 reconstruction."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_46_gb300 as ts
+import workloads
+from gpu_helpers import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_46_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _meta(case):
+    return (torch.from_numpy(case.block_table).to(DEV), torch.from_numpy(case.attn_lens).to(DEV),
+            torch.from_numpy(case.positions).to(DEV))
+
+
+def _decode(case, ctas=None):
+    bt, lens, _ = _meta(case)
+    if ctas is not None:
+        os.environ["TS_PAGED_DECODE_CTAS"] = str(ctas)
+    try:
+        ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D))
+        out, lse = ts.ts_paged_decode_fp8_attn(case.q, case.k_pool, case.v_pool, case.k_scale, case.v_scale,
+                                               bt, lens, case.scale, workspace=ws, return_lse=True)
+        torch.cuda.synchronize()
+        assert ts.ts_read_device_error(ws) == 0
+    finally:
+        os.environ.pop("TS_PAGED_DECODE_CTAS", None)
+    return out, lse
+
+
+def _oracle(case, view=None):
+    v = view or workloads.oracle_view(case)
+    return oracle.decode_attention_fp8(v["q"], v["k_pool"], v["v_pool"], v["k_scale"], v["v_scale"],
+                                       v["block_table"], v["seq_lens"], case.scale)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_append_fp8_bit_exact(dtype):
+    lens = [0, 15, 16, 31, 100, 1]
+    case = workloads.build_fp8_case("fp8_append", 81, B=len(lens), H_q=16, H_kv=4, D=128, page_size=16,
+                                    seq_lens=lens, scale=0.09, append=True, device=DEV)
+    kn, vn = case.k_new, case.v_new
+    if dtype == "f32":  # f32 rows that are not bf16 values
+        g = torch.Generator(device=DEV).manual_seed(5)
+        kn = torch.randn(kn.shape, generator=g, device=DEV) * 3
+        vn = torch.randn(vn.shape, generator=g, device=DEV) * 0.01
+        vn[0, 0] = 0.0  # an all-zero group takes the 1e-10 scale floor
+    before = [t.clone() for t in (case.k_pool, case.v_pool, case.k_scale, case.v_scale)]
+    bt, _, pos = _meta(case)
+    ts.ts_kv_append_fp8(kn, vn, case.k_pool, case.v_pool, case.k_scale, case.v_scale, bt, pos)
+    torch.cuda.synchronize()
+    ref = oracle.kv_append_fp8(*(t.cpu().numpy() for t in before), kn.float().cpu().numpy(),
+                               vn.float().cpu().numpy(), case.block_table, case.positions, case.page_size)
+    got = [t.cpu().numpy() for t in (case.k_pool, case.v_pool, case.k_scale, case.v_scale)]
+    for r, gt, what in zip(ref, got, ("k codes", "v codes", "k scales", "v scales")):
+        if r.dtype == np.float32:  # NaN sentinels stay NaN: compare bit patterns
+            np.testing.assert_array_equal(r.view(np.uint32), gt.view(np.uint32), err_msg=what)
+        else:
+            np.testing.assert_array_equal(r, gt, err_msg=what)
+
+
+@pytest.mark.parametrize("D,H_q,H_kv,ps", [(128, 32, 8, 16), (64, 32, 8, 16), (128, 8, 8, 8), (64, 16, 8, 32),
+                                           (128, 4, 1, 16), (64, 8, 4, 16)])
+def test_decode_fp8_matches_oracle(D, H_q, H_kv, ps):
+    rng = np.random.default_rng(D + H_q + ps)
+    lens = rng.integers(1, 900, size=9)
+    lens[0], lens[1] = 1, ps
+    case = workloads.build_fp8_case(f"fp8_{D}_{H_q}_{H_kv}_{ps}", 83, B=9, H_q=H_q, H_kv=H_kv, D=D,
+                                    page_size=ps, seq_lens=lens, scale=D ** -0.5, device=DEV)
+    o_ref, l_ref = _oracle(case)
+    for ctas in (None, 5):
+        out, lse = _decode(case, ctas)
+        compare(out, o_ref, "bf16", lse, l_ref, f"fp8 D={D} {H_q}/{H_kv} ps={ps} ctas={ctas}")
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 1000])
+def test_decode_fp8_independent_of_split_pattern(ctas):
+    lens = [0, 1, 15, 16, 17, 700, 2049, 64]
+    case = workloads.build_fp8_case("fp8_split", 85, B=len(lens), H_q=32, H_kv=8, D=128, page_size=16,
+                                    seq_lens=lens, scale=0.0884, device=DEV)
+    out, lse = _decode(case, ctas)
+    o_ref, l_ref = _oracle(case)
+    compare(out, o_ref, "bf16", lse, l_ref, f"ctas={ctas}")
+
+
+def test_llama_fp8_step_append_then_decode():
+    """The Llama-3-8B layer shape over an fp8 cache, one append then decode,
+    every output row against the oracle (which quantizes the new rows itself)."""
+    case = workloads.llama3_8b_layer_fp8(device=DEV)
+    view = workloads.oracle_view(case)
+    bt, lens, pos = _meta(case)
+    ts.ts_kv_append_fp8(case.k_new, case.v_new, case.k_pool, case.v_pool, case.k_scale, case.v_scale, bt, pos)
+    out, lse = _decode(case)
+    kp, vp, ks, vs = oracle.kv_append_fp8(view["k_pool"], view["v_pool"], view["k_scale"], view["v_scale"],
+                                          view["k_new"], view["v_new"], view["block_table"], view["positions"],
+                                          case.page_size)
+    o_ref, l_ref = oracle.decode_attention_fp8(view["q"], kp, vp, ks, vs, view["block_table"], view["seq_lens"],
+                                               case.scale)
+    compare(out, o_ref, "bf16", lse, l_ref, "llama fp8 step")

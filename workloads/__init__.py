@@ -59,6 +59,11 @@ class PagedCase:
     v_new: Optional[torch.Tensor] = None
     groups_truth: Optional[List[np.ndarray]] = None  # cascade: members per constructed group
     q_len: int = 1              # query tokens per sequence (q [B, q_len, H_q, D] when > 1)
+    # fp8 (e4m3fn) cache: k_pool / v_pool hold uint8 codes, with float32
+    # scales [num_pages, page_size, H_kv] per (page, row, kv head)
+    kv_fp8: bool = False
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
     prefix_pages_truth: int = 0
     meta: Dict = field(default_factory=dict)
 
@@ -82,6 +87,8 @@ class PagedCase:
         tokens = int(self.attn_lens.astype(np.int64).sum())
         if self.mla:
             return tokens * self.D * esize
+        if self.kv_fp8:  # one-byte codes plus a float32 scale per row and kv head, K and V
+            return kv_cache_bytes(tokens, self.H_kv, self.D, self.Dv, 1) + tokens * self.H_kv * 2 * 4
         return kv_cache_bytes(tokens, self.H_kv, self.D, self.Dv, esize)
 
 
@@ -205,6 +212,59 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
 # The five workloads (sizes as stated by the workload list) and small variants
 # --------------------------------------------------------------------------
 
+def build_fp8_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int, page_size: int,
+                   seq_lens: Sequence[int], scale: float, append: bool = False, device="cpu",
+                   rng: Optional[np.random.Generator] = None) -> PagedCase:
+    """A case over an fp8 (e4m3fn) cache: the same page placement as
+    :func:`build_case`, with uniformly drawn non-NaN e4m3 codes and per-row
+    scales U[2.5, 3.5] / 448 (a row of N(0,1) values has its maximum there).
+    Rows holding no cached token carry the NaN code 0x7F and NaN scales.
+    Queries (and appended rows) are bf16 N(0,1)."""
+    base = build_case(name, seed, B=B, H_q=H_q, H_kv=H_kv, D=D, page_size=page_size, seq_lens=seq_lens,
+                      dtype="bf16", scale=scale, append=append, device=device, rng=rng, values=False)
+    P = base.num_pages
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    def codes():
+        c = torch.randint(0, 256, (P, page_size, H_kv, D), generator=g, device=device, dtype=torch.int32)
+        c = torch.where((c & 0x7F) == 0x7F, c - 1, c)  # no NaN codes among cached rows
+        return c.to(torch.uint8)
+    def scales():
+        return (torch.rand((P, page_size, H_kv), generator=g, device=device) + 2.5) / 448.0
+    k_pool, v_pool = codes(), codes()
+    k_scale, v_scale = scales(), scales()
+    q = _randn((B, H_q, D), g, device, "bf16")
+    k_new = v_new = None
+    if append:
+        k_new = _randn((B, H_kv, D), g, device, "bf16")
+        v_new = _randn((B, H_kv, D), g, device, "bf16")
+    lens = base.seq_lens
+    sentinel_rows = np.ones((P, page_size), dtype=bool)
+    for b in range(B):
+        full, rem = divmod(int(lens[b]), page_size)
+        if full:
+            sentinel_rows[base.block_table[b, :full]] = False
+        if rem:
+            sentinel_rows[base.block_table[b, full], :rem] = False
+    mask = torch.from_numpy(sentinel_rows).to(device)
+    for pool in (k_pool, v_pool):
+        pool.view(P, page_size, -1).masked_fill_(mask[:, :, None], 0x7F)
+    for sc in (k_scale, v_scale):
+        sc.masked_fill_(mask[:, :, None], float("nan"))
+    base.q, base.k_pool, base.v_pool, base.k_new, base.v_new = q, k_pool, v_pool, k_new, v_new
+    base.kv_fp8, base.k_scale, base.v_scale = True, k_scale, v_scale
+    return base
+
+
+def llama3_8b_layer_fp8(device="cpu", seed: int = 7, B: int = 64, lo: int = 512, hi: int = 4096,
+                        append: bool = True) -> PagedCase:
+    """The Llama-3-8B-shaped layer over an fp8 cache (same lengths and shapes)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_fp8_case(f"llama3_8b_layer_fp8_B{B}", seed, B=B, H_q=32, H_kv=8, D=128, page_size=16,
+                          seq_lens=lens, scale=1.0 / math.sqrt(128), append=append, device=device, rng=rng)
+
+
 def tiny_gqa_append(device="cpu", seed: int = 1) -> PagedCase:
     """Tiny paged GQA decode: B=4, 8/2 heads, D=64, page 16, fp32, lens
     {17, 40, 64, 100}, 64-page pool, scale 1/8, one appended token."""
@@ -311,15 +371,20 @@ def oracle_view(case: PagedCase, seq_idx: Optional[Sequence[int]] = None,
     kp = case.k_pool if k_pool is None else k_pool
     vp = case.v_pool if v_pool is None else v_pool
     dev_pages = torch.from_numpy(used.astype(np.int64)).to(kp.device)
+    # fp8 caches travel as their raw codes (uint8) and float32 scales
+    conv = (lambda t: t.cpu().numpy()) if case.kv_fp8 else _to_f64
     out = {
         "q": _to_f64(case.q[torch.from_numpy(idx).to(case.q.device)]),
-        "k_pool": _to_f64(kp.index_select(0, dev_pages)) if len(used) else None,
-        "v_pool": _to_f64(vp.index_select(0, dev_pages)) if (vp is not None and len(used)) else None,
+        "k_pool": conv(kp.index_select(0, dev_pages)) if len(used) else None,
+        "v_pool": conv(vp.index_select(0, dev_pages)) if (vp is not None and len(used)) else None,
         "block_table": bt,
         "seq_lens": lens.astype(np.int64),
         "positions": case.seq_lens[idx].astype(np.int64),
         "page_of_remapped": used,
     }
+    if case.kv_fp8:
+        out["k_scale"] = case.k_scale.index_select(0, dev_pages).cpu().numpy() if len(used) else None
+        out["v_scale"] = case.v_scale.index_select(0, dev_pages).cpu().numpy() if len(used) else None
     if case.append:
         dev_idx = torch.from_numpy(idx).to(case.q.device)
         out["k_new"] = _to_f64(case.k_new[dev_idx])
