@@ -57,7 +57,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla",
-                                           "spec_verify_q2", "spec_verify_q4", "llama3_8b_layer_fp8"],
+                                           "spec_verify_q2", "spec_verify_q4", "llama3_8b_layer_fp8",
+                                           "cascade_nested"],
                     default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -207,6 +208,8 @@ def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
                                                members=32 if small else 1024)
     if name == "mla":
         return workloads.absorbed_mla(device=device, B=2 if small else n(64))
+    if name == "cascade_nested":
+        return workloads.nested_prefix_cascade(device=device, members=8 if small else n(256))
     if name == "llama3_8b_layer_fp8":
         return workloads.llama3_8b_layer_fp8(device=device, B=8 if small else n(64))
     if name.startswith("spec_verify_q"):
@@ -234,6 +237,28 @@ def algorithmic(case, groups=None):
         flops = 4 * int((groups["prefix_len"].astype(np.int64) * members).sum()) * case.H_q * case.D
         return (tokens - shared + prefix_tokens) * row, flops
     return tokens * row, 0
+
+
+def forest_as_groups(forest):
+    """The per-node view algorithmic() needs: each node's own tokens and its
+    members, and every sequence's shared tokens (its deepest node's path)."""
+    N = int(forest["num_nodes"])
+    own = np.diff(forest["prefix_indptr"]).astype(np.int64) * 16
+    members = np.diff(forest["member_indptr"]).astype(np.int64)
+    deep = forest["group_of"]
+    shared = int(forest["prefix_len"][deep[deep >= 0]].astype(np.int64).sum()) if N else 0
+    return {"num_groups": N, "own_tokens": own, "members": members, "shared_tokens": shared}
+
+
+def algorithmic_forest(case, fg):
+    """Nested cascade: each node's own pages once plus every sequence's own
+    rows past its deepest node; prefix flops over every (member, node token)."""
+    es = 2
+    tokens = int(case.attn_lens.astype(np.int64).sum())
+    row = case.H_kv * (case.D + case.Dv) * es
+    distinct = int(fg["own_tokens"].sum())
+    flops = 4 * int((fg["own_tokens"] * fg["members"]).sum()) * case.H_q * case.D
+    return (tokens - fg["shared_tokens"] + distinct) * row, flops, (tokens - fg["shared_tokens"]) * row
 
 
 def suffix_bytes(case, groups):
@@ -309,7 +334,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla") or
+    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla", "cascade_nested") or
                           args.workload.startswith("spec_verify") or args.workload.endswith("fp8"))
     # size each step's sample so the whole run stays within ~2 minutes
     t1, _ = time_oracle(case, [0], 0.0)
@@ -368,7 +393,14 @@ class DeviceStep:
                                                   for _ in range(rotate - 1)] if c.kv_fp8 else None
         self.groups = None
         self.gdev = None
-        if c.name.startswith("cascade"):
+        self.forest = None
+        if c.name.startswith("nested_cascade"):
+            t = time.perf_counter()
+            self.forest = ts.ts_group_prefixes_nested(c.block_table, c.seq_lens, c.page_size, 2)
+            self.group_ms = (time.perf_counter() - t) * 1e3
+            self.gdev = ts.forest_to_device(self.forest, dev)
+            ws_bytes = ts.ts_cascade_decode_workspace_size(c.B, c.H_q, c.D)
+        elif c.name.startswith("cascade"):
             t = time.perf_counter()
             self.groups = ts.ts_group_prefixes(c.block_table, c.seq_lens, c.page_size, 2)
             self.group_ms = (time.perf_counter() - t) * 1e3
@@ -388,7 +420,10 @@ class DeviceStep:
         q = c.q if q is None else q
         bt = self.bt if bt is None else bt
         lens = self.lens if lens is None else lens
-        if self.groups is not None:
+        if self.forest is not None:
+            ts.ts_cascade_nested_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=self.out,
+                                             lse=self.lse, workspace=self.ws, stream=stream)
+        elif self.groups is not None:
             ts.ts_cascade_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=self.out, lse=self.lse,
                                       workspace=self.ws, stream=stream)
         elif c.mla:
@@ -445,7 +480,11 @@ def run_ours(args):
         rotate = 1  # already many times larger than L2
     runner = DeviceStep(ts, case, dev, rotate)
     stream = torch.cuda.current_stream()
-    nbytes, flops = algorithmic(case, runner.groups)
+    if runner.forest is not None:
+        fg = forest_as_groups(runner.forest)
+        nbytes, flops, forest_suffix = algorithmic_forest(case, fg)
+    else:
+        nbytes, flops = algorithmic(case, runner.groups)
 
     for i in range(args.warmup):
         runner.step(i, stream=stream)
@@ -519,7 +558,12 @@ def run_ours(args):
         def e2e_step(i, st):
             d_pack.copy_(h_pack, non_blocking=True)
             inputs = dict(din)
-            if runner.groups is not None:
+            if runner.forest is not None:
+                t = time.perf_counter()
+                f = ts.ts_group_prefixes_nested(case.block_table, case.seq_lens, case.page_size, 2)
+                host_group_ms.append((time.perf_counter() - t) * 1e3)
+                inputs["gdev"] = ts.forest_to_device(f, dev)
+            elif runner.groups is not None:
                 # the user's call sequence: group on the host, upload the groups, attend
                 t = time.perf_counter()
                 g = ts.ts_group_prefixes(case.block_table, case.seq_lens, case.page_size, 2)
@@ -528,7 +572,8 @@ def run_ours(args):
             runner.step(i, stream=st, inputs=inputs)
             h_out.copy_(runner.out, non_blocking=True)
 
-        n_e2e = min(args.steps, 50) if runner.groups is not None else args.steps
+        regroups = runner.groups is not None or runner.forest is not None
+        n_e2e = min(args.steps, 50) if regroups else args.steps
         for i in range(min(args.warmup, 3)):
             e2e_step(i, stream)
         torch.cuda.synchronize()
@@ -536,7 +581,7 @@ def run_ours(args):
         # step (input upload, library calls, result download) once, replay it
         # every step. Cascade regroups on the host every step and stays eager.
         graph = None
-        if runner.groups is None:
+        if not regroups:
             cap = torch.cuda.Stream(device=dev)
             cap.wait_stream(stream)
             graph = torch.cuda.CUDAGraph()
@@ -584,6 +629,8 @@ def run_ours(args):
     dom_bytes, dom_flops = nbytes, flops
     if runner.groups is not None and dom == "paged_decode_kernel":
         dom_bytes, dom_flops = suffix_bytes(case, runner.groups), 0
+    if runner.forest is not None and dom == "paged_decode_kernel":
+        dom_bytes, dom_flops = forest_suffix, 0
     source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu"}.get(
         dom, "ts_paged_decode.cu")
     hbm_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -620,11 +667,19 @@ def run_ours(args):
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
     if flops and "cascade_prefix_kernel" in kernels:
-        pms = kernels["cascade_prefix_kernel"]["mean_ms"]
+        # all prefix launches of a step (one per level of a nested forest)
+        pms = kernels["cascade_prefix_kernel"]["mean_ms"] * kernels["cascade_prefix_kernel"]["launches_per_step"]
         tflops = flops / (pms * 1e-3) / 1e12
         line["tensor"] = {"kernel": "cascade_prefix_kernel", "achieved": tflops, "peak": tc_peak,
-                          "unit": "TFLOP/s", "frac": tflops / tc_peak, "flops_per_launch": flops,
+                          "unit": "TFLOP/s", "frac": tflops / tc_peak, "flops_per_step": flops,
+                          "launches_per_step": kernels["cascade_prefix_kernel"]["launches_per_step"],
                           "kernel_ms": pms, "peak_source": f"{peak_kind} bf16_tflops (burst)"}
+    if runner.forest is not None:
+        flat = sample_bytes(case, np.arange(case.B))
+        line["config"]["flat_kv_bytes"] = flat
+        line["config"]["forest_nodes"] = int(runner.forest["num_nodes"])
+        line["config"]["forest_levels"] = int(runner.forest["num_levels"])
+        line["flat_equivalent_gbs"] = flat / (ms_step * 1e-3) / 1e9
     if runner.groups is not None:
         flat = sample_bytes(case, np.arange(case.B))
         line["config"]["flat_kv_bytes"] = flat

@@ -330,6 +330,53 @@ TS_API ts_status ts_group_prefixes(const int32_t* block_table, int32_t bt_stride
                             int32_t B, int32_t page_size, int32_t min_group, ts_prefix_groups* out);
 
 /*
+ * A forest of shared prefixes (ts_group_prefixes_nested). Nodes are listed
+ * level by level: level l holds nodes level_indptr[l] .. level_indptr[l+1]-1
+ * (roots at level 0). Node i owns the pages of its own stretch only,
+ * prefix_pages[prefix_indptr[i] .. prefix_indptr[i+1]-1] (the path above it
+ * belongs to its ancestors); prefix_len[i] counts the tokens shared from the
+ * root through node i; parent[i] is its parent node or -1; its members
+ * (member_ids[member_indptr[i] ..]) are all sequences that share its path.
+ * group_of[b] is the deepest node of sequence b, -1 if none. All arrays int32
+ * and caller-allocated (capacities say their sizes: level_indptr holds
+ * capacity_levels + 1, prefix_indptr and member_indptr capacity_nodes + 1).
+ */
+typedef struct {
+  int32_t num_nodes;
+  int32_t num_levels;
+  int32_t* level_indptr;
+  int32_t* parent;
+  int32_t* prefix_indptr;
+  int32_t* prefix_pages;
+  int32_t* prefix_len;
+  int32_t* member_indptr;
+  int32_t* member_ids;
+  int32_t* group_of;
+  int32_t capacity_nodes;
+  int32_t capacity_levels;
+  int32_t capacity_prefix_pages;
+  int32_t capacity_members;
+} ts_prefix_forest;
+
+/*
+ * ts_group_prefixes_nested - the greedy longest-shared-prefix search kept as a
+ * tree (Tokasaurus blog, "Dynamic prefix identification and exploration").
+ *
+ * Host only, over host copies of the block table and lengths; same page and
+ * cap rules as ts_group_prefixes (whole pages by physical id, a member of
+ * length L shares at most (L-1)/page_size pages). A node is a maximal stretch
+ * of pages shared by at least min_group sequences; at its end, members that
+ * can go deeper branch on the next page and branches of at least min_group
+ * sequences become child nodes. Each sequence's shared depth is then the
+ * largest d for which at least min_group sequences (itself included) share
+ * its first d pages within their caps. Returns TS_ERR_CAPACITY (with
+ * num_nodes / num_levels set to the counts needed) if an array is too small.
+ */
+TS_API ts_status ts_group_prefixes_nested(const int32_t* block_table, int32_t bt_stride,
+                                          const int32_t* seq_lens, int32_t B, int32_t page_size,
+                                          int32_t min_group, ts_prefix_forest* out);
+
+/*
  * ts_cascade_decode_workspace_size - workspace bytes for ts_cascade_decode_attn.
  */
 TS_API size_t ts_cascade_decode_workspace_size(int32_t B, int32_t H_q, int32_t D);
@@ -358,6 +405,32 @@ TS_API ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, const
                                  int32_t num_pages, float scale, ts_dtype dtype, void* out,
                                  float* lse, void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/*
+ * ts_cascade_nested_decode_attn - ts_cascade_decode_attn over a forest of
+ * nested shared prefixes (ts_group_prefixes_nested).
+ *
+ * Same result as ts_paged_decode_attn over the full block tables (up to
+ * float32 rounding). Level by level, the queries of each node's members
+ * attend the node's own stretch of pages as one dense tensor-core product,
+ * and each member's state over its path is merged by LSE (TokenSpeed deep
+ * dive, section 7.1); a prefix shared by a large set is thus computed once
+ * even where subsets share longer ones. Each sequence's pages past its
+ * deepest node take the paged split-KV path and are merged last.
+ *
+ *   forest            device copies of the arrays of ts_group_prefixes_nested
+ *                     (num_nodes and num_levels as returned; capacities ignored)
+ *   level_indptr_host HOST copy of forest level_indptr (num_levels + 1 entries)
+ *   workspace         >= ts_cascade_decode_workspace_size(B, H_q, D)
+ *   other arguments and support as ts_cascade_decode_attn.
+ */
+TS_API ts_status ts_cascade_nested_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                               const ts_prefix_forest* forest, const int32_t* level_indptr_host,
+                                               const int32_t* block_table, int32_t bt_stride,
+                                               const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                               int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                               ts_dtype dtype, void* out, float* lse, void* workspace,
+                                               size_t workspace_bytes, void* stream);
 
 /*
  * ts_mla_workspace_size - workspace bytes for ts_mla_paged_decode.

@@ -33,7 +33,7 @@ from .attention import (
     merge_states_many,
     kv_append,
 )
-from .prefix_groups import check_prefix_groups, PrefixGroups
+from .prefix_groups import check_prefix_groups, check_prefix_forest, shared_depth_brute_force, PrefixGroups
 from .fp8 import (
     e4m3_decode,
     e4m3_encode,
@@ -53,6 +53,8 @@ __all__ = [
     "merge_states_many",
     "kv_append",
     "check_prefix_groups",
+    "check_prefix_forest",
+    "shared_depth_brute_force",
     "e4m3_decode",
     "e4m3_encode",
     "quantize_token_groups",

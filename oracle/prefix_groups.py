@@ -118,3 +118,78 @@ def check_prefix_groups(block_table, seq_lens, page_size: int, min_group: int,
         if len(seqs) >= min_group:
             errors.append(f"{len(seqs)} ungrouped sequences share first page {page}")
     return errors
+
+
+def shared_depth_brute_force(block_table, seq_lens, page_size: int, min_group: int) -> np.ndarray:
+    """Per sequence: the largest d such that at least ``min_group`` sequences
+    (itself included) share its first d pages by id, each within its cap
+    ((L - 1) // page_size pages). Plain O(B^2 * depth) search for small inputs."""
+    bt = np.asarray(block_table)
+    B = len(seq_lens)
+    cap = [shareable_pages(seq_lens[b], page_size) for b in range(B)]
+    out = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        for d in range(cap[b], 0, -1):
+            n = sum(1 for t in range(B) if cap[t] >= d and np.array_equal(bt[t, :d], bt[b, :d]))
+            if n >= min_group:
+                out[b] = d
+                break
+    return out
+
+
+def check_prefix_forest(block_table, seq_lens, page_size: int, min_group: int, forest: dict):
+    """Invariants of a nested (tree) grouping, raising AssertionError on the first violation.
+
+    Tokasaurus blog, "Dynamic prefix identification and exploration" (greedy
+    search for the longest shared prefixes), kept as a tree: nodes level by
+    level, each node a stretch of whole pages shared by id by all its members
+    below its parent's path, members within their caps, at least
+    ``min_group`` members, children's members inside their parent's, and
+    every sequence's shared depth the largest possible (brute force).
+    """
+    bt = np.asarray(block_table)
+    B = len(seq_lens)
+    N = int(forest["num_nodes"])
+    lvl = forest["level_indptr"]
+    ptr, pages, plen = forest["prefix_indptr"], forest["prefix_pages"], forest["prefix_len"]
+    mptr, mids, parent, group_of = forest["member_indptr"], forest["member_ids"], forest["parent"], forest["group_of"]
+    level_of = np.full(N, -1)
+    for l in range(int(forest["num_levels"])):
+        level_of[lvl[l]:lvl[l + 1]] = l
+    assert N == 0 or (lvl[0] == 0 and lvl[-1] == N and np.all(level_of >= 0)), "level ranges"
+    members = [set(mids[mptr[i]:mptr[i + 1]].tolist()) for i in range(N)]
+    depth_end = plen // page_size
+    for i in range(N):
+        par = int(parent[i])
+        assert (par == -1) == (level_of[i] == 0), f"node {i}: roots are exactly level 0"
+        d0 = 0 if par < 0 else int(depth_end[par])
+        if par >= 0:
+            assert level_of[par] == level_of[i] - 1 and members[i] <= members[par], f"node {i}: parent"
+        d1 = int(depth_end[i])
+        own = pages[ptr[i]:ptr[i + 1]]
+        assert plen[i] % page_size == 0 and d1 - d0 == len(own) >= 1, f"node {i}: stretch"
+        assert len(members[i]) >= min_group, f"node {i}: {len(members[i])} members"
+        m_sorted = mids[mptr[i]:mptr[i + 1]]
+        assert np.all(np.diff(m_sorted) > 0), f"node {i}: members not increasing"
+        for m in members[i]:
+            assert shareable_pages(seq_lens[m], page_size) >= d1, f"node {i}: member {m} over its cap"
+            assert np.array_equal(bt[m, d0:d1], own), f"node {i}: member {m} does not share the pages"
+        # maximal stretch: the members do not all continue with one more shared page
+        ext = [m for m in members[i] if shareable_pages(seq_lens[m], page_size) > d1]
+        assert not (len(ext) == len(members[i]) and len({int(bt[m, d1]) for m in ext}) == 1), \
+            f"node {i}: stretch could go on"
+    # each sequence's node is the deepest holding it, on one chain, at the largest shared depth
+    want = shared_depth_brute_force(bt, seq_lens, page_size, min_group)
+    for b in range(B):
+        holding = [i for i in range(N) if b in members[i]]
+        g = int(group_of[b])
+        if not holding:
+            assert g == -1 and want[b] == 0, f"sequence {b}: ungrouped but depth {want[b]} is shared"
+            continue
+        assert g == max(holding, key=lambda i: depth_end[i]), f"sequence {b}: not its deepest node"
+        chain, i = set(), g
+        while i >= 0:
+            chain.add(i)
+            i = int(parent[i])
+        assert chain == set(holding), f"sequence {b}: nodes off its chain"
+        assert depth_end[g] == want[b], f"sequence {b}: shared depth {depth_end[g]} != {want[b]}"

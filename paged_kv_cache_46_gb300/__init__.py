@@ -51,6 +51,25 @@ class PrefixGroupsC(ctypes.Structure):
     ]
 
 
+class PrefixForestC(ctypes.Structure):
+    _fields_ = [
+        ("num_nodes", ctypes.c_int32),
+        ("num_levels", ctypes.c_int32),
+        ("level_indptr", ctypes.c_void_p),
+        ("parent", ctypes.c_void_p),
+        ("prefix_indptr", ctypes.c_void_p),
+        ("prefix_pages", ctypes.c_void_p),
+        ("prefix_len", ctypes.c_void_p),
+        ("member_indptr", ctypes.c_void_p),
+        ("member_ids", ctypes.c_void_p),
+        ("group_of", ctypes.c_void_p),
+        ("capacity_nodes", ctypes.c_int32),
+        ("capacity_levels", ctypes.c_int32),
+        ("capacity_prefix_pages", ctypes.c_int32),
+        ("capacity_members", ctypes.c_int32),
+    ]
+
+
 class LaunchRecordC(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_char * 48), ("ms", ctypes.c_float)]
 
@@ -79,7 +98,11 @@ _SIGNATURES = {
                                                 _I32, _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_merge_states": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, ctypes.c_int, _VP]),
     "ts_group_prefixes": (ctypes.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, ctypes.POINTER(PrefixGroupsC)]),
+    "ts_group_prefixes_nested": (ctypes.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, ctypes.POINTER(PrefixForestC)]),
     "ts_cascade_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "ts_cascade_nested_decode_attn": (ctypes.c_int, [_VP, _VP, _VP, ctypes.POINTER(PrefixForestC), _VP, _VP, _I32,
+                                                     _VP, _I32, _I32, _I32, _I32, _I32, _I32, _F32, ctypes.c_int,
+                                                     _VP, _VP, _VP, _SZ, _VP]),
     "ts_cascade_decode_attn": (ctypes.c_int, [_VP, _VP, _VP, ctypes.POINTER(PrefixGroupsC), _VP, _I32, _VP,
                                               _I32, _I32, _I32, _I32, _I32, _I32, _F32, ctypes.c_int,
                                               _VP, _VP, _VP, _SZ, _VP]),
@@ -324,6 +347,87 @@ def ts_group_prefixes(block_table: np.ndarray, seq_lens: np.ndarray, page_size: 
         "member_ids": arrays["member_ids"][:arrays["member_indptr"][G]].copy(),
         "group_of": arrays["group_of"][:B].copy(),
     }
+
+
+def ts_group_prefixes_nested(block_table: np.ndarray, seq_lens: np.ndarray, page_size: int,
+                             min_group: int = 2):
+    """Host greedy shared-prefix search kept as a tree; returns a dict of int32 numpy arrays
+    (nodes level by level, see ts_prefix_forest in ts_attn.h)."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = lens.shape[0]
+    caps = np.maximum(0, (lens.astype(np.int64) - 1) // page_size)
+    cap_n = max(1, B)               # every node has >= 2 members and its own sequence set
+    cap_l = max(1, int(caps.max()) if B else 1)
+    cap_pages = max(1, int(caps.sum()))
+    cap_members = max(1, int(caps.sum()))  # a sequence is in at most one node per shared page
+    while True:
+        arrays = {
+            "level_indptr": np.empty(cap_l + 1, np.int32), "parent": np.empty(cap_n, np.int32),
+            "prefix_indptr": np.empty(cap_n + 1, np.int32), "prefix_pages": np.empty(cap_pages, np.int32),
+            "prefix_len": np.empty(cap_n, np.int32), "member_indptr": np.empty(cap_n + 1, np.int32),
+            "member_ids": np.empty(cap_members, np.int32), "group_of": np.empty(max(1, B), np.int32),
+        }
+        c = PrefixForestC(0, 0, *[arrays[k].ctypes.data for k in
+                                  ("level_indptr", "parent", "prefix_indptr", "prefix_pages", "prefix_len",
+                                   "member_indptr", "member_ids", "group_of")],
+                          cap_n, cap_l, cap_pages, cap_members)
+        st = lib().ts_group_prefixes_nested(bt.ctypes.data, bt.shape[1], lens.ctypes.data, B, page_size,
+                                            min_group, ctypes.byref(c))
+        if st != TS_ERR_CAPACITY:
+            break
+        cap_n, cap_l = max(cap_n, c.num_nodes), max(cap_l, c.num_levels)
+        cap_members *= 2
+    _check(st)
+    N, L = c.num_nodes, c.num_levels
+    return {
+        "num_nodes": N, "num_levels": L,
+        "level_indptr": arrays["level_indptr"][:L + 1].copy() if N else np.zeros(1, np.int32),
+        "parent": arrays["parent"][:N].copy(),
+        "prefix_indptr": arrays["prefix_indptr"][:N + 1].copy(),
+        "prefix_pages": arrays["prefix_pages"][:arrays["prefix_indptr"][N]].copy(),
+        "prefix_len": arrays["prefix_len"][:N].copy(),
+        "member_indptr": arrays["member_indptr"][:N + 1].copy(),
+        "member_ids": arrays["member_ids"][:arrays["member_indptr"][N]].copy(),
+        "group_of": arrays["group_of"][:B].copy(),
+    }
+
+
+def forest_to_device(forest: dict, device="cuda") -> dict:
+    """Device int32 copies of the arrays of ts_group_prefixes_nested (plus the host level_indptr)."""
+    out = {"num_nodes": int(forest["num_nodes"]), "num_levels": int(forest["num_levels"]),
+           "level_indptr_host": np.ascontiguousarray(forest["level_indptr"], dtype=np.int32)}
+    for k in ("level_indptr", "parent", "prefix_indptr", "prefix_pages", "prefix_len", "member_indptr",
+              "member_ids", "group_of"):
+        a = forest[k] if len(forest[k]) else np.zeros(1, np.int32)
+        out[k] = torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    return out
+
+
+def ts_cascade_nested_decode_attn(q, k_pool, v_pool, forest_dev: dict, block_table, seq_lens, scale: float,
+                                  out=None, lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Cascade decode over a nested prefix forest (device arrays from forest_to_device)."""
+    _require_i32(block_table, seq_lens)
+    B, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, H_q, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(ts_cascade_decode_workspace_size(B, H_q, D), q.device)
+    f = forest_dev
+    c = PrefixForestC(f["num_nodes"], f["num_levels"], *[f[k].data_ptr() for k in
+                                                         ("level_indptr", "parent", "prefix_indptr", "prefix_pages",
+                                                          "prefix_len", "member_indptr", "member_ids", "group_of")],
+                      0, 0, 0, 0)
+    lvl = f["level_indptr_host"]
+    _check(lib().ts_cascade_nested_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), ctypes.byref(c),
+                                               lvl.ctypes.data, _ptr(block_table), block_table.shape[1],
+                                               _ptr(seq_lens), B, H_q, H_kv, D, ps, P, float(scale), _dt(q),
+                                               _ptr(out), _ptr(lse), _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(), _stream(stream)))
+    return (out, lse) if return_lse else out
 
 
 def groups_to_device(groups: dict, device="cuda") -> dict:

@@ -68,6 +68,9 @@ struct PrefixParams {
   float* prefix_o;    // [B, H_q, 64]
   float* prefix_lse;  // [B, H_q]
   uint32_t* err_word;
+  // nested prefixes: merge this launch's state into the member's state from
+  // the launches of the levels above instead of overwriting it
+  int32_t accumulate;
 };
 
 // --- kernels -----------------------------------------------------------------
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
   const int mcount = min(p.mpt, p.member_indptr[gi + 1] - mbeg);
   const int pp0 = p.prefix_indptr[gi];
   const int n_pages = p.prefix_indptr[gi + 1] - pp0;
-  const int plen = p.prefix_len[gi];
+  const int plen = n_pages * kPS;  // this node's own pages (the path above it is other launches')
   const int n_kt = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
       if (lane == 0) mbar_arrive(b_pfull);
     }
     // epilogue: O row / l, LSE (an empty prefix gives O = 0, LSE = -inf)
-    if (ok && n_kt == 0) {
+    if (ok && n_kt == 0 && !p.accumulate) {
       const int mi = r / p.g;
       if (mi < mcount) {
         const int64_t row = static_cast<int64_t>(p.member_ids[mbeg + mi]) * p.H_q + h * p.g + r % p.g;
@@ -385,7 +388,21 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
         const bool valid = mi < mcount;
         const int b = valid ? p.member_ids[mbeg + mi] : 0;
         const int64_t row = static_cast<int64_t>(b) * p.H_q + h * p.g + r % p.g;
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        float lse_new = l > 0.f ? (m + log2f(l)) * kLn2C : -INFINITY;
+        // weights of the state already there (accumulate) and of this one,
+        // by LSE (TokenSpeed deep dive, section 7.1)
+        float w_old = 0.f, w_new = l > 0.f ? 1.0f / l : 0.f;
+        if (p.accumulate && valid) {
+          const float lse_old = p.prefix_lse[row];
+          const float mx = fmaxf(lse_old, lse_new);
+          const float ea = lse_old == -INFINITY ? 0.f : __expf(lse_old - mx);
+          const float eb = lse_new == -INFINITY ? 0.f : __expf(lse_new - mx);
+          const float den = ea + eb;
+          const float iden = den > 0.f ? 1.0f / den : 0.f;
+          w_old = ea * iden;
+          w_new *= eb * iden;
+          lse_new = den > 0.f ? mx + logf(den) : -INFINITY;
+        }
 #pragma unroll
         for (int c0 = 0; c0 < kHD; c0 += 16) {
           uint32_t u[16];
@@ -394,12 +411,19 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
           if (valid) {
             float4* dst = reinterpret_cast<float4*>(p.prefix_o + row * kHD + c0);
 #pragma unroll
-            for (int x = 0; x < 16; x += 4)
-              dst[x / 4] = make_float4(__uint_as_float(u[x]) * inv, __uint_as_float(u[x + 1]) * inv,
-                                       __uint_as_float(u[x + 2]) * inv, __uint_as_float(u[x + 3]) * inv);
+            for (int x = 0; x < 16; x += 4) {
+              float4 o = make_float4(__uint_as_float(u[x]) * w_new, __uint_as_float(u[x + 1]) * w_new,
+                                     __uint_as_float(u[x + 2]) * w_new, __uint_as_float(u[x + 3]) * w_new);
+              if (p.accumulate) {
+                const float4 prev = dst[x / 4];
+                o = make_float4(o.x + w_old * prev.x, o.y + w_old * prev.y, o.z + w_old * prev.z,
+                                o.w + w_old * prev.w);
+              }
+              dst[x / 4] = o;
+            }
           }
         }
-        if (valid) p.prefix_lse[row] = l > 0.f ? (m + log2f(l)) * kLn2C : -INFINITY;
+        if (valid) p.prefix_lse[row] = lse_new;
       } else {
         ok = false;
       }
@@ -449,6 +473,64 @@ CascadeWs cascade_layout(int B, int H_q, int D) {
   off = align_up(off + static_cast<size_t>(B) * H_q * sizeof(float), kWorkspaceAlign);
   w.total = off;
   return w;
+}
+
+// One launch pair (plan + prefix kernel) over groups 0..G-1 of the given CSR
+// arrays: every member row's fp32 state over its group's own pages, written
+// to prefix_o / prefix_lse, or merged into what is there (accumulate).
+ts_status prefix_pass(const void* q, const void* k_pool, const void* v_pool, const int32_t* prefix_indptr,
+                      const int32_t* prefix_pages, const int32_t* prefix_len, const int32_t* member_indptr,
+                      const int32_t* member_ids, int G, int B, int H_q, int H_kv, int num_pages, float scale,
+                      float* prefix_o, float* prefix_lse, int32_t* tile_offset, uint32_t* err_word,
+                      bool accumulate, cudaStream_t s) {
+  const int g = H_q / H_kv;
+  const int mpt = kBM / g;
+  ts_status st;
+  {
+    LaunchTrace trace("cascade_plan_kernel", s);
+    cascade_plan_kernel<<<1, 1024, 0, s>>>(member_indptr, G, mpt, tile_offset);
+    st = cuda_check(cudaGetLastError(), "cascade plan launch");
+  }
+  if (st != TS_OK) return st;
+  CUtensorMap kmap, vmap;
+  st = make_page_map(&kmap, k_pool, num_pages, H_kv);
+  if (st != TS_OK) return st;
+  st = make_page_map(&vmap, v_pool, num_pages, H_kv);
+  if (st != TS_OK) return st;
+  PrefixParams pp;
+  pp.q = static_cast<const __nv_bfloat16*>(q);
+  pp.prefix_indptr = prefix_indptr;
+  pp.prefix_pages = prefix_pages;
+  pp.prefix_len = prefix_len;
+  pp.member_indptr = member_indptr;
+  pp.member_ids = member_ids;
+  pp.tile_offset = tile_offset;
+  pp.num_groups = G;
+  pp.H_q = H_q;
+  pp.H_kv = H_kv;
+  pp.g = g;
+  pp.mpt = mpt;
+  pp.num_pages = num_pages;
+  pp.scale_log2 = scale * kLog2eC;
+  pp.prefix_o = prefix_o;
+  pp.prefix_lse = prefix_lse;
+  pp.err_word = err_word;
+  pp.accumulate = accumulate ? 1 : 0;
+  st = prepare_once(reinterpret_cast<const void*>(cascade_prefix_kernel), [](const void* k) {
+    ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
+                              "prefix smem attribute");
+    if (s2 != TS_OK) return s2;
+    // all of the SM's unified L1/shared memory as shared memory: two CTAs per SM
+    return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           static_cast<int>(cudaSharedmemCarveoutMaxShared)),
+                      "prefix carveout attribute");
+  });
+  if (st != TS_OK) return st;
+  // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
+  const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);
+  LaunchTrace trace("cascade_prefix_kernel", s);
+  cascade_prefix_kernel<<<dim3(tiles, H_kv), kThreadsPfx, kSmemPfx, s>>>(pp, kmap, vmap);
+  return cuda_check(cudaGetLastError(), "cascade prefix launch");
 }
 
 }  // namespace
@@ -515,55 +597,11 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
   float* prefix_lse = reinterpret_cast<float*>(wsb + ws.prefix_lse);
 
   if (G > 0) {
-    int32_t* tile_offset = reinterpret_cast<int32_t*>(wsb + ws.tile_offset);
-    const int mpt = kBM / g;
-    ts_status st;
-    {
-      LaunchTrace trace("cascade_plan_kernel", s);
-      cascade_plan_kernel<<<1, 1024, 0, s>>>(groups->member_indptr, G, mpt, tile_offset);
-      st = cuda_check(cudaGetLastError(), "cascade plan launch");
-    }
-    if (st != TS_OK) return st;
-    CUtensorMap kmap, vmap;
-    st = make_page_map(&kmap, k_pool, num_pages, H_kv);
-    if (st != TS_OK) return st;
-    st = make_page_map(&vmap, v_pool, num_pages, H_kv);
-    if (st != TS_OK) return st;
-    PrefixParams pp;
-    pp.q = static_cast<const __nv_bfloat16*>(q);
-    pp.prefix_indptr = groups->prefix_indptr;
-    pp.prefix_pages = groups->prefix_pages;
-    pp.prefix_len = groups->prefix_len;
-    pp.member_indptr = groups->member_indptr;
-    pp.member_ids = groups->member_ids;
-    pp.tile_offset = tile_offset;
-    pp.num_groups = G;
-    pp.H_q = H_q;
-    pp.H_kv = H_kv;
-    pp.g = g;
-    pp.mpt = mpt;
-    pp.num_pages = num_pages;
-    pp.scale_log2 = scale * kLog2eC;
-    pp.prefix_o = prefix_o;
-    pp.prefix_lse = prefix_lse;
-    pp.err_word = reinterpret_cast<uint32_t*>(wsb);
-    st = prepare_once(reinterpret_cast<const void*>(cascade_prefix_kernel), [](const void* k) {
-      ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPfx),
-                                "prefix smem attribute");
-      if (s2 != TS_OK) return s2;
-      // all of the SM's unified L1/shared memory as shared memory: two CTAs per SM
-      return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                             static_cast<int>(cudaSharedmemCarveoutMaxShared)),
-                        "prefix carveout attribute");
-    });
-    if (st != TS_OK) return st;
-    // upper bound on tiles: sum ceil(n_g / mpt) <= B / mpt + G; extra CTAs exit at once
-    const unsigned tiles = static_cast<unsigned>(B / mpt + G + 1);
-    {
-      LaunchTrace trace("cascade_prefix_kernel", s);
-      cascade_prefix_kernel<<<dim3(tiles, H_kv), kThreadsPfx, kSmemPfx, s>>>(pp, kmap, vmap);
-      st = cuda_check(cudaGetLastError(), "cascade prefix launch");
-    }
+    const ts_status st = prefix_pass(q, k_pool, v_pool, groups->prefix_indptr, groups->prefix_pages,
+                                     groups->prefix_len, groups->member_indptr, groups->member_ids, G, B, H_q,
+                                     H_kv, num_pages, scale, prefix_o, prefix_lse,
+                                     reinterpret_cast<int32_t*>(wsb + ws.tile_offset),
+                                     reinterpret_cast<uint32_t*>(wsb), false, s);
     if (st != TS_OK) return st;
   }
   PrefixInputs pre;
@@ -574,4 +612,73 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
   return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q,
                                   H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                   ws.tile_offset, s, who, G > 0 ? &pre : nullptr);
+}
+
+extern "C" ts_status ts_cascade_nested_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                                   const ts_prefix_forest* forest,
+                                                   const int32_t* level_indptr_host,
+                                                   const int32_t* block_table, int32_t bt_stride,
+                                                   const int32_t* seq_lens, int32_t B, int32_t H_q,
+                                                   int32_t H_kv, int32_t D, int32_t page_size,
+                                                   int32_t num_pages, float scale, ts_dtype dtype,
+                                                   void* out, float* lse, void* workspace,
+                                                   size_t workspace_bytes, void* stream) {
+  using namespace ts;
+  const char* who = "ts_cascade_nested_decode_attn";
+  if (!forest) return fail(TS_ERR_INVALID_ARG, "%s: null forest", who);
+  if (B == 0) return TS_OK;
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d)", who, B, H_q, H_kv);
+  const int g = H_q / H_kv;
+  if (dtype != TS_BF16 || D != kHD || page_size != kPS || (g != 1 && g != 2 && g != 4 && g != 8))
+    return fail(TS_ERR_UNSUPPORTED, "%s: needs bf16, D=64, page_size=16, H_q/H_kv in {1,2,4,8}", who);
+  const int N = forest->num_nodes, L = forest->num_levels;
+  if (N < 0 || L < 0 || (N > 0) != (L > 0)) return fail(TS_ERR_INVALID_ARG, "%s: %d nodes, %d levels", who, N, L);
+  if (N > 0) {
+    if (!level_indptr_host) return fail(TS_ERR_INVALID_ARG, "%s: null host level_indptr", who);
+    if (level_indptr_host[0] != 0 || level_indptr_host[L] != N)
+      return fail(TS_ERR_INVALID_ARG, "%s: level_indptr must run from 0 to num_nodes", who);
+    for (int l = 0; l < L; ++l)
+      if (level_indptr_host[l + 1] <= level_indptr_host[l])
+        return fail(TS_ERR_INVALID_ARG, "%s: level %d holds no node", who, l);
+  }
+  if (!forest->group_of || (N > 0 && (!forest->prefix_indptr || !forest->prefix_pages || !forest->prefix_len ||
+                                      !forest->member_indptr || !forest->member_ids)))
+    return fail(TS_ERR_INVALID_ARG, "%s: null forest array", who);
+  if (!q || !k_pool || !v_pool || !out || !block_table || !seq_lens)
+    return fail(TS_ERR_INVALID_ARG, "%s: null pointer", who);
+  for (const void* ptr : {q, k_pool, v_pool})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+      return fail(TS_ERR_INVALID_ARG, "%s: q and pools must be 16-byte aligned", who);
+  const size_t need = ts_cascade_decode_workspace_size(B, H_q, D);
+  if (need == 0) return fail(TS_ERR_CUDA, "%s: cannot size the workspace", who);
+  if (!workspace || workspace_bytes < need)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace %zu B < %zu B needed", who, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", who);
+  const CascadeWs ws = cascade_layout(B, H_q, D);
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* prefix_o = reinterpret_cast<float*>(wsb + ws.prefix_o);
+  float* prefix_lse = reinterpret_cast<float*>(wsb + ws.prefix_lse);
+  // level by level: the roots write each member's prefix state, deeper levels
+  // merge their stretch into it (a member is in one node per level, so no two
+  // tiles of a launch touch the same row)
+  for (int l = 0; l < L; ++l) {
+    const int n0 = level_indptr_host[l], nl = level_indptr_host[l + 1] - n0;
+    const ts_status st =
+        prefix_pass(q, k_pool, v_pool, forest->prefix_indptr + n0, forest->prefix_pages, forest->prefix_len + n0,
+                    forest->member_indptr + n0, forest->member_ids, nl, B, H_q, H_kv, num_pages, scale, prefix_o,
+                    prefix_lse, reinterpret_cast<int32_t*>(wsb + ws.tile_offset),
+                    reinterpret_cast<uint32_t*>(wsb), l > 0, s);
+    if (st != TS_OK) return st;
+  }
+  PrefixInputs pre;
+  pre.group_of = forest->group_of;   // deepest node
+  pre.prefix_len = forest->prefix_len;  // tokens shared through it
+  pre.prefix_o = prefix_o;
+  pre.prefix_lse = prefix_lse;
+  return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q, H_kv, D, page_size,
+                                  num_pages, scale, dtype, out, lse, workspace, ws.tile_offset, s, who,
+                                  N > 0 ? &pre : nullptr);
 }

@@ -180,3 +180,155 @@ extern "C" ts_status ts_group_prefixes(const int32_t* block_table, int32_t bt_st
   out->num_groups = G;
   return TS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// ts_group_prefixes_nested: the same greedy search kept as a tree.
+//
+// Tokasaurus blog, "Dynamic prefix identification and exploration": the
+// search iteratively finds the longest shared prefixes. Kept as a tree, a
+// prefix shared by a large set and a longer one shared by a subset are both
+// used: the short one once for the whole set, the extension once for the
+// subset. Reading used here:
+//   * a node is a maximal stretch of whole pages [d0, d1) shared by physical
+//     page id by a set of at least min_group sequences that all share the
+//     path above it and may all share d1 pages (cap, as above); its members
+//     are all of them;
+//   * at the node's end the members that can go deeper branch on the next
+//     page; branches of at least min_group sequences become child nodes, the
+//     others (and the members whose cap is reached) end at this node;
+//   * a sequence's node is the deepest one it belongs to, so its shared depth
+//     is the largest d for which at least min_group sequences (itself
+//     included) share its first d pages within their caps;
+//   * nodes are listed level by level (roots first), each level in visiting
+//     order (increasing page ids), members in increasing sequence index.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct NestedGrouper {
+  const int32_t* bt;
+  int64_t stride;
+  const std::vector<int32_t>& cap;
+  int min_group;
+  struct Node {
+    int parent, level, d0, d1;
+    std::vector<int32_t> members;
+  };
+  std::vector<Node> nodes;
+  std::vector<int32_t> deepest;  // per sequence
+
+  int32_t page(int32_t s, int d) const { return bt[s * stride + d]; }
+
+  // end of the stretch that all of M share from depth d (>= d + 1: they share page d)
+  int stretch_end(const std::vector<int32_t>& M, int d) const {
+    int32_t lim = cap[M[0]];
+    for (int32_t s : M) lim = std::min(lim, cap[s]);
+    const int32_t* r0 = bt + static_cast<int64_t>(M[0]) * stride;
+    int32_t e = lim;
+    for (size_t i = 1; i < M.size() && e > d + 1; ++i) {
+      const int32_t* rs = bt + static_cast<int64_t>(M[i]) * stride;
+      if (std::memcmp(rs + d, r0 + d, static_cast<size_t>(e - d) * sizeof(int32_t)) == 0) continue;
+      int32_t t = d;
+      while (t < e && rs[t] == r0[t]) ++t;
+      e = t;
+    }
+    return e;
+  }
+
+  // S: sequences sharing pages [0, d) under `parent`; branch on page d.
+  void branch(const std::vector<int32_t>& S, int d, int parent, int level) {
+    std::vector<std::pair<int32_t, int32_t>> keyed;  // (page at d, sequence)
+    keyed.reserve(S.size());
+    for (int32_t s : S)
+      if (cap[s] > d) keyed.emplace_back(page(s, d), s);
+    std::sort(keyed.begin(), keyed.end());
+    for (size_t i = 0; i < keyed.size();) {
+      size_t j = i;
+      while (j < keyed.size() && keyed[j].first == keyed[i].first) ++j;
+      if (static_cast<int>(j - i) >= min_group) {
+        std::vector<int32_t> M;
+        M.reserve(j - i);
+        for (size_t t = i; t < j; ++t) M.push_back(keyed[t].second);  // increasing index
+        const int e = stretch_end(M, d);
+        const int id = static_cast<int>(nodes.size());
+        nodes.push_back(Node{parent, level, d, e, M});
+        for (int32_t s : M) deepest[s] = id;
+        branch(M, e, id, level + 1);
+      }
+      i = j;
+    }
+  }
+};
+
+}  // namespace
+
+extern "C" ts_status ts_group_prefixes_nested(const int32_t* block_table, int32_t bt_stride,
+                                              const int32_t* seq_lens, int32_t B, int32_t page_size,
+                                              int32_t min_group, ts_prefix_forest* out) {
+  using ts::fail;
+  const char* who = "ts_group_prefixes_nested";
+  if (!out) return fail(TS_ERR_INVALID_ARG, "%s: null output", who);
+  out->num_nodes = 0;
+  out->num_levels = 0;
+  if (B < 0 || bt_stride <= 0 || page_size <= 0 || min_group < 2)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad arguments (B=%d bt_stride=%d page_size=%d min_group=%d)", who, B,
+                bt_stride, page_size, min_group);
+  if (B > 0 && (!block_table || !seq_lens)) return fail(TS_ERR_INVALID_ARG, "%s: null block table or lengths", who);
+  if (!out->prefix_indptr || !out->member_indptr || !out->prefix_len || !out->level_indptr || !out->parent ||
+      (B > 0 && (!out->member_ids || !out->group_of)) || out->capacity_nodes < 0)
+    return fail(TS_ERR_INVALID_ARG, "%s: null output array", who);
+  std::vector<int32_t> cap(static_cast<size_t>(B));
+  std::vector<int32_t> all;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t L = seq_lens[b];
+    int64_t c = L > 0 ? (L - 1) / page_size : 0;
+    if (c > bt_stride) c = bt_stride;
+    cap[b] = static_cast<int32_t>(c);
+    all.push_back(b);
+  }
+  NestedGrouper g{block_table, bt_stride, cap, min_group, {}, std::vector<int32_t>(static_cast<size_t>(B), -1)};
+  g.branch(all, 0, -1, 0);
+
+  // level order: stable by level keeps each level's visiting order
+  const int32_t N = static_cast<int32_t>(g.nodes.size());
+  std::vector<int32_t> order(static_cast<size_t>(N));
+  for (int32_t i = 0; i < N; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return g.nodes[a].level < g.nodes[b].level; });
+  std::vector<int32_t> rank(static_cast<size_t>(N));
+  for (int32_t i = 0; i < N; ++i) rank[order[i]] = i;
+  int32_t levels = 0;
+  int64_t total_pages = 0, total_members = 0;
+  for (const auto& nd : g.nodes) {
+    levels = std::max(levels, nd.level + 1);
+    total_pages += nd.d1 - nd.d0;
+    total_members += static_cast<int64_t>(nd.members.size());
+  }
+  if (N > out->capacity_nodes || levels > out->capacity_levels || total_pages > out->capacity_prefix_pages ||
+      total_members > out->capacity_members || (total_pages > 0 && !out->prefix_pages)) {
+    out->num_nodes = N;
+    out->num_levels = levels;
+    return fail(TS_ERR_CAPACITY,
+                "%s: need %d nodes, %d levels, %lld prefix pages, %lld members (capacities %d, %d, %d, %d)", who,
+                N, levels, static_cast<long long>(total_pages), static_cast<long long>(total_members),
+                out->capacity_nodes, out->capacity_levels, out->capacity_prefix_pages, out->capacity_members);
+  }
+  int32_t pp = 0, mm = 0;
+  out->prefix_indptr[0] = 0;
+  out->member_indptr[0] = 0;
+  for (int32_t l = 0; l <= levels; ++l) out->level_indptr[l] = 0;
+  for (int32_t i = 0; i < N; ++i) {
+    const auto& nd = g.nodes[order[i]];
+    out->level_indptr[nd.level + 1] = i + 1;
+    for (int d = nd.d0; d < nd.d1; ++d)
+      out->prefix_pages[pp++] = block_table[static_cast<int64_t>(nd.members[0]) * bt_stride + d];
+    out->prefix_indptr[i + 1] = pp;
+    out->prefix_len[i] = nd.d1 * page_size;  // tokens shared from the root through this node
+    out->parent[i] = nd.parent >= 0 ? rank[nd.parent] : -1;
+    for (int32_t s : nd.members) out->member_ids[mm++] = s;
+    out->member_indptr[i + 1] = mm;
+  }
+  for (int32_t b = 0; b < B; ++b) out->group_of[b] = g.deepest[b] >= 0 ? rank[g.deepest[b]] : -1;
+  out->num_nodes = N;
+  out->num_levels = levels;
+  return TS_OK;
+}

@@ -8,6 +8,7 @@ import pytest
 
 import paged_kv_cache_46_gb300 as ts
 import workloads
+import oracle
 from oracle import PrefixGroups, check_prefix_groups
 from paged_kv_cache_46_gb300 import build as ts_build
 
@@ -103,3 +104,80 @@ def test_capacity_and_argument_errors():
     assert g["num_groups"] == 1 and list(g["prefix_pages"]) == [1]
     g = ts.ts_group_prefixes(np.zeros((0, 4), np.int32), np.zeros(0, np.int32), 16, 2)
     assert g["num_groups"] == 0
+
+
+# ---------------------------------------------------------------------------
+# Nested (tree) grouping: ts_group_prefixes_nested against the invariant
+# checker, whose maximality pin is a brute-force search.
+# ---------------------------------------------------------------------------
+
+def _check_forest(bt, lens, ps, min_group=2):
+    f = ts.ts_group_prefixes_nested(bt, lens, ps, min_group)
+    oracle.check_prefix_forest(bt, lens, ps, min_group, f)
+    return f
+
+
+def test_forest_hand_example():
+    # pages: 0-3 = system prompt (4 pages); seqs 0-3 share it; 0,1 share 2 more pages; 4 is alone
+    ps = 4
+    bt = np.array([[0, 1, 2, 3, 10, 11, 20, 21],
+                   [0, 1, 2, 3, 10, 11, 22, 23],
+                   [0, 1, 2, 3, 12, 13, 24, 25],
+                   [0, 1, 2, 3, 14, 15, 26, 27],
+                   [30, 31, 32, 33, 34, 35, 36, 37]], np.int32)
+    lens = np.array([29, 32, 20, 30, 32], np.int32)
+    f = _check_forest(bt, lens, ps)
+    assert f["num_nodes"] == 2 and f["num_levels"] == 2
+    assert f["prefix_len"].tolist() == [16, 24]
+    assert f["prefix_pages"].tolist() == [0, 1, 2, 3, 10, 11]
+    assert f["member_ids"].tolist() == [0, 1, 2, 3, 0, 1]
+    assert f["group_of"].tolist() == [1, 1, 0, 0, -1] and f["parent"].tolist() == [-1, 0]
+
+
+def test_forest_cap_splits_a_stretch():
+    # all three share 6 pages, but sequence 2 may share only 3 (length 13, page 4)
+    ps = 4
+    bt = np.array([[5, 6, 7, 8, 9, 1, 40], [5, 6, 7, 8, 9, 1, 41], [5, 6, 7, 8, 9, 1, 42]], np.int32)
+    lens = np.array([28, 25, 13], np.int32)
+    f = _check_forest(bt, lens, ps)
+    assert f["prefix_len"].tolist() == [12, 24] and f["group_of"].tolist() == [1, 1, 0]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_forest_random_prefix_trees(seed):
+    rng = np.random.default_rng(100 + seed)
+    B, ps, depth = 40, 4, 12
+    # random tree: each sequence walks down a small random trie of shared pages
+    bt = np.zeros((B, depth), np.int32)
+    nxt = [1000]
+    children = {}
+    for b in range(B):
+        node = ()
+        for d in range(depth):
+            kids = children.setdefault(node, [])
+            if kids and rng.random() < 0.7:
+                pg = kids[rng.integers(len(kids))]
+            else:
+                pg = nxt[0]
+                nxt[0] += 1
+                kids.append(pg)
+            bt[b, d] = pg
+            node = node + (pg,)
+    lens = rng.integers(1, depth * ps + 1, size=B).astype(np.int32)
+    for mg in (2, 3, 5):
+        _check_forest(bt, lens, ps, mg)
+
+
+def test_forest_on_the_cascade_workload_structure():
+    case = workloads.shared_prefix_cascade(groups=2, members=64, values=False)
+    f = _check_forest(case.block_table, case.attn_lens, case.page_size)
+    assert f["num_levels"] >= 1 and set(f["group_of"].tolist()) != {-1}
+
+
+def test_forest_arguments():
+    bt = np.zeros((2, 2), np.int32)
+    lens = np.array([9, 9], np.int32)
+    with pytest.raises(ts.TSError):
+        ts.ts_group_prefixes_nested(bt, lens, 4, 1)  # min_group < 2
+    f = ts.ts_group_prefixes_nested(np.zeros((0, 1), np.int32), np.zeros(0, np.int32), 4)
+    assert f["num_nodes"] == 0

@@ -122,11 +122,12 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
                pool_factor: float = 1.25, shared_groups: Optional[List[np.ndarray]] = None,
                shared_pages: int = 0, device="cpu", rng: Optional[np.random.Generator] = None,
                extra_pages: int = 1, num_pages: Optional[int] = None, values: bool = True,
-               q_len: int = 1) -> PagedCase:
+               q_len: int = 1, layout: Optional[tuple] = None) -> PagedCase:
     """Build a case: lengths -> page need -> shuffled pool -> block tables -> values.
 
     ``q_len`` > 1 draws ``q_len`` query tokens per sequence (q [B, q_len, H_q, D]);
-    ``seq_lens`` then already count them.
+    ``seq_lens`` then already count them. ``layout`` = (block_table, num_pages)
+    replaces the page assignment (a caller-built sharing structure).
 
     ``shared_groups``: lists of sequence ids; each list shares its first
     ``shared_pages`` pages by physical id (the cascade workload).
@@ -135,6 +136,10 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
     lens = np.asarray(seq_lens, dtype=np.int32)
     assert len(lens) == B
     attn = lens + (1 if append else 0)
+    if layout is not None:
+        bt, num_pages = np.asarray(layout[0], dtype=np.int32), int(layout[1])
+        return _finish_case(name, seed, B, H_q, H_kv, D, page_size, lens, dtype, scale, append, mla, Dv,
+                            num_pages, bt, 0, None, 0, values, device, q_len)
     n_alloc = _pages_for(attn, page_size)                  # pages each sequence needs
     own = n_alloc.copy()
     if shared_groups:
@@ -163,6 +168,14 @@ def build_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
         cursor += n_own
     assert cursor == need
 
+    return _finish_case(name, seed, B, H_q, H_kv, D, page_size, lens, dtype, scale, append, mla, Dv, num_pages,
+                        bt, sentinel, shared_groups, shared_pages, values, device, q_len)
+
+
+def _finish_case(name, seed, B, H_q, H_kv, D, page_size, lens, dtype, scale, append, mla, Dv, num_pages, bt,
+                 sentinel, shared_groups, shared_pages, values, device, q_len) -> PagedCase:
+    """Values of a case whose page layout is fixed: NaN sentinels on rows holding
+    no cached token, seeded N(0,1) pools, queries and appended rows."""
     # NaN sentinel mask over [num_pages, page_size]: everything not holding a
     # cached token of some sequence (the pending append row included).
     sentinel_rows = np.ones((num_pages, page_size), dtype=bool)
@@ -254,6 +267,46 @@ def build_fp8_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
     base.q, base.k_pool, base.v_pool, base.k_new, base.v_new = q, k_pool, v_pool, k_new, v_new
     base.kv_fp8, base.k_scale, base.v_scale = True, k_scale, v_scale
     return base
+
+
+def nested_prefix_cascade(device="cpu", seed: int = 8, roots: int = 4, subs: int = 4, members: int = 256,
+                          root_tokens: int = 1024, sub_tokens: int = 1024, suffix_lo: int = 64,
+                          suffix_hi: int = 512, values: bool = True) -> PagedCase:
+    """Two-level shared prefixes: ``roots`` root prefixes (``root_tokens``
+    each, e.g. a system prompt) each followed by ``subs`` second-level
+    prefixes (``sub_tokens``, e.g. a problem statement) each shared by
+    ``members`` sequences with their own suffix U[suffix_lo, suffix_hi];
+    32/8 heads, D=64, bf16, page 16; pages shuffled over a 1.25x pool."""
+    ps = 16
+    rng = np.random.default_rng(seed)
+    B = roots * subs * members
+    rp, sp = root_tokens // ps, sub_tokens // ps
+    suffix = rng.integers(suffix_lo, suffix_hi + 1, size=B).astype(np.int32)
+    lens = (rp + sp) * ps + suffix
+    own = _pages_for(lens, ps) - rp - sp
+    need = roots * rp + roots * subs * sp + int(own.sum())
+    num_pages = int(math.ceil(1.25 * need))
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((B, int((rp + sp + own).max())), perm[need], dtype=np.int32)
+    cur = 0
+    for r in range(roots):
+        root = perm[cur:cur + rp]
+        cur += rp
+        for k in range(subs):
+            sub = perm[cur:cur + sp]
+            cur += sp
+            for m in range(members):
+                b = (r * subs + k) * members + m
+                bt[b, :rp], bt[b, rp:rp + sp] = root, sub
+    for b in range(B):
+        bt[b, rp + sp:rp + sp + own[b]] = perm[cur:cur + own[b]]
+        cur += int(own[b])
+    assert cur == need
+    case = build_case(f"nested_cascade_{roots}x{subs}x{members}", seed, B=B, H_q=32, H_kv=8, D=64, page_size=ps,
+                      seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(64), device=device, rng=rng,
+                      values=values, layout=(bt, num_pages))
+    case.meta.update(roots=roots, subs=subs, members=members, root_pages=rp, sub_pages=sp)
+    return case
 
 
 def llama3_8b_layer_fp8(device="cpu", seed: int = 7, B: int = 64, lo: int = 512, hi: int = 4096,
