@@ -1,0 +1,457 @@
+// Tensor-core path of ts_paged_decode_multi_attn: decode with q_len new query
+// tokens per sequence (speculative verify) when their rows fill a real tile.
+//
+// TokenSpeed deep dive, section 7.2 (fold_sq_factor): folding query tokens
+// into the head dimension turns the rows of a decode step into a tile that
+// the tensor cores can take. Here one CTA takes one (sequence, kv head): its
+// R = q_len x g query rows (token j, head h*g + i at row j*g + i; rows past R
+// are zero) attend the sequence's pages as S = Q K^T and O += P V on tcgen05,
+// 128 keys per tile, with the online softmax between them and the causal
+// limit of each token (row of token j: keys before L - q_len + 1 + j).
+//
+// Roles (192 threads): warps 0-3 own one query row per thread (Q load,
+// softmax, epilogue; warps whose 32 rows are all padding skip the softmax),
+// warp 4 issues the TMA loads of K and V page boxes (its lanes hold the page
+// ids of the next key tile), warp 5 lane 0 issues the MMAs, S(j+1) or P V(j)
+// whichever is ready first. TMEM: S (128 fp32 columns), O (D columns), P (64
+// columns of bf16 pairs, the P V product's A operand). K and V tiles are
+// double-buffered; at D = 128 the K, V and Q tiles are two 64-column atoms
+// each and V's atoms are read by one N = 128 product.
+#include <cmath>
+#include <cstdlib>
+
+#include "ts_tcgen05.cuh"
+
+namespace ts {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per tile
+constexpr int kPS = 16;   // page size of this path
+constexpr int kPagesPerTile = kBN / kPS;
+constexpr int kThreads = 192;
+constexpr int kAtom = kBN * 128;  // one [128 rows x 64 bf16] SW128 atom: 16 KB
+constexpr int kStages = 3;        // K and V tile buffers
+constexpr float kLog2eC = 1.4426950408889634f;
+constexpr float kLn2C = 0.6931471805599453f;
+constexpr float kSlack = 8.0f;
+
+template <int kHD>
+struct Layout {
+  static constexpr int kAtoms = kHD / 64;
+  static constexpr int kOffQ = 0;                          // kAtoms atoms of Q
+  static constexpr int kOffK = kOffQ + kAtoms * kAtom;     // kStages buffers x kAtoms atoms
+  static constexpr int kOffV = kOffK + kStages * kAtoms * kAtom;
+  static constexpr int kOffBar = kOffV + kStages * kAtoms * kAtom;
+  static constexpr int kOffTmem = kOffBar + 128;
+  static constexpr int kSmem = kOffTmem + 16;
+  static constexpr uint32_t kTmemO = 128;
+  static constexpr uint32_t kTmemP = 128 + kHD;            // bf16 pairs: key k of row r at column k/2
+  static constexpr uint32_t kTmemCols = kHD == 64 ? 256 : 512;
+  static constexpr int kMinBlocks = 1;  // a softmax thread keeps its 128 scores in registers
+};
+
+struct MqParams {
+  const __nv_bfloat16* q;       // [B, q_len, H_q, D]
+  __nv_bfloat16* out;           // [B, q_len, H_q, D]
+  float* lse;                   // [B, q_len, H_q] or nullptr
+  const int32_t* block_table;   // [B, bt_stride]
+  const int32_t* seq_lens;      // [B], counting the q_len new tokens
+  int32_t bt_stride, q_len, H_q, H_kv, g, num_pages;
+  float scale_log2;
+  uint32_t* err_word;
+};
+
+template <int kHD>
+__global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kernel(
+    const MqParams p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  using Lay = Layout<kHD>;
+  constexpr int kAtoms = Lay::kAtoms;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, b = blockIdx.y;
+  // Programmatic dependent launch: outputs are written only after the wait.
+  pdl_launch_dependents();
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) set_device_error(p.err_word, TS_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  const int R = p.q_len * p.g;   // real rows
+  const int L = p.seq_lens[b];   // tokens in the cache, the q_len new ones included
+  const int n_pages = L > 0 ? min((L + kPS - 1) / kPS, p.bt_stride) : 0;
+  const int n_kt = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
+  // Before this wait only the lengths are read (the queries, the pools with
+  // freshly appended rows and the outputs may belong to the previous kernel).
+  pdl_wait_primary();
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
+  // key tile j lives in buffer j % kStages as that buffer's (j / kStages)-th use
+  auto b_kfull = [&](int buf) { return smem_u32(&bars[0 * kStages + buf]); };
+  auto b_vfull = [&](int buf) { return smem_u32(&bars[1 * kStages + buf]); };
+  auto b_kempty = [&](int buf) { return smem_u32(&bars[2 * kStages + buf]); };
+  auto b_vempty = [&](int buf) { return smem_u32(&bars[3 * kStages + buf]); };
+  const uint32_t b_sfull = smem_u32(&bars[4 * kStages]), b_sfree = smem_u32(&bars[4 * kStages + 1]);
+  const uint32_t b_pfull = smem_u32(&bars[4 * kStages + 2]), b_pvdone = smem_u32(&bars[4 * kStages + 3]);
+  static_assert((4 * kStages + 4) * 8 <= 128, "mbarriers fit their slot");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
+  const uint32_t sQ = smem_u32(smem + Lay::kOffQ), sK = smem_u32(smem + Lay::kOffK);
+  const uint32_t sV = smem_u32(smem + Lay::kOffV);
+  constexpr int kTileKV = kAtoms * kAtom;  // one K (or V) tile: 128 keys x D
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(b_kfull(i), 1);
+      mbar_init(b_vfull(i), 1);
+      mbar_init(b_kempty(i), 1);
+      mbar_init(b_vempty(i), 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 4);
+    mbar_init(b_pfull, 4);
+    mbar_init(b_pvdone, 1);
+    fence_mbar_init();
+  }
+  // Q tile: row r = (token r / g, head h*g + r % g); rows past R are zero.
+  if (warp < 4) {
+    const int r = tid;
+    const bool real = r < R;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + ((static_cast<int64_t>(b) * p.q_len + (real ? r / p.g : 0)) * p.H_q + h * p.g + r % p.g) * kHD);
+#pragma unroll
+    for (int a = 0; a < kAtoms; ++a) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = real ? src[a * 8 + c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(smem + Lay::kOffQ + a * kAtom + sw128_off(r, c)) = v;
+      }
+    }
+    fence_async_smem();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 4) {
+    // ---------------- TMA producer (lane 0 issues; lane i < 8 holds page i) ----
+    const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
+    auto tile_rows = [&](int j) {       // this lane's page of key tile j, as a pool row
+      const int pi = j * kPagesPerTile + lane;
+      int row = oob;
+      if (lane < kPagesPerTile && pi < n_pages) {
+        const int page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + pi];
+        if (page >= 0 && page < p.num_pages)
+          row = page * kPS;
+        else
+          set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
+      }
+      return row;
+    };
+    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int rows) {
+      if (lane == 0) mbar_arrive_expect_tx(bar, kTileKV);
+#pragma unroll
+      for (int i = 0; i < kPagesPerTile; ++i) {
+        const int row = __shfl_sync(0xffffffffu, rows, i);
+        if (lane == 0)
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) tma_load_3d(dst + a * kAtom + i * (kPS * 128), map, a * 64, h, row, bar);
+      }
+    };
+    int rows = n_kt > 0 ? tile_rows(0) : oob;
+    for (int j = 0; j < n_kt && ok; ++j) {
+      const int rows_next = j + 1 < n_kt ? tile_rows(j + 1) : oob;  // page ids one tile ahead
+      const int buf = j % kStages, ph = (j / kStages - 1) & 1;  // buffer; phase of its previous use
+      ok = __shfl_sync(0xffffffffu, lane == 0 && j >= kStages ? mbar_wait(b_kempty(buf), ph) : true, 0);
+      if (!ok) break;
+      load_tile(&kmap, sK + buf * kTileKV, b_kfull(buf), rows);
+      ok = __shfl_sync(0xffffffffu, lane == 0 && j >= kStages ? mbar_wait(b_vempty(buf), ph) : true, 0);
+      if (!ok) break;
+      load_tile(&vmap, sV + buf * kTileKV, b_vfull(buf), rows);
+      rows = rows_next;
+    }
+    if (!ok && lane == 0) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t iS = idesc_bf16(kBM, kBN, 0);
+      constexpr uint32_t iO = idesc_bf16(kBM, kHD, 1);
+      auto issue_s = [&](int js) {
+        tc_fence_after();
+        const uint32_t sKj = sK + (js % kStages) * kTileKV;
+#pragma unroll
+        for (int ks = 0; ks < kHD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kAtom + (ks & 3) * 32;  // atom, then 16 dims within it
+          mma_bf16(tmem, desc_sw128(sQ + off), desc_sw128(sKj + off), iS, ks > 0);
+        }
+        mma_commit(b_sfull);
+        mma_commit(b_kempty(js % kStages));
+      };
+      int js = 0;
+      if (n_kt > 0) {
+        ok = mbar_wait(b_kfull(0), 0);
+        if (ok) issue_s(js++);
+      }
+      for (int j = 0; j < n_kt && ok; ++j) {
+        const int buf = j % kStages;
+        const unsigned long long t0 = globaltimer_ns();
+        while (true) {
+          if (js < n_kt && mbar_test(b_sfree, (js - 1) & 1) &&
+              mbar_test(b_kfull(js % kStages), (js / kStages) & 1))
+            issue_s(js++);
+          if (mbar_test(b_pfull, j & 1) && mbar_test(b_vfull(buf), (j / kStages) & 1)) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sVj = sV + buf * kTileKV;
+        // O[:, 0:D] += P V: V is MN-major over its 64-column atoms (LBO = atom stride)
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_bf16_tmem_a(tmem + Lay::kTmemO, tmem + Lay::kTmemP + ks * 8, desc_sw128(sVj + ks * 2048, kAtom, 1024),
+                          iO, (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(b_pvdone);
+        mma_commit(b_vempty(buf));
+      }
+      if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ---------------- softmax warps: thread = query row ----------------
+    // A warp whose 32 rows are all padding only keeps the barrier protocol:
+    // its rows' S, P and O lanes are never read into an output.
+    const int r = tid;
+    const bool warp_real = warp * 32 < R;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int jt = r / p.g;                        // this row's token
+    const int lim = L - p.q_len + 1 + jt;          // keys it may attend
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_kt && ok; ++j) {
+      ok = mbar_wait(b_sfull, j & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kBN];
+      if (warp_real) {
+#pragma unroll
+        for (int c0 = 0; c0 < kBN; c0 += 16) {
+          uint32_t u[16];
+          tmem_ld16(trow + c0, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) s[c0 + x] = __uint_as_float(u[x]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sfree);
+      // the previous P V must be done before P and O are touched
+      if (j > 0) {
+        ok = mbar_wait(b_pvdone, (j - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (warp_real) {
+        const int key0 = j * kBN;
+        // keys at or past this row's limit are masked (the sequence's end, the
+        // causal limit of its token); the scale is folded into the exponent
+        const float sl = p.scale_log2;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          s[c] = key0 + c < lim ? s[c] * sl : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+        const bool need = mx > m + kSlack;
+        if (j == 0) {
+          m = mx;
+        } else if (__any_sync(0xffffffffu, need)) {
+          const float mnew = fmaxf(m, mx);
+          const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
+          m = mnew;
+          l *= alpha;
+#pragma unroll
+          for (int c0 = 0; c0 < kHD; c0 += 16) {
+            uint32_t u[16];
+            tmem_ld16(trow + Lay::kTmemO + c0, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+            tmem_st16(trow + Lay::kTmemO + c0, u);
+          }
+          tmem_wait_st();
+        }
+        const float ms = m == -INFINITY ? 0.f : m;
+        float2 ls2 = make_float2(0.f, 0.f);
+        // P straight into TMEM (the P V MMA reads its A operand there)
+#pragma unroll
+        for (int c = 0; c < kBN; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const float e0 = fast_exp2(s[c + x] - ms);
+            const float e1 = fast_exp2(s[c + x + 1] - ms);
+            ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+            pk[x / 2] = float2_to_bf16x2(e0, e1);
+          }
+          tmem_st16(trow + Lay::kTmemP + c / 2, pk);
+        }
+        tmem_wait_st();
+        l += ls2.x + ls2.y;
+      }
+      // The last tile's V rows past the sequence may hold anything (NaN
+      // included) and 0 * NaN is NaN in the product: zero them once landed.
+      const int vrow0 = L - j * kBN;
+      if (j == n_kt - 1 && vrow0 < kBN) {
+        const int buf = j % kStages;
+        ok = mbar_wait(b_vfull(buf), (j / kStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        if (r >= vrow0) {
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(smem + Lay::kOffV + buf * kTileKV + a * kAtom + r * 128 + c * 16) =
+                  make_uint4(0, 0, 0, 0);
+        }
+        fence_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pfull);
+    }
+    // epilogue: O row / l in bf16 and the LSE (no key: O = 0, LSE = -inf)
+    if (ok && n_kt > 0) {
+      ok = mbar_wait(b_pvdone, (n_kt - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) ok = false;
+      else tc_fence_after();
+    }
+    if (ok && warp_real) {
+      const bool real = r < R;
+      const int64_t row = (static_cast<int64_t>(b) * p.q_len + jt) * p.H_q + h * p.g + r % p.g;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < kHD; c0 += 16) {
+        uint32_t u[16];
+        if (n_kt > 0) {
+          tmem_ld16(trow + Lay::kTmemO + c0, u);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) u[x] = 0u;
+        }
+        if (real) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * kHD + c0);
+#pragma unroll
+          for (int x = 0; x < 16; x += 8)
+            dst[x / 8] = make_uint4(float2_to_bf16x2(__uint_as_float(u[x]) * inv, __uint_as_float(u[x + 1]) * inv),
+                                    float2_to_bf16x2(__uint_as_float(u[x + 2]) * inv, __uint_as_float(u[x + 3]) * inv),
+                                    float2_to_bf16x2(__uint_as_float(u[x + 4]) * inv, __uint_as_float(u[x + 5]) * inv),
+                                    float2_to_bf16x2(__uint_as_float(u[x + 6]) * inv, __uint_as_float(u[x + 7]) * inv));
+        }
+      }
+      if (real && p.lse) p.lse[row] = l > 0.f ? (m + log2f(l)) * kLn2C : -INFINITY;
+    }
+    if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+// 3-D map over a pool [P * 16 rows][H_kv][D] bf16 with a box of one page of
+// one kv head and 64 columns (16 rows x 128 B), 128-byte swizzle, zero fill.
+ts_status make_map(CUtensorMap* map, const void* pool, int num_pages, int H_kv, int D) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
+                        static_cast<cuuint64_t>(num_pages) * kPS};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H_kv) * D * 2};
+  cuuint32_t box[3] = {64, 1, kPS};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(res));
+  return TS_OK;
+}
+
+template <int kHD>
+ts_status launch(const MqParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap, int B, cudaStream_t s) {
+  using Lay = Layout<kHD>;
+  ts_status st = prepare_once(reinterpret_cast<const void*>(mq_tc_kernel<kHD>), [](const void* k) {
+    ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kHD>::kSmem),
+                              "multi-query tensor-core smem attribute");
+    if (s2 != TS_OK) return s2;
+    return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           static_cast<int>(cudaSharedmemCarveoutMaxShared)),
+                      "multi-query tensor-core carveout attribute");
+  });
+  if (st != TS_OK) return st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.H_kv, B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Lay::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  LaunchTrace trace("mq_tc_kernel", s);
+  return cuda_check(cudaLaunchKernelEx(&cfg, mq_tc_kernel<kHD>, prm, kmap, vmap), "multi-query tensor-core launch");
+}
+
+}  // namespace
+
+// Runs the tensor-core path when it applies (bf16, page 16, D 64 or 128,
+// q_len * g <= 128, 16-byte aligned rows); TS_ERR_UNSUPPORTED otherwise, with
+// nothing enqueued, so that the caller takes the CUDA-core path.
+ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                                int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
+                                int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream) {
+  const int g = H_q / H_kv;
+  if (dtype != TS_BF16 || page_size != kPS || (D != 64 && D != 128) || q_len < 1 || q_len * g > kBM ||
+      H_kv > 65535 || B > 65535)
+    return TS_ERR_UNSUPPORTED;
+  MqParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.bt_stride = bt_stride;
+  prm.q_len = q_len;
+  prm.H_q = H_q;
+  prm.H_kv = H_kv;
+  prm.g = g;
+  prm.num_pages = num_pages;
+  prm.scale_log2 = scale * kLog2eC;
+  prm.err_word = err_word;
+  CUtensorMap kmap, vmap;
+  ts_status st = make_map(&kmap, k_pool, num_pages, H_kv, D);
+  if (st != TS_OK) return st;
+  st = make_map(&vmap, v_pool, num_pages, H_kv, D);
+  if (st != TS_OK) return st;
+  return D == 64 ? launch<64>(prm, kmap, vmap, B, stream) : launch<128>(prm, kmap, vmap, B, stream);
+}
+
+}  // namespace ts

@@ -36,6 +36,8 @@
 //     sequence) or an fp32 partial state into one of the CTA's two workspace
 //     slots (first / last segment of its range). The merge kernel, launched
 //     with programmatic dependent launch, reduces the split sequences.
+#include <cstring>
+
 #include "ts_paged_decode_kernel.cuh"
 
 namespace ts {
@@ -174,6 +176,12 @@ int gqa_fold(int g, int q_len) {
 
 // Launches the paged split-KV kernel pair for q_len query tokens per
 // sequence; `pre` non-null selects prefix (cascade) mode (q_len 1 only).
+// Tensor-core path for several query tokens per sequence (ts_mq_tc.cu).
+ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                                int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
+                                int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream);
+
 // Group scales of an fp8 (e4m3fn) cache, [num_pages, page_size, H_kv] each.
 struct Fp8Scales {
   const float* k_scale;
@@ -459,6 +467,26 @@ extern "C" ts_status ts_paged_decode_multi_attn(const void* q, const void* k_poo
                                                 ts_dtype dtype, void* out, float* lse,
                                                 void* workspace, size_t workspace_bytes,
                                                 void* stream) {
+  // Two or more query tokens fill a tensor-core tile: one CTA per (sequence,
+  // kv head) on tcgen05 when the shape allows it (TS_MULTI_QUERY_PATH=cuda
+  // forces the CUDA-core kernel; tests compare both).
+  const char* path = getenv("TS_MULTI_QUERY_PATH");
+  const bool tc_allowed = !(path && std::strcmp(path, "cuda") == 0);
+  if (tc_allowed && q_len >= 2 && B > 0 && H_q > 0 && H_kv > 0 && H_q % H_kv == 0 && q && k_pool && v_pool &&
+      block_table && seq_lens && out && bt_stride > 0 && num_pages > 0 && std::isfinite(scale) &&
+      reinterpret_cast<uintptr_t>(q) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(k_pool) % 16 == 0 && reinterpret_cast<uintptr_t>(v_pool) % 16 == 0) {
+    const size_t need = ts::paged_decode_multi_workspace_bytes(B, q_len, H_q, D);
+    if (!workspace || need == 0 || workspace_bytes < need ||
+        reinterpret_cast<uintptr_t>(workspace) % ts::kWorkspaceAlign != 0)
+      return ts::fail(TS_ERR_WORKSPACE, "ts_paged_decode_multi_attn: workspace %zu B < %zu B needed or misaligned",
+                      workspace_bytes, need);
+    const ts_status st = ts::launch_multi_query_tc(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, q_len,
+                                                   H_q, H_kv, D, page_size, num_pages, scale, dtype, out, lse,
+                                                   static_cast<uint32_t*>(workspace),
+                                                   static_cast<cudaStream_t>(stream));
+    if (st != TS_ERR_UNSUPPORTED) return st;
+  }
   return ts::paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, q_len, H_q,
                                H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                workspace_bytes, static_cast<cudaStream_t>(stream),

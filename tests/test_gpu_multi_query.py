@@ -29,11 +29,15 @@ def _case(name, seed, lens, q_len, H_q=32, H_kv=8, D=128, ps=16, dtype="bf16"):
                                 seq_lens=lens, dtype=dtype, scale=D ** -0.5, device=DEV, q_len=q_len)
 
 
-def _run(case, q_len, ctas=None):
+def _run(case, q_len, ctas=None, path=None):
+    """path: None = the library's choice (tensor cores where the shape allows),
+    "cuda" = the CUDA-core split-KV kernel."""
     bt = torch.from_numpy(case.block_table).to(DEV)
     lens = torch.from_numpy(case.seq_lens).to(DEV)
     if ctas is not None:
         os.environ["TS_PAGED_DECODE_CTAS"] = str(ctas)
+    if path is not None:
+        os.environ["TS_MULTI_QUERY_PATH"] = path
     try:
         ws = ts.new_workspace(ts.ts_paged_decode_multi_workspace_size(case.B, q_len, case.H_q, case.D))
         out, lse = ts.ts_paged_decode_multi_attn(case.q, case.k_pool, case.v_pool, bt, lens, case.scale,
@@ -42,6 +46,7 @@ def _run(case, q_len, ctas=None):
         assert ts.ts_read_device_error(ws) == 0
     finally:
         os.environ.pop("TS_PAGED_DECODE_CTAS", None)
+        os.environ.pop("TS_MULTI_QUERY_PATH", None)
     return out, lse
 
 
@@ -69,16 +74,16 @@ def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, dtype):
     lens[2] = 33
     case = _case(f"mq_{q_len}_{H_q}_{H_kv}_{D}_{dtype}", 61 + q_len, lens, q_len, H_q, H_kv, D, dtype=dtype)
     o_ref, l_ref = _oracle(case)
-    for ctas in (None, 5):
-        out, lse = _run(case, q_len, ctas)
-        compare(out, o_ref, dtype, lse, l_ref, f"q_len={q_len} {H_q}/{H_kv} D={D} {dtype} ctas={ctas}")
+    for ctas, path in ((None, None), (None, "cuda"), (5, "cuda")):
+        out, lse = _run(case, q_len, ctas, path)
+        compare(out, o_ref, dtype, lse, l_ref, f"q_len={q_len} {H_q}/{H_kv} D={D} {dtype} ctas={ctas} path={path}")
 
 
 @pytest.mark.parametrize("ctas", [1, 7, None, 1000])
 def test_multi_query_independent_of_split_pattern(ctas):
     lens = [4, 5, 19, 64, 700, 2049, 31, 300]
     case = _case("mq_split", 71, lens, 4)
-    out, lse = _run(case, 4, ctas)
+    out, lse = _run(case, 4, ctas, "cuda")
     o_ref, l_ref = _oracle(case)
     compare(out, o_ref, "bf16", lse, l_ref, f"ctas={ctas}")
 
@@ -101,6 +106,21 @@ def test_full_llama_shape_with_two_draft_tokens():
     rng = np.random.default_rng(2)
     lens = rng.integers(512, 4097, size=64)
     case = _case("mq_llama", 2, lens, 2)
-    out, lse = _run(case, 2)
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, "llama shape q_len=2")
+    for path in (None, "cuda"):
+        out, lse = _run(case, 2, path=path)
+        compare(out, o_ref, "bf16", lse, l_ref, f"llama shape q_len=2 path={path}")
+
+
+@pytest.mark.parametrize("q_len,H_q,H_kv,D", [(4, 32, 8, 128), (8, 64, 8, 128), (16, 32, 4, 64), (3, 8, 1, 64)])
+def test_tensor_core_path_shapes(q_len, H_q, H_kv, D):
+    """Rows q_len * g from 24 to 128 on the tensor-core path (one CTA per
+    sequence and kv head), including sequences shorter than a key tile, a
+    context of only the new tokens, and one past a tile boundary."""
+    rng = np.random.default_rng(q_len * 7 + D)
+    lens = rng.integers(q_len, 3000, size=6)
+    lens[0], lens[1], lens[2] = q_len, 127 + q_len, 128
+    case = _case(f"mq_tc_{q_len}_{H_q}_{H_kv}_{D}", 91 + q_len, lens, q_len, H_q, H_kv, D)
+    out, lse = _run(case, q_len)
+    o_ref, l_ref = _oracle(case)
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D}")
