@@ -633,8 +633,8 @@ def run_ours(args):
         dom_bytes, dom_flops = forest_suffix, 0
     # the file holding the dominant kernel's device code (its hash ties a
     # recorded DRAM-traffic figure to the code that produced it)
-    source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu"}.get(
-        dom, "ts_paged_decode_kernel.cuh")
+    source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu",
+              "mq_tc_kernel": "ts_mq_tc.cu"}.get(dom, "ts_paged_decode_kernel.cuh")
     hbm_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = kernel_traffic(f"{dom}__{args.workload}.md", source)
     if case.mla:

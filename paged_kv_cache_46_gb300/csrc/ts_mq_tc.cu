@@ -46,11 +46,13 @@ struct Layout {
   static constexpr int kOffK = kOffQ + kAtoms * kAtom;     // kStages buffers x kAtoms atoms
   static constexpr int kOffV = kOffK + kStages * kAtoms * kAtom;
   static constexpr int kOffBar = kOffV + kStages * kAtoms * kAtom;
-  static constexpr int kOffTmem = kOffBar + 128;
+  static constexpr int kOffTmem = kOffBar + 256;
   static constexpr int kSmem = kOffTmem + 16;
   static constexpr uint32_t kTmemO = 128;
-  static constexpr uint32_t kTmemP = 128 + kHD;            // bf16 pairs: key k of row r at column k/2
-  static constexpr uint32_t kTmemCols = kHD == 64 ? 256 : 512;
+  // two P buffers of 64 columns (bf16 pairs: key k of row r at column k/2):
+  // the softmax writes P(j+1) while P V(j) still reads P(j)
+  static constexpr uint32_t kTmemP = 128 + kHD;
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr int kMinBlocks = 1;  // a softmax thread keeps its 128 scores in registers
 };
 
@@ -94,8 +96,10 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   auto b_kempty = [&](int buf) { return smem_u32(&bars[2 * kStages + buf]); };
   auto b_vempty = [&](int buf) { return smem_u32(&bars[3 * kStages + buf]); };
   const uint32_t b_sfull = smem_u32(&bars[4 * kStages]), b_sfree = smem_u32(&bars[4 * kStages + 1]);
-  const uint32_t b_pfull = smem_u32(&bars[4 * kStages + 2]), b_pvdone = smem_u32(&bars[4 * kStages + 3]);
-  static_assert((4 * kStages + 4) * 8 <= 128, "mbarriers fit their slot");
+  // per P buffer: written by the softmax (4 warps) / read by its P V product
+  auto b_pfull = [&](int pb) { return smem_u32(&bars[4 * kStages + 2 + pb]); };
+  auto b_pvdone = [&](int pb) { return smem_u32(&bars[4 * kStages + 4 + pb]); };
+  static_assert((4 * kStages + 6) * 8 <= 256, "mbarriers fit their slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
   const uint32_t sQ = smem_u32(smem + Lay::kOffQ), sK = smem_u32(smem + Lay::kOffK);
   const uint32_t sV = smem_u32(smem + Lay::kOffV);
@@ -110,8 +114,10 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     }
     mbar_init(b_sfull, 1);
     mbar_init(b_sfree, 4);
-    mbar_init(b_pfull, 4);
-    mbar_init(b_pvdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_pfull(i), 4);
+      mbar_init(b_pvdone(i), 1);
+    }
     fence_mbar_init();
   }
   // Q tile: row r = (token r / g, head h*g + r % g); rows past R are zero.
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
           if (js < n_kt && mbar_test(b_sfree, (js - 1) & 1) &&
               mbar_test(b_kfull(js % kStages), (js / kStages) & 1))
             issue_s(js++);
-          if (mbar_test(b_pfull, j & 1) && mbar_test(b_vfull(buf), (j / kStages) & 1)) break;
+          if (mbar_test(b_pfull(j & 1), (j >> 1) & 1) && mbar_test(b_vfull(buf), (j / kStages) & 1)) break;
           if (globaltimer_ns() - t0 > kWaitLimitNs) {
             ok = false;
             break;
@@ -215,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         // O[:, 0:D] += P V: V is MN-major over its 64-column atoms (LBO = atom stride)
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_bf16_tmem_a(tmem + Lay::kTmemO, tmem + Lay::kTmemP + ks * 8, desc_sw128(sVj + ks * 2048, kAtom, 1024),
+          mma_bf16_tmem_a(tmem + Lay::kTmemO, tmem + Lay::kTmemP + (j & 1) * 64 + ks * 8,
+                          desc_sw128(sVj + ks * 2048, kAtom, 1024),
                           iO, (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(b_pvdone);
+        mma_commit(b_pvdone(j & 1));
         mma_commit(b_vempty(buf));
       }
       if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
@@ -253,15 +260,6 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_sfree);
-      // the previous P V must be done before P and O are touched
-      if (j > 0) {
-        ok = mbar_wait(b_pvdone, (j - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
       if (warp_real) {
         const int key0 = j * kBN;
         // keys at or past this row's limit are masked (the sequence's end, the
@@ -277,6 +275,13 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         if (j == 0) {
           m = mx;
         } else if (__any_sync(0xffffffffu, need)) {
+          // O is rescaled: every P V issued so far (the last is P V(j-1)) must be done
+          ok = mbar_wait(b_pvdone((j - 1) & 1), ((j - 1) >> 1) & 1);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float mnew = fmaxf(m, mx);
           const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
           m = mnew;
@@ -294,6 +299,15 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         }
         const float ms = m == -INFINITY ? 0.f : m;
         float2 ls2 = make_float2(0.f, 0.f);
+        // P(j)'s buffer was last read by P V(j-2)
+        if (j >= 2) {
+          ok = mbar_wait(b_pvdone(j & 1), ((j >> 1) - 1) & 1);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         // P straight into TMEM (the P V MMA reads its A operand there)
 #pragma unroll
         for (int c = 0; c < kBN; c += 32) {
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
             ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
             pk[x / 2] = float2_to_bf16x2(e0, e1);
           }
-          tmem_st16(trow + Lay::kTmemP + c / 2, pk);
+          tmem_st16(trow + Lay::kTmemP + (j & 1) * 64 + c / 2, pk);
         }
         tmem_wait_st();
         l += ls2.x + ls2.y;
@@ -332,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull);
+      if (lane == 0) mbar_arrive(b_pfull(j & 1));
     }
     // epilogue: O row / l in bf16 and the LSE (no key: O = 0, LSE = -inf)
     if (ok && n_kt > 0) {
-      ok = mbar_wait(b_pvdone, (n_kt - 1) & 1);
+      ok = mbar_wait(b_pvdone((n_kt - 1) & 1), ((n_kt - 1) >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) ok = false;
       else tc_fence_after();
     }

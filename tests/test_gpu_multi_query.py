@@ -30,8 +30,8 @@ def _case(name, seed, lens, q_len, H_q=32, H_kv=8, D=128, ps=16, dtype="bf16"):
 
 
 def _run(case, q_len, ctas=None, path=None):
-    """path: None = the library's choice (tensor cores where the shape allows),
-    "cuda" = the CUDA-core split-KV kernel."""
+    """path: None = the library's choice, "tensor" = the tcgen05 kernel where the
+    shape allows it, "cuda" = the CUDA-core split-KV kernel."""
     bt = torch.from_numpy(case.block_table).to(DEV)
     lens = torch.from_numpy(case.seq_lens).to(DEV)
     if ctas is not None:
@@ -74,7 +74,7 @@ def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, dtype):
     lens[2] = 33
     case = _case(f"mq_{q_len}_{H_q}_{H_kv}_{D}_{dtype}", 61 + q_len, lens, q_len, H_q, H_kv, D, dtype=dtype)
     o_ref, l_ref = _oracle(case)
-    for ctas, path in ((None, None), (None, "cuda"), (5, "cuda")):
+    for ctas, path in ((None, "tensor"), (None, "cuda"), (5, "cuda")):
         out, lse = _run(case, q_len, ctas, path)
         compare(out, o_ref, dtype, lse, l_ref, f"q_len={q_len} {H_q}/{H_kv} D={D} {dtype} ctas={ctas} path={path}")
 
@@ -107,7 +107,7 @@ def test_full_llama_shape_with_two_draft_tokens():
     lens = rng.integers(512, 4097, size=64)
     case = _case("mq_llama", 2, lens, 2)
     o_ref, l_ref = _oracle(case)
-    for path in (None, "cuda"):
+    for path in ("tensor", "cuda"):
         out, lse = _run(case, 2, path=path)
         compare(out, o_ref, "bf16", lse, l_ref, f"llama shape q_len=2 path={path}")
 
@@ -121,6 +121,6 @@ def test_tensor_core_path_shapes(q_len, H_q, H_kv, D):
     lens = rng.integers(q_len, 3000, size=6)
     lens[0], lens[1], lens[2] = q_len, 127 + q_len, 128
     case = _case(f"mq_tc_{q_len}_{H_q}_{H_kv}_{D}", 91 + q_len, lens, q_len, H_q, H_kv, D)
-    out, lse = _run(case, q_len)
+    out, lse = _run(case, q_len, path="tensor")
     o_ref, l_ref = _oracle(case)
     compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D}")
