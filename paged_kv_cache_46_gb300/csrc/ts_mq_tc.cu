@@ -38,6 +38,9 @@ constexpr int kStages = 3;        // K and V tile buffers
 constexpr float kLog2eC = 1.4426950408889634f;
 constexpr float kLn2C = 0.6931471805599453f;
 constexpr float kSlack = 8.0f;
+// Up to this many sequences the CTAs take them longest first (each CTA ranks
+// the key-tile counts itself, B^2 / 192 comparisons per thread).
+constexpr int kLongestFirstMaxB = 128;
 
 template <int kHD>
 struct Layout {
@@ -62,7 +65,7 @@ struct MqParams {
   float* lse;                   // [B, q_len, H_q] or nullptr
   const int32_t* block_table;   // [B, bt_stride]
   const int32_t* seq_lens;      // [B], counting the q_len new tokens
-  int32_t bt_stride, q_len, H_q, H_kv, g, num_pages;
+  int32_t B, bt_stride, q_len, H_q, H_kv, g, num_pages;
   float scale_log2;
   uint32_t* err_word;
 };
@@ -74,12 +77,34 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   constexpr int kAtoms = Lay::kAtoms;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, b = blockIdx.y;
   // Programmatic dependent launch: outputs are written only after the wait.
   pdl_launch_dependents();
   if ((smem_u32(smem) & 1023u) != 0) {
     if (tid == 0) set_device_error(p.err_word, TS_DEVERR_SMEM_ALIGN);
     return;
+  }
+  const int h = static_cast<int>(blockIdx.x % p.H_kv);
+  int b = static_cast<int>(blockIdx.x / p.H_kv);
+  if (p.B <= kLongestFirstMaxB) {
+    // CTAs start roughly in index order: handing out the sequences by
+    // decreasing key-tile count (ties by index) is the longest-first rule,
+    // which keeps the last wave short when the lengths differ.
+    auto tiles = [&](int s) {
+      const int len = p.seq_lens[s];
+      return len > 0 ? (min((len + kPS - 1) / kPS, p.bt_stride) + kPagesPerTile - 1) / kPagesPerTile : 0;
+    };
+    int* pick = reinterpret_cast<int*>(smem + Lay::kOffTmem + 8);
+    for (int s = tid; s < p.B; s += kThreads) {
+      const int ws = tiles(s);
+      int rank = 0;
+      for (int t = 0; t < p.B; ++t) {
+        const int wt = tiles(t);
+        rank += (wt > ws || (wt == ws && t < s)) ? 1 : 0;
+      }
+      if (rank == b) *pick = s;
+    }
+    __syncthreads();
+    b = *pick;
   }
   const int R = p.q_len * p.g;   // real rows
   const int L = p.seq_lens[b];   // tokens in the cache, the q_len new ones included
@@ -158,15 +183,14 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       }
       return row;
     };
+    // One box (a page's rows of one 64-column atom) per lane: a single thread
+    // issuing them one after another caps the tile rate well below HBM's.
     auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int rows) {
+      const int pg = lane / kAtoms, a = lane % kAtoms;
+      const int row = __shfl_sync(0xffffffffu, rows, pg & (kPagesPerTile - 1));
       if (lane == 0) mbar_arrive_expect_tx(bar, kTileKV);
-#pragma unroll
-      for (int i = 0; i < kPagesPerTile; ++i) {
-        const int row = __shfl_sync(0xffffffffu, rows, i);
-        if (lane == 0)
-#pragma unroll
-          for (int a = 0; a < kAtoms; ++a) tma_load_3d(dst + a * kAtom + i * (kPS * 128), map, a * 64, h, row, bar);
-      }
+      __syncwarp();
+      if (pg < kPagesPerTile) tma_load_3d(dst + a * kAtom + pg * (kPS * 128), map, a * 64, h, row, bar);
     };
     int rows = n_kt > 0 ? tile_rows(0) : oob;
     for (int j = 0; j < n_kt && ok; ++j) {
@@ -260,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_sfree);
+      float ms = 0.f;
       if (warp_real) {
         const int key0 = j * kBN;
         // keys at or past this row's limit are masked (the sequence's end, the
@@ -297,17 +322,20 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
           }
           tmem_wait_st();
         }
-        const float ms = m == -INFINITY ? 0.f : m;
-        float2 ls2 = make_float2(0.f, 0.f);
-        // P(j)'s buffer was last read by P V(j-2)
-        if (j >= 2) {
-          ok = mbar_wait(b_pvdone(j & 1), ((j >> 1) - 1) & 1);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        ms = m == -INFINITY ? 0.f : m;
+      }
+      // P(j)'s buffer was last read by P V(j-2). Padding warps wait too, so
+      // that an arrival for tile j only ever counts toward tile j's phase.
+      if (j >= 2) {
+        ok = mbar_wait(b_pvdone(j & 1), ((j >> 1) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+      }
+      if (warp_real) {
+        float2 ls2 = make_float2(0.f, 0.f);
         // P straight into TMEM (the P V MMA reads its A operand there)
 #pragma unroll
         for (int c = 0; c < kBN; c += 32) {
@@ -423,7 +451,7 @@ ts_status launch(const MqParams& prm, const CUtensorMap& kmap, const CUtensorMap
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(prm.H_kv, B);
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(prm.H_kv));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Lay::kSmem;
   cfg.stream = s;
@@ -444,7 +472,7 @@ ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v
                                 ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream) {
   const int g = H_q / H_kv;
   if (dtype != TS_BF16 || page_size != kPS || (D != 64 && D != 128) || q_len < 1 || q_len * g > kBM ||
-      H_kv > 65535 || B > 65535)
+      static_cast<int64_t>(B) * H_kv > 0x7fffffff)
     return TS_ERR_UNSUPPORTED;
   MqParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -452,6 +480,7 @@ ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v
   prm.lse = lse;
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
+  prm.B = B;
   prm.bt_stride = bt_stride;
   prm.q_len = q_len;
   prm.H_q = H_q;

@@ -467,17 +467,18 @@ extern "C" ts_status ts_paged_decode_multi_attn(const void* q, const void* k_poo
                                                 ts_dtype dtype, void* out, float* lse,
                                                 void* workspace, size_t workspace_bytes,
                                                 void* stream) {
-  // More than 8 query rows per kv head (q_len x g) do not fit one pass of
-  // the CUDA-core kernel: there one CTA per (sequence, kv head) runs them on
-  // tcgen05 when the shape allows it (measured on the Llama-3-8B layer shape:
-  // 4 tokens x 4 heads 206 us against 367 us; at 8 rows the CUDA-core kernel
-  // is ahead, 190 us against 206). TS_MULTI_QUERY_PATH=cuda / =tensor forces
-  // one path (tests compare both).
+  // From 8 query rows per kv head (q_len x g) one CTA per (sequence, kv
+  // head) runs them on tcgen05 when the shape allows it; the CUDA-core kernel
+  // keeps at most 8 rows in registers per pass and is the slower of the two
+  // there (Llama-3-8B layer shape, B=64: 2 tokens x 4 heads 140 us against
+  // 190 us, 4 x 4 140 us against 367 us). Fewer rows stay on the CUDA-core
+  // kernel. TS_MULTI_QUERY_PATH=cuda / =tensor forces one path (tests
+  // compare both).
   const char* path = getenv("TS_MULTI_QUERY_PATH");
   const bool force_cuda = path && std::strcmp(path, "cuda") == 0;
   const bool force_tc = path && std::strcmp(path, "tensor") == 0;
   const int rows_per_kv = H_kv > 0 && H_q % H_kv == 0 ? q_len * (H_q / H_kv) : 0;
-  if (!force_cuda && (force_tc || rows_per_kv > 8) && q_len >= 2 && B > 0 && H_q > 0 && H_kv > 0 &&
+  if (!force_cuda && (force_tc || rows_per_kv >= 8) && q_len >= 2 && B > 0 && H_q > 0 && H_kv > 0 &&
       H_q % H_kv == 0 && q && k_pool && v_pool &&
       block_table && seq_lens && out && bt_stride > 0 && num_pages > 0 && std::isfinite(scale) &&
       reinterpret_cast<uintptr_t>(q) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&

@@ -124,3 +124,20 @@ def test_tensor_core_path_shapes(q_len, H_q, H_kv, D):
     out, lse = _run(case, q_len, path="tensor")
     o_ref, l_ref = _oracle(case)
     compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D}")
+
+
+@pytest.mark.parametrize("B", [40, 129, 300])
+def test_tensor_core_path_work_order(B):
+    """Up to 128 sequences the CTAs take them longest first, above that in index
+    order: both against the oracle, with runs of equal lengths (ties in the
+    ranking) and lengths of zero, one and a tile boundary mixed in."""
+    rng = np.random.default_rng(B)
+    lens = rng.integers(4, 700, size=B)
+    lens[: B // 4] = 257                   # a block of ties
+    lens[B // 4] = 4
+    lens[B // 4 + 1] = 128
+    rng.shuffle(lens)
+    case = _case(f"mq_tc_order_{B}", 300 + B, lens, 4)
+    out, lse = _run(case, 4, path="tensor")
+    o_ref, l_ref = _oracle(case)
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B}")
