@@ -70,7 +70,7 @@ struct MqParams {
   uint32_t* err_word;
 };
 
-template <int kHD>
+template <int kHD, int kHG>
 __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kernel(
     const MqParams p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using Lay = Layout<kHD>;
@@ -83,15 +83,20 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     if (tid == 0) set_device_error(p.err_word, TS_DEVERR_SMEM_ALIGN);
     return;
   }
-  const int h = static_cast<int>(blockIdx.x % p.H_kv);
-  int b = static_cast<int>(blockIdx.x / p.H_kv);
+  // A CTA takes HG kv heads of one sequence: head slot hs owns the lanes
+  // [hs * Rw, (hs + 1) * Rw) of every tile, and a key tile holds TP pages of
+  // all HG heads, so that one TMA box brings a page's rows of HG heads.
+  constexpr int HG = kHG, TP = kPagesPerTile / HG, Rw = kBM / HG, kKeys = TP * kPS;
+  const int hgroups = p.H_kv / HG;
+  const int h0 = static_cast<int>(blockIdx.x % hgroups) * HG;  // first kv head
+  int b = static_cast<int>(blockIdx.x / hgroups);
   if (p.B <= kLongestFirstMaxB) {
     // CTAs start roughly in index order: handing out the sequences by
-    // decreasing key-tile count (ties by index) is the longest-first rule,
-    // which keeps the last wave short when the lengths differ.
+    // decreasing page count (ties by index) is the longest-first rule, which
+    // keeps the last wave short when the lengths differ.
     auto tiles = [&](int s) {
       const int len = p.seq_lens[s];
-      return len > 0 ? (min((len + kPS - 1) / kPS, p.bt_stride) + kPagesPerTile - 1) / kPagesPerTile : 0;
+      return len > 0 ? min((len + kPS - 1) / kPS, p.bt_stride) : 0;
     };
     int* pick = reinterpret_cast<int*>(smem + Lay::kOffTmem + 8);
     for (int s = tid; s < p.B; s += kThreads) {
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   const int R = p.q_len * p.g;   // real rows
   const int L = p.seq_lens[b];   // tokens in the cache, the q_len new ones included
   const int n_pages = L > 0 ? min((L + kPS - 1) / kPS, p.bt_stride) : 0;
-  const int n_kt = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
+  const int n_kt = (n_pages + TP - 1) / TP;
   // Before this wait only the lengths are read (the queries, the pools with
   // freshly appended rows and the outputs may belong to the previous kernel).
   pdl_wait_primary();
@@ -145,18 +150,20 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     }
     fence_mbar_init();
   }
-  // Q tile: row r = (token r / g, head h*g + r % g); rows past R are zero.
+  // Q tile: lane hs * Rw + r holds row r of head slot hs, (token r / g,
+  // query head (h0 + hs) * g + r % g); rows past R are zero.
   if (warp < 4) {
-    const int r = tid;
+    const int hs = tid / Rw, r = tid % Rw;
     const bool real = r < R;
     const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + ((static_cast<int64_t>(b) * p.q_len + (real ? r / p.g : 0)) * p.H_q + h * p.g + r % p.g) * kHD);
+        p.q + ((static_cast<int64_t>(b) * p.q_len + (real ? r / p.g : 0)) * p.H_q + (h0 + hs) * p.g + r % p.g) *
+                  kHD);
 #pragma unroll
     for (int a = 0; a < kAtoms; ++a) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint4 v = real ? src[a * 8 + c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(smem + Lay::kOffQ + a * kAtom + sw128_off(r, c)) = v;
+        *reinterpret_cast<uint4*>(smem + Lay::kOffQ + a * kAtom + sw128_off(tid, c)) = v;
       }
     }
     fence_async_smem();
@@ -172,9 +179,9 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     // ---------------- TMA producer (lane 0 issues; lane i < 8 holds page i) ----
     const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
     auto tile_rows = [&](int j) {       // this lane's page of key tile j, as a pool row
-      const int pi = j * kPagesPerTile + lane;
+      const int pi = j * TP + lane;
       int row = oob;
-      if (lane < kPagesPerTile && pi < n_pages) {
+      if (lane < TP && pi < n_pages) {
         const int page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + pi];
         if (page >= 0 && page < p.num_pages)
           row = page * kPS;
@@ -183,14 +190,16 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       }
       return row;
     };
-    // One box (a page's rows of one 64-column atom) per lane: a single thread
-    // issuing them one after another caps the tile rate well below HBM's.
+    // One box per lane: a page's 16 rows of the CTA's HG heads in one
+    // 64-column atom, landing as [head][16 keys] blocks of 128-byte rows. A
+    // single thread issuing the boxes one after another, or boxes of one
+    // head, cap the tile rate well below HBM's.
     auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int rows) {
       const int pg = lane / kAtoms, a = lane % kAtoms;
       const int row = __shfl_sync(0xffffffffu, rows, pg & (kPagesPerTile - 1));
       if (lane == 0) mbar_arrive_expect_tx(bar, kTileKV);
       __syncwarp();
-      if (pg < kPagesPerTile) tma_load_3d(dst + a * kAtom + pg * (kPS * 128), map, a * 64, h, row, bar);
+      if (pg < TP) tma_load_3d(dst + a * kAtom + pg * (HG * kPS * 128), map, a * 64, row, h0, bar);
     };
     int rows = n_kt > 0 ? tile_rows(0) : oob;
     for (int j = 0; j < n_kt && ok; ++j) {
@@ -256,13 +265,30 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   } else {
     // ---------------- softmax warps: thread = query row ----------------
     // A warp whose 32 rows are all padding only keeps the barrier protocol:
-    // its rows' S, P and O lanes are never read into an output.
-    const int r = tid;
-    const bool warp_real = warp * 32 < R;
+    // its rows' S, P and O lanes are never read into an output. Row r of
+    // head slot hs scores the tile's keys of its own head only: columns
+    // [pb * HG * 16 + hs * 16, +16) for page block pb < TP; P is zero in the
+    // other heads' columns, so the block-diagonal P V adds its head's V alone.
+    const int hs = tid / Rw, r = tid % Rw;
+    const bool warp_real = (warp * 32) % Rw < R;
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int jt = r / p.g;                        // this row's token
-    const int lim = L - p.q_len + 1 + jt;          // keys it may attend
-    float m = -INFINITY, l = 0.f;
+    const uint32_t hcol = static_cast<uint32_t>(hs * kPS);
+    const int jt = r / p.g;                            // this row's token
+    const int lim = r < R ? L - p.q_len + 1 + jt : 0;  // keys it may attend (padding: none)
+    // l: the row sum of exp2(s - m) for the LSE; lr: the same over P as
+    // rounded to bf16 for the product, which normalises O, so that the
+    // weights the product applied sum to one
+    float m = -INFINITY, l = 0.f, lr = 0.f;
+    if constexpr (HG > 1) {
+      if (warp_real) {
+      uint32_t z[16];
+#pragma unroll
+      for (int x = 0; x < 16; ++x) z[x] = 0u;
+#pragma unroll
+        for (int c = 0; c < 128; c += 16) tmem_st16(trow + Lay::kTmemP + c, z);  // both P buffers
+        tmem_wait_st();
+      }
+    }
     for (int j = 0; j < n_kt && ok; ++j) {
       ok = mbar_wait(b_sfull, j & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -270,15 +296,15 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         break;
       }
       tc_fence_after();
-      float s[kBN];
+      float s[kKeys];  // key c of the tile (page block c / 16) in s[c]
       if (warp_real) {
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 16) {
+        for (int pb = 0; pb < TP; ++pb) {
           uint32_t u[16];
-          tmem_ld16(trow + c0, u);
+          tmem_ld16(trow + pb * HG * kPS + hcol, u);
           tmem_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 16; ++x) s[c0 + x] = __uint_as_float(u[x]);
+          for (int x = 0; x < 16; ++x) s[pb * 16 + x] = __uint_as_float(u[x]);
         }
       }
       tc_fence_before();
@@ -286,13 +312,13 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       if (lane == 0) mbar_arrive(b_sfree);
       float ms = 0.f;
       if (warp_real) {
-        const int key0 = j * kBN;
+        const int key0 = j * kKeys;
         // keys at or past this row's limit are masked (the sequence's end, the
         // causal limit of its token); the scale is folded into the exponent
         const float sl = p.scale_log2;
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < kKeys; ++c) {
           s[c] = key0 + c < lim ? s[c] * sl : -INFINITY;
           mx = fmaxf(mx, s[c]);
         }
@@ -311,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
           const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
           m = mnew;
           l *= alpha;
+          lr *= alpha;
 #pragma unroll
           for (int c0 = 0; c0 < kHD; c0 += 16) {
             uint32_t u[16];
@@ -335,39 +362,41 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         tc_fence_after();
       }
       if (warp_real) {
-        float2 ls2 = make_float2(0.f, 0.f);
+        float2 ls2 = make_float2(0.f, 0.f), lr2 = make_float2(0.f, 0.f);
         // P straight into TMEM (the P V MMA reads its A operand there)
 #pragma unroll
-        for (int c = 0; c < kBN; c += 32) {
-          uint32_t pk[16];
+        for (int pb = 0; pb < TP; ++pb) {
+          uint32_t pk[8];
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            const float e0 = fast_exp2(s[c + x] - ms);
-            const float e1 = fast_exp2(s[c + x + 1] - ms);
-            ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+          for (int x = 0; x < 16; x += 2) {
+            const float e0 = fast_exp2(s[pb * 16 + x] - ms);
+            const float e1 = fast_exp2(s[pb * 16 + x + 1] - ms);
             pk[x / 2] = float2_to_bf16x2(e0, e1);
+            ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+            lr2 = __fadd2_rn(lr2, bf16x2_to_float2(pk[x / 2]));
           }
-          tmem_st16(trow + Lay::kTmemP + (j & 1) * 64 + c / 2, pk);
+          tmem_st8(trow + Lay::kTmemP + (j & 1) * 64 + (pb * HG * kPS + hcol) / 2, pk);
         }
         tmem_wait_st();
         l += ls2.x + ls2.y;
+        lr += lr2.x + lr2.y;
       }
       // The last tile's V rows past the sequence may hold anything (NaN
       // included) and 0 * NaN is NaN in the product: zero them once landed.
-      const int vrow0 = L - j * kBN;
-      if (j == n_kt - 1 && vrow0 < kBN) {
+      if (j == n_kt - 1 && (j + 1) * kKeys > L) {
         const int buf = j % kStages;
         ok = mbar_wait(b_vfull(buf), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        if (r >= vrow0) {
+        // tile row t holds key (t / (HG * 16)) * 16 + t % 16 of its head
+        if (j * kKeys + (tid / (HG * kPS)) * kPS + tid % kPS >= L) {
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(smem + Lay::kOffV + buf * kTileKV + a * kAtom + r * 128 + c * 16) =
+              *reinterpret_cast<uint4*>(smem + Lay::kOffV + buf * kTileKV + a * kAtom + tid * 128 + c * 16) =
                   make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
@@ -384,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     }
     if (ok && warp_real) {
       const bool real = r < R;
-      const int64_t row = (static_cast<int64_t>(b) * p.q_len + jt) * p.H_q + h * p.g + r % p.g;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const int64_t row = (static_cast<int64_t>(b) * p.q_len + jt) * p.H_q + (h0 + hs) * p.g + r % p.g;
+      const float inv = lr > 0.f ? 1.0f / lr : 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < kHD; c0 += 16) {
         uint32_t u[16];
@@ -418,15 +447,16 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   }
 }
 
-// 3-D map over a pool [P * 16 rows][H_kv][D] bf16 with a box of one page of
-// one kv head and 64 columns (16 rows x 128 B), 128-byte swizzle, zero fill.
-ts_status make_map(CUtensorMap* map, const void* pool, int num_pages, int H_kv, int D) {
+// 3-D map over a pool [P * 16 rows][H_kv][D] bf16 taken as (column, pool
+// row, kv head): a box is one page (16 rows) of hg heads in one 64-column
+// atom and lands head by head, [hg][16][64]; 128-byte swizzle, zero fill.
+ts_status make_map(CUtensorMap* map, const void* pool, int num_pages, int H_kv, int D, int hg) {
   auto fn = tensor_map_encoder();
   if (!fn) return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
-                        static_cast<cuuint64_t>(num_pages) * kPS};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H_kv) * D * 2};
-  cuuint32_t box[3] = {64, 1, kPS};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_pages) * kPS,
+                        static_cast<cuuint64_t>(H_kv)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(H_kv) * D * 2, static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, kPS, static_cast<cuuint32_t>(hg)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -435,10 +465,10 @@ ts_status make_map(CUtensorMap* map, const void* pool, int num_pages, int H_kv, 
   return TS_OK;
 }
 
-template <int kHD>
+template <int kHD, int kHG>
 ts_status launch(const MqParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap, int B, cudaStream_t s) {
   using Lay = Layout<kHD>;
-  ts_status st = prepare_once(reinterpret_cast<const void*>(mq_tc_kernel<kHD>), [](const void* k) {
+  ts_status st = prepare_once(reinterpret_cast<const void*>(mq_tc_kernel<kHD, kHG>), [](const void* k) {
     ts_status s2 = cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kHD>::kSmem),
                               "multi-query tensor-core smem attribute");
     if (s2 != TS_OK) return s2;
@@ -451,14 +481,15 @@ ts_status launch(const MqParams& prm, const CUtensorMap& kmap, const CUtensorMap
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(prm.H_kv));
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(prm.H_kv / kHG));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Lay::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   LaunchTrace trace("mq_tc_kernel", s);
-  return cuda_check(cudaLaunchKernelEx(&cfg, mq_tc_kernel<kHD>, prm, kmap, vmap), "multi-query tensor-core launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, mq_tc_kernel<kHD, kHG>, prm, kmap, vmap),
+                    "multi-query tensor-core launch");
 }
 
 }  // namespace
@@ -489,12 +520,32 @@ ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v
   prm.num_pages = num_pages;
   prm.scale_log2 = scale * kLog2eC;
   prm.err_word = err_word;
+  // Heads per CTA: more heads make fewer, larger TMA boxes, fewer heads more
+  // CTAs. Take the most that the rows allow (hg * R <= 128 with R padded to a
+  // warp's 32 lanes) while the grid still covers 1.5 waves of SMs, else one.
+  // TS_MULTI_QUERY_HEAD_GROUP=1/2/4 forces a value the shape allows (tests).
+  const int R = q_len * g;
+  const int hg_max = R <= 32 ? 4 : (R <= 64 ? 2 : 1);
+  int hg = 1;
+  for (int c = hg_max; c > 1; c >>= 1)
+    if (H_kv % c == 0 && static_cast<int64_t>(B) * (H_kv / c) * 2 >= 3 * static_cast<int64_t>(device_sm_count())) {
+      hg = c;
+      break;
+    }
+  if (const char* e = getenv("TS_MULTI_QUERY_HEAD_GROUP")) {
+    const int f = atoi(e);
+    if ((f == 1 || f == 2 || f == 4) && f <= hg_max && H_kv % f == 0) hg = f;
+  }
   CUtensorMap kmap, vmap;
-  ts_status st = make_map(&kmap, k_pool, num_pages, H_kv, D);
+  ts_status st = make_map(&kmap, k_pool, num_pages, H_kv, D, hg);
   if (st != TS_OK) return st;
-  st = make_map(&vmap, v_pool, num_pages, H_kv, D);
+  st = make_map(&vmap, v_pool, num_pages, H_kv, D, hg);
   if (st != TS_OK) return st;
-  return D == 64 ? launch<64>(prm, kmap, vmap, B, stream) : launch<128>(prm, kmap, vmap, B, stream);
+  if (D == 64)
+    return hg == 4 ? launch<64, 4>(prm, kmap, vmap, B, stream)
+                   : hg == 2 ? launch<64, 2>(prm, kmap, vmap, B, stream) : launch<64, 1>(prm, kmap, vmap, B, stream);
+  return hg == 4 ? launch<128, 4>(prm, kmap, vmap, B, stream)
+                 : hg == 2 ? launch<128, 2>(prm, kmap, vmap, B, stream) : launch<128, 1>(prm, kmap, vmap, B, stream);
 }
 
 }  // namespace ts

@@ -29,15 +29,18 @@ def _case(name, seed, lens, q_len, H_q=32, H_kv=8, D=128, ps=16, dtype="bf16"):
                                 seq_lens=lens, dtype=dtype, scale=D ** -0.5, device=DEV, q_len=q_len)
 
 
-def _run(case, q_len, ctas=None, path=None):
+def _run(case, q_len, ctas=None, path=None, hg=None):
     """path: None = the library's choice, "tensor" = the tcgen05 kernel where the
-    shape allows it, "cuda" = the CUDA-core split-KV kernel."""
+    shape allows it, "cuda" = the CUDA-core split-KV kernel; hg: kv heads per
+    CTA of the tcgen05 kernel (None = the library's choice)."""
     bt = torch.from_numpy(case.block_table).to(DEV)
     lens = torch.from_numpy(case.seq_lens).to(DEV)
     if ctas is not None:
         os.environ["TS_PAGED_DECODE_CTAS"] = str(ctas)
     if path is not None:
         os.environ["TS_MULTI_QUERY_PATH"] = path
+    if hg is not None:
+        os.environ["TS_MULTI_QUERY_HEAD_GROUP"] = str(hg)
     try:
         ws = ts.new_workspace(ts.ts_paged_decode_multi_workspace_size(case.B, q_len, case.H_q, case.D))
         out, lse = ts.ts_paged_decode_multi_attn(case.q, case.k_pool, case.v_pool, bt, lens, case.scale,
@@ -47,6 +50,7 @@ def _run(case, q_len, ctas=None, path=None):
     finally:
         os.environ.pop("TS_PAGED_DECODE_CTAS", None)
         os.environ.pop("TS_MULTI_QUERY_PATH", None)
+        os.environ.pop("TS_MULTI_QUERY_HEAD_GROUP", None)
     return out, lse
 
 
@@ -112,22 +116,26 @@ def test_full_llama_shape_with_two_draft_tokens():
         compare(out, o_ref, "bf16", lse, l_ref, f"llama shape q_len=2 path={path}")
 
 
-@pytest.mark.parametrize("q_len,H_q,H_kv,D", [(4, 32, 8, 128), (8, 64, 8, 128), (16, 32, 4, 64), (3, 8, 1, 64)])
-def test_tensor_core_path_shapes(q_len, H_q, H_kv, D):
-    """Rows q_len * g from 24 to 128 on the tensor-core path (one CTA per
-    sequence and kv head), including sequences shorter than a key tile, a
-    context of only the new tokens, and one past a tile boundary."""
+@pytest.mark.parametrize("q_len,H_q,H_kv,D,hg", [
+    (4, 32, 8, 128, 1), (4, 32, 8, 128, 2), (4, 32, 8, 128, 4),   # 16 rows: 1, 2 or 4 kv heads per CTA
+    (2, 32, 8, 64, 4), (8, 64, 8, 128, 1), (8, 64, 8, 128, 2),    # 8 and 64 rows
+    (16, 32, 4, 64, 1), (3, 8, 1, 64, 1)])                         # 128 rows; one kv head
+def test_tensor_core_path_shapes(q_len, H_q, H_kv, D, hg):
+    """Rows q_len * g from 8 to 128 on the tensor-core path, with 1, 2 or 4 kv
+    heads per CTA, including sequences shorter than a key tile, a context of
+    only the new tokens, and one past a tile boundary."""
     rng = np.random.default_rng(q_len * 7 + D)
     lens = rng.integers(q_len, 3000, size=6)
     lens[0], lens[1], lens[2] = q_len, 127 + q_len, 128
+    lens[3] = 16 * (8 // hg) + 1        # one key past a tile of 8 / hg pages
     case = _case(f"mq_tc_{q_len}_{H_q}_{H_kv}_{D}", 91 + q_len, lens, q_len, H_q, H_kv, D)
-    out, lse = _run(case, q_len, path="tensor")
+    out, lse = _run(case, q_len, path="tensor", hg=hg)
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D}")
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D} hg={hg}")
 
 
-@pytest.mark.parametrize("B", [40, 129, 300])
-def test_tensor_core_path_work_order(B):
+@pytest.mark.parametrize("B,hg", [(40, 1), (40, 4), (129, 2), (300, 2)])
+def test_tensor_core_path_work_order(B, hg):
     """Up to 128 sequences the CTAs take them longest first, above that in index
     order: both against the oracle, with runs of equal lengths (ties in the
     ranking) and lengths of zero, one and a tile boundary mixed in."""
@@ -138,6 +146,6 @@ def test_tensor_core_path_work_order(B):
     lens[B // 4 + 1] = 128
     rng.shuffle(lens)
     case = _case(f"mq_tc_order_{B}", 300 + B, lens, 4)
-    out, lse = _run(case, 4, path="tensor")
+    out, lse = _run(case, 4, path="tensor", hg=hg)
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B}")
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B} hg={hg}")
