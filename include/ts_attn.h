@@ -204,9 +204,16 @@ TS_API size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int
  * position seq_lens[b] - q_len + j and attends tokens 0 .. that position
  * (causal among the new tokens); each (token, head) row is otherwise the
  * single-query decode of ts_paged_decode_attn. Tokens are folded into the
- * kernel's per-kv-head rows (TokenSpeed deep dive, section 7.2): F of them
- * with the g heads of a kv head when g * F is 1, 2, 4 or 8 (the largest such
- * factor F of q_len); the others run as separate passes over the pages.
+ * rows of a kv head (TokenSpeed deep dive, section 7.2). With R = q_len * g
+ * rows per kv head from 8 to 128 (bf16, page 16, D 64 or 128) a tensor-core
+ * kernel takes all R rows in one pass: S = Q K^T and P V on tcgen05, one CTA
+ * per sequence and group of 1, 2 or 4 kv heads, P rounded to bf16 for the
+ * product (O normalised by the sum of the rounded P; the LSE from the
+ * unrounded sum). Otherwise the CUDA-core kernel folds F tokens with the g
+ * heads of a kv head when g * F is 1, 2, 4 or 8 (the largest such factor F of
+ * q_len) and runs the others as separate passes over the pages. The
+ * environment variable TS_MULTI_QUERY_PATH=cuda|tensor forces one path where
+ * the shape allows it.
  *
  *   q             device [B, q_len, H_q, D] of dtype
  *   out           device [B, q_len, H_q, D] of dtype (written)
