@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
   bool ok = true;
 
   if (warp == 4) {
-    // ---------------- TMA producer (lane 0 issues; lane i < 8 holds page i) ----
+    // ---------------- TMA producer (lane i < 8 holds and loads page i) ----
     const int oob = p.num_pages * kPS;  // a row coordinate past the pool: zero fill
     auto tile_rows = [&](int j) {       // this lane's page of key tile j, as a pool row
       const int pi = j * kPagesPerTile + lane;
@@ -212,13 +212,12 @@ __global__ void __launch_bounds__(kThreadsPfx, 2) cascade_prefix_kernel(
       }
       return row;
     };
+    // One box per lane: a single thread issuing a tile's boxes one after
+    // another caps the tile rate (measured on the multi-query kernel).
     auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int rows) {
       if (lane == 0) mbar_arrive_expect_tx(bar, kBN * kHD * 2);
-#pragma unroll
-      for (int i = 0; i < kPagesPerTile; ++i) {
-        const int row = __shfl_sync(0xffffffffu, rows, i);
-        if (lane == 0) tma_load_3d(dst + i * (kPS * 128), map, 0, h, row, bar);
-      }
+      __syncwarp();
+      if (lane < kPagesPerTile) tma_load_3d(dst + lane * (kPS * 128), map, 0, h, rows, bar);
     };
     int rows = n_kt > 0 ? tile_rows(0) : oob;
     for (int j = 0; j < n_kt && ok; ++j) {
