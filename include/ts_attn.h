@@ -19,6 +19,9 @@
  *     is split into fixed-size blocks found through a per-request block
  *     table; section 5.1: attention takes the query, block tables and
  *     context lengths.)
+ *     Pools may be any size the device holds (byte offsets are 64-bit), but
+ *     their row count num_pages * page_size must stay below 2^31 (rows are
+ *     32-bit TMA coordinates); a larger num_pages is an argument error.
  *   - GQA: query head h reads kv head h / (H_q / H_kv).
  *   - LSE outputs are natural-log log-sum-exp of the scaled scores, float32.
  *     A sequence of length 0 yields O = 0 and LSE = -inf.

@@ -567,8 +567,9 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
   const char* who = "ts_cascade_decode_attn";
   if (!groups) return fail(TS_ERR_INVALID_ARG, "%s: null groups", who);
   if (B == 0) return TS_OK;
-  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0)
-    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d)", who, B, H_q, H_kv);
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || num_pages <= 0 ||
+      static_cast<long long>(num_pages) * page_size > INT32_MAX)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d P=%d)", who, B, H_q, H_kv, num_pages);
   const int g = H_q / H_kv;
   if (dtype != TS_BF16 || D != kHD || page_size != kPS || (g != 1 && g != 2 && g != 4 && g != 8))
     return fail(TS_ERR_UNSUPPORTED, "%s: needs bf16, D=64, page_size=16, H_q/H_kv in {1,2,4,8}", who);
@@ -626,8 +627,9 @@ extern "C" ts_status ts_cascade_nested_decode_attn(const void* q, const void* k_
   const char* who = "ts_cascade_nested_decode_attn";
   if (!forest) return fail(TS_ERR_INVALID_ARG, "%s: null forest", who);
   if (B == 0) return TS_OK;
-  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0)
-    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d)", who, B, H_q, H_kv);
+  if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || num_pages <= 0 ||
+      static_cast<long long>(num_pages) * page_size > INT32_MAX)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d P=%d)", who, B, H_q, H_kv, num_pages);
   const int g = H_q / H_kv;
   if (dtype != TS_BF16 || D != kHD || page_size != kPS || (g != 1 && g != 2 && g != 4 && g != 8))
     return fail(TS_ERR_UNSUPPORTED, "%s: needs bf16, D=64, page_size=16, H_q/H_kv in {1,2,4,8}", who);

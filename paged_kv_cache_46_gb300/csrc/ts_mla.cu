@@ -670,7 +670,7 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
                                          void* workspace, size_t workspace_bytes, void* stream) {
   using namespace ts;
   const char* who = "ts_mla_paged_decode";
-  if (B < 0 || num_pages <= 0 || bt_stride <= 0)
+  if (B < 0 || num_pages <= 0 || bt_stride <= 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d P=%d bt=%d)", who, B, num_pages, bt_stride);
   if (H != kH || D_qk != kDqk || D_v != kDv || page_size != kPS)
     return fail(TS_ERR_UNSUPPORTED, "%s: needs H=128, D_qk=576, D_v=512, page_size=64 (got %d, %d, %d, %d)",

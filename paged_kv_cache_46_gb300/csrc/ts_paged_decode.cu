@@ -196,7 +196,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
                             cudaStream_t stream, const char* who, const PrefixInputs* pre,
                             const Fp8Scales* f8 = nullptr) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
-      bt_stride <= 0)
+      bt_stride <= 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
                 who, B, H_q, H_kv, D, page_size, num_pages, bt_stride);
   if (q_len < 1 || (pre != nullptr && q_len != 1) ||
@@ -480,7 +480,8 @@ extern "C" ts_status ts_paged_decode_multi_attn(const void* q, const void* k_poo
   const int rows_per_kv = H_kv > 0 && H_q % H_kv == 0 ? q_len * (H_q / H_kv) : 0;
   if (!force_cuda && (force_tc || rows_per_kv >= 8) && q_len >= 2 && B > 0 && H_q > 0 && H_kv > 0 &&
       H_q % H_kv == 0 && q && k_pool && v_pool &&
-      block_table && seq_lens && out && bt_stride > 0 && num_pages > 0 && std::isfinite(scale) &&
+      block_table && seq_lens && out && bt_stride > 0 && num_pages > 0 &&
+      static_cast<long long>(num_pages) * page_size <= INT32_MAX && std::isfinite(scale) &&
       reinterpret_cast<uintptr_t>(q) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
       reinterpret_cast<uintptr_t>(k_pool) % 16 == 0 && reinterpret_cast<uintptr_t>(v_pool) % 16 == 0) {
     const size_t need = ts::paged_decode_multi_workspace_bytes(B, q_len, H_q, D);

@@ -72,6 +72,24 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.ts_merge_states(unaligned, vp, vp, vp, vp, vp, 3, 64, 1, None) == ts.TS_ERR_INVALID_ARG
 
 
+def test_pool_rows_beyond_int32_are_rejected_before_any_launch(lib):
+    """Pools may exceed 4 GiB (64-bit byte offsets), but num_pages * page_size
+    rows must stay below 2^31 (32-bit TMA row coordinates): every attention
+    entry point rejects more as an argument error, the tensor-core
+    multi-query shape included, without touching the device."""
+    vp = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    P = (1 << 27)  # x 16 rows = 2^31
+    assert lib.ts_paged_decode_attn(vp, vp, vp, vp, 4, vp, 2, 32, 8, 128, 16, P, 1.0, 1, vp, None, vp,
+                                    1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_paged_decode_multi_attn(vp, vp, vp, vp, 4, vp, 2, 4, 32, 8, 128, 16, P, 1.0, 1, vp, None,
+                                          vp, 1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    groups = ts.PrefixGroupsC()  # zeroed: never read, the size check comes first
+    assert lib.ts_cascade_decode_attn(vp, vp, vp, ctypes.byref(groups), vp, 4, vp, 2, 32, 8, 64, 16, P, 1.0, 1,
+                                      vp, None, vp, 1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_mla_paged_decode(vp, vp, vp, 4, vp, 2, 128, 576, 512, 64, (1 << 25), 1.0, vp, None, vp,
+                                   1 << 20, None) == ts.TS_ERR_INVALID_ARG
+
+
 def test_python_binding_requires_int32_metadata():
     import torch
     q = torch.zeros(1, 8, 64)
