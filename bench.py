@@ -414,30 +414,31 @@ class DeviceStep:
             ws_bytes = ts.ts_paged_decode_workspace_size(c.B, c.H_q, c.D)
         self.ws = ts.new_workspace(ws_bytes, dev)
 
-    def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None):
+    def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None, out=None):
         ts, c = self.ts, self.case
         kp, vp = self.pools[i % len(self.pools)]
+        out = self.out if out is None else out
         q = c.q if q is None else q
         bt = self.bt if bt is None else bt
         lens = self.lens if lens is None else lens
         if self.forest is not None:
-            ts.ts_cascade_nested_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=self.out,
+            ts.ts_cascade_nested_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=out,
                                              lse=self.lse, workspace=self.ws, stream=stream)
         elif self.groups is not None:
-            ts.ts_cascade_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=self.out, lse=self.lse,
+            ts.ts_cascade_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=out, lse=self.lse,
                                       workspace=self.ws, stream=stream)
         elif c.mla:
-            ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=self.out, lse=self.lse,
+            ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=out, lse=self.lse,
                                    workspace=self.ws, stream=stream)
         elif c.q_len > 1:
-            ts.ts_paged_decode_multi_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse,
+            ts.ts_paged_decode_multi_attn(q, kp, vp, bt, lens, c.scale, out=out, lse=self.lse,
                                           workspace=self.ws, stream=stream)
         elif c.kv_fp8:
             ks, vs = self.scales[i % len(self.scales)]
-            ts.ts_paged_decode_fp8_attn(q, kp, vp, ks, vs, bt, lens, c.scale, out=self.out, lse=self.lse,
+            ts.ts_paged_decode_fp8_attn(q, kp, vp, ks, vs, bt, lens, c.scale, out=out, lse=self.lse,
                                         workspace=self.ws, stream=stream)
         else:
-            ts.ts_paged_decode_attn(q, kp, vp, bt, lens, c.scale, out=self.out, lse=self.lse, workspace=self.ws,
+            ts.ts_paged_decode_attn(q, kp, vp, bt, lens, c.scale, out=out, lse=self.lse, workspace=self.ws,
                                     stream=stream)
 
     def step(self, i, ev=None, stream=None, inputs=None):
@@ -454,7 +455,7 @@ class DeviceStep:
         if ev is not None:
             ev[0].record(stream)
         self.attention(i, q=inputs.get("q"), bt=inputs.get("bt"), lens=inputs.get("lens"), stream=stream,
-                       gdev=inputs.get("gdev"))
+                       gdev=inputs.get("gdev"), out=inputs.get("out"))
         if ev is not None:
             ev[1].record(stream)
 
@@ -544,20 +545,26 @@ def run_ours(args):
             offs[k] = total
             total += (v.numel() * v.element_size() + 255) // 256 * 256
         h_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
-        d_pack = torch.empty(total, dtype=torch.uint8, device=dev)
-        din = {}
         for k, v in hin.items():
             nb = v.numel() * v.element_size()
             h_pack[offs[k]:offs[k] + nb].copy_(v.reshape(-1).view(torch.uint8))
-            din[k] = d_pack[offs[k]:offs[k] + nb].view(v.dtype).view(v.shape)
-        h_out = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+        # two device copies of the inputs and of the output: step i+1's inputs
+        # go up, and step i-1's output comes back, while step i computes
+        d_packs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+        def views(dp):
+            return {k: dp[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                    for k, v in hin.items()}
+        dins = [views(dp) for dp in d_packs]
+        d_outs = [runner.out, torch.empty_like(runner.out)]
+        h_outs = [torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hin.values())
-        d2h = h_out.numel() * h_out.element_size()
+        d2h = h_outs[0].numel() * h_outs[0].element_size()
         host_group_ms = []
 
         def e2e_step(i, st):
-            d_pack.copy_(h_pack, non_blocking=True)
-            inputs = dict(din)
+            d_packs[0].copy_(h_pack, non_blocking=True)
+            inputs = dict(dins[0])
             if runner.forest is not None:
                 t = time.perf_counter()
                 f = ts.ts_group_prefixes_nested(case.block_table, case.seq_lens, case.page_size, 2)
@@ -570,23 +577,54 @@ def run_ours(args):
                 host_group_ms.append((time.perf_counter() - t) * 1e3)
                 inputs["gdev"] = ts.groups_to_device(g, dev)
             runner.step(i, stream=st, inputs=inputs)
-            h_out.copy_(runner.out, non_blocking=True)
+            h_outs[0].copy_(runner.out, non_blocking=True)
+
+        UNROLL = 8
+        cp = torch.cuda.Stream(device=dev)
+        ev_h2d, ev_comp, ev_d2h = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+        def pipelined_steps(st):
+            """UNROLL decode steps, each with its own input upload and output
+            read-back, on two streams: uploads and read-backs run on `cp`
+            beside the previous / next step's kernels (double-buffered)."""
+            cp.wait_stream(st)
+            with torch.cuda.stream(cp):
+                d_packs[0].copy_(h_pack, non_blocking=True)
+            ev_h2d[0].record(cp)
+            for k in range(UNROLL):
+                b = k & 1
+                if k + 1 < UNROLL:
+                    if k >= 1:
+                        cp.wait_event(ev_comp[b ^ 1])  # step k-1 has read its inputs
+                    with torch.cuda.stream(cp):
+                        d_packs[b ^ 1].copy_(h_pack, non_blocking=True)
+                    ev_h2d[b ^ 1].record(cp)
+                st.wait_event(ev_h2d[b])
+                if k >= 2:
+                    st.wait_event(ev_d2h[b])  # step k-2's output is back on the host
+                runner.step(k, stream=st, inputs=dict(dins[b], out=d_outs[b]))
+                ev_comp[b].record(st)
+                cp.wait_event(ev_comp[b])
+                with torch.cuda.stream(cp):
+                    h_outs[b].copy_(d_outs[b], non_blocking=True)
+                ev_d2h[b].record(cp)
+            st.wait_stream(cp)
 
         regroups = runner.groups is not None or runner.forest is not None
-        n_e2e = min(args.steps, 50) if regroups else args.steps
+        n_e2e = min(args.steps, 50) if regroups else (args.steps + UNROLL - 1) // UNROLL * UNROLL
         for i in range(min(args.warmup, 3)):
             e2e_step(i, stream)
         torch.cuda.synchronize()
-        # A serving loop replays its decode step from a CUDA graph: capture the
-        # step (input upload, library calls, result download) once, replay it
-        # every step. Cascade regroups on the host every step and stays eager.
+        # A serving loop replays its decode steps from a CUDA graph: capture
+        # UNROLL pipelined steps (uploads, library calls, read-backs) once and
+        # replay them. Cascade regroups on the host every step and stays eager.
         graph = None
         if not regroups:
             cap = torch.cuda.Stream(device=dev)
             cap.wait_stream(stream)
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=cap):
-                e2e_step(0, cap)
+                pipelined_steps(cap)
             stream.wait_stream(cap)
             for _ in range(2):
                 graph.replay()
@@ -595,10 +633,11 @@ def run_ours(args):
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         s2.record(stream)
-        for i in range(n_e2e):
-            if graph is not None:
+        if graph is not None:
+            for _ in range(n_e2e // UNROLL):
                 graph.replay()
-            else:
+        else:
+            for i in range(n_e2e):
                 e2e_step(i, stream)
         e2.record(stream)
         torch.cuda.synchronize()
@@ -607,7 +646,8 @@ def run_ours(args):
         e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
                "query_tokens_per_s": world * case.B * case.q_len / (e2e_ms * 1e-3),
-               "cuda_graph": graph is not None}
+               "cuda_graph": graph is not None,
+               "copies_overlap_compute": graph is not None}
         if host_group_ms:
             e2e["host_grouping_ms"] = statistics.median(host_group_ms)
 
