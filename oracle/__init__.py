@@ -16,6 +16,9 @@ Each function restates the operation from the pages it cites:
   section 7.1: split-KV partial outputs carry a log-sum-exp and are reduced by it.
 * tokenspeed 딥다이브 (fiv.co.kr), section 6-4: fp8 token-group quantization
   (scale = group max / fp8 max, clamp, cast; reconstruction = code * scale).
+* TokenSpeed deep dive (wth2jhl.online), section 4.1, and tokenspeed 딥다이브
+  (fiv.co.kr), section 6-3: sliding-window KV groups (the last
+  ``sliding_window_tokens`` tokens, placeholders in front of the window).
 * Tokasaurus blog (Stanford), "Dynamic prefix identification and exploration":
   shared-prefix (Hydragen / cascade) attention over greedily found shared prefixes.
 
@@ -26,6 +29,7 @@ docstring names the pins that tie it to something other than itself.
 from .attention import (
     gather_sequence,
     decode_attention,
+    decode_attention_window,
     fold_sq_factor,
     multi_query_decode_attention,
     mla_decode_attention,

@@ -103,6 +103,56 @@ def decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale):
     return out, lse
 
 
+def decode_attention_window(q, k_pool, v_pool, block_table, seq_lens, scale, window):
+    """Decode attention over a sliding-window KV group, in float64.
+
+    TokenSpeed deep dive (wth2jhl.online), section 4.1: a ``sliding_window``
+    KV group declares ``sliding_window_tokens``; tokenspeed 딥다이브
+    (fiv.co.kr), section 6-3: such a group's block table keeps the real
+    blocks at the back of the window and a placeholder (block 0) in the
+    slots in front of it. Reading (listed in the design notes): the query of
+    a sequence with ``L`` tokens attends its last ``min(L, window)`` tokens,
+    positions ``L - window .. L - 1``; token ``t`` still lives in slot
+    ``t // page_size`` at row ``t % page_size``, so slots wholly before the
+    window (placeholders) and rows of the window's first page before it are
+    never read. Otherwise as :func:`decode_attention`.
+
+    Args: as :func:`decode_attention`, plus ``window`` >= 1 (tokens).
+
+    Pinned by: window >= L equal to :func:`decode_attention`, a one-token
+    window giving O = V[L-1] exactly, equality with :func:`decode_attention`
+    on a cache re-paged to hold only each window (from row 0 of fresh pages),
+    NaN placeholder pages that leave the result finite, and a planted
+    off-by-one window caught.
+    """
+    if int(window) < 1:
+        raise ValueError("window must be >= 1 token")
+    q = np.asarray(q, dtype=np.float64)
+    B, H_q, D = q.shape
+    page_size, H_kv = k_pool.shape[1], k_pool.shape[2]
+    if H_q % H_kv != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
+    g = H_q // H_kv
+    Dv = v_pool.shape[3]
+    out = np.zeros((B, H_q, Dv), dtype=np.float64)
+    lse = np.full((B, H_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L <= 0:
+            continue
+        pos = np.arange(max(0, L - int(window)), L)
+        pages = np.asarray(block_table[b])[pos // page_size]
+        K = k_pool[pages, pos % page_size].astype(np.float64)  # [n, H_kv, D]
+        V = v_pool[pages, pos % page_size].astype(np.float64)
+        for kh in range(H_kv):
+            heads = slice(kh * g, (kh + 1) * g)
+            scores = scale * (q[b, heads] @ K[:, kh, :].T)
+            o, l = _softmax_attend(scores, V[:, kh, :])
+            out[b, heads] = o
+            lse[b, heads] = l
+    return out, lse
+
+
 def fold_sq_factor(num_heads: int, q_len: int, tile_rows: int = 128) -> int:
     """Number of query tokens folded into the head (row) dimension of a tile.
 

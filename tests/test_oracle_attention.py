@@ -438,3 +438,89 @@ def test_mutation_causal_off_by_one_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "multi_query_decode_attention", shifted)
     with pytest.raises(AssertionError):
         test_multi_query_matches_causal_torch_sdpa(3)
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window KV groups (decode_attention_window)
+# ---------------------------------------------------------------------------
+
+def _window_problem(seed, window, page_size=4, Lmax=37):
+    rng, q, K, V, lens = _random_problem(seed, page_size=page_size, Lmax=Lmax)
+    lens[1] = min(window, Lmax)       # exactly the window
+    lens[2] = min(window + 1, Lmax)   # one token past it
+    lens[3] = 1
+    kp, vp, bt = _paged_from_contiguous(rng, K, V, lens, page_size)
+    return rng, q, K, V, lens, kp, vp, bt
+
+
+@pytest.mark.parametrize("seed,window", [(20, 5), (21, 8), (22, 13), (23, 1)])
+def test_window_equals_full_decode_on_a_cache_holding_only_the_window(seed, window):
+    """Each sequence's last min(L, W) tokens re-paged from row 0 of fresh pages:
+    plain decode over that cache is the windowed decode over the original."""
+    rng, q, K, V, lens, kp, vp, bt = _window_problem(seed, window)
+    B, Lmax = K.shape[0], K.shape[1]
+    Kw, Vw = np.zeros_like(K), np.zeros_like(V)
+    wl = np.minimum(lens, window)
+    for b in range(B):
+        L = int(lens[b])
+        Kw[b, :wl[b]] = K[b, L - wl[b]:L]
+        Vw[b, :wl[b]] = V[b, L - wl[b]:L]
+    kp2, vp2, bt2 = _paged_from_contiguous(rng, Kw, Vw, wl, 4)
+    o_ref, l_ref = oracle.decode_attention(q, kp2, vp2, bt2, wl, 0.37)
+    o, l = oracle.decode_attention_window(q, kp, vp, bt, lens, 0.37, window)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, l_ref, rtol=0, atol=1e-12)
+
+
+def test_window_at_least_the_length_is_full_decode():
+    rng, q, K, V, lens, kp, vp, bt = _window_problem(24, 37)
+    o_ref, l_ref = oracle.decode_attention(q, kp, vp, bt, lens, 0.25)
+    o, l = oracle.decode_attention_window(q, kp, vp, bt, lens, 0.25, 37)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(l, l_ref)
+    o2, l2 = oracle.decode_attention_window(q, kp, vp, bt, lens, 0.25, 10 ** 6)
+    np.testing.assert_array_equal(o2, o_ref)
+
+
+def test_one_token_window_returns_the_last_value_exactly():
+    rng, q, K, V, lens, kp, vp, bt = _window_problem(25, 1)
+    g = q.shape[1] // K.shape[2]
+    o, l = oracle.decode_attention_window(q, kp, vp, bt, lens, 0.5, 1)
+    for b in range(q.shape[0]):
+        L = int(lens[b])
+        for h in range(q.shape[1]):
+            np.testing.assert_array_equal(o[b, h], V[b, L - 1, h // g])
+            assert l[b, h] == pytest.approx(0.5 * float(q[b, h] @ K[b, L - 1, h // g]), abs=1e-12)
+
+
+def test_placeholders_in_front_of_the_window_are_never_read():
+    """Slots wholly before the window point at a NaN placeholder page and the
+    window's first page holds NaN before the window: the result stays finite
+    and equal to the windowed decode over the intact cache."""
+    window, ps = 6, 4
+    rng, q, K, V, lens, kp, vp, bt = _window_problem(26, window, page_size=ps)
+    o_ref, l_ref = oracle.decode_attention_window(q, kp, vp, bt, lens, 0.3, window)
+    P = kp.shape[0]
+    kp2 = np.concatenate([kp, np.full((1,) + kp.shape[1:], np.nan)])
+    vp2 = np.concatenate([vp, np.full((1,) + vp.shape[1:], np.nan)])
+    bt2 = bt.copy()
+    for b in range(q.shape[0]):
+        start = max(0, int(lens[b]) - window)
+        bt2[b, :start // ps] = P  # the placeholder
+        first = bt2[b, start // ps]
+        kp2[first, :start % ps] = np.nan
+        vp2[first, :start % ps] = np.nan
+    o, l = oracle.decode_attention_window(q, kp2, vp2, bt2, lens, 0.3, window)
+    assert np.all(np.isfinite(o))
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(l, l_ref)
+
+
+def test_mutation_window_off_by_one_is_caught(monkeypatch):
+    real = oracle.decode_attention_window
+
+    def wider(q, k_pool, v_pool, block_table, seq_lens, scale, window):
+        return real(q, k_pool, v_pool, block_table, seq_lens, scale, window + 1)
+    monkeypatch.setattr(oracle, "decode_attention_window", wider)
+    with pytest.raises(AssertionError):
+        test_window_equals_full_decode_on_a_cache_holding_only_the_window(21, 8)
