@@ -196,6 +196,32 @@ TS_API int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t tile_
  * ts_paged_decode_multi_attn (B sequences of q_len query tokens). Returns 0 on
  * invalid arguments.
  */
+/*
+ * ts_paged_decode_window_attn - decode attention over a sliding-window KV
+ * group: each sequence's query attends its last `window` tokens only.
+ *
+ * TokenSpeed deep dive, section 4.1: a sliding_window KV group declares
+ * sliding_window_tokens; tokenspeed 딥다이브 (fiv.co.kr), section 6-3: its
+ * block table keeps the real blocks at the back of the window and a
+ * placeholder (block 0) in the slots in front of it. The query of a sequence
+ * with L = seq_lens[b] tokens attends positions max(0, L - window) .. L - 1;
+ * token t lives in slot t / page_size at row t % page_size as everywhere, so
+ * the slots wholly in front of the window (placeholders or stale pages) and
+ * the rows of the window's first page in front of it are never read. With
+ * window >= L this is ts_paged_decode_attn's result.
+ *
+ *   window    tokens, >= 1 (else TS_ERR_INVALID_ARG)
+ *   workspace >= ts_paged_decode_workspace_size(B, H_q, D)
+ *   all other arguments, support (dtype f32 / bf16) and errors as in
+ *   ts_paged_decode_attn.
+ */
+TS_API ts_status ts_paged_decode_window_attn(const void* q, const void* k_pool, const void* v_pool,
+                                             const int32_t* block_table, int32_t bt_stride,
+                                             const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                             int32_t D, int32_t page_size, int32_t num_pages, int32_t window,
+                                             float scale, ts_dtype dtype, void* out, float* lse,
+                                             void* workspace, size_t workspace_bytes, void* stream);
+
 TS_API size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q, int32_t D);
 
 /*

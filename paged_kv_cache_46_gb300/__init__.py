@@ -88,6 +88,8 @@ _SIGNATURES = {
                                             _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
     "ts_paged_decode_attn_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32,
                                                     _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP]),
+    "ts_paged_decode_window_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
+                                                   _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
     "ts_paged_decode_multi_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "ts_paged_decode_multi_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
                                                   _I32, _I32, _F32, ctypes.c_int, _VP, _VP, _VP, _SZ, _VP]),
@@ -214,6 +216,27 @@ def ts_paged_decode_attn(q, k_pool, v_pool, block_table, seq_lens, scale: float,
                                       block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, ps, P,
                                       float(scale), _dt(q), _ptr(out), _ptr(lse), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def ts_paged_decode_window_attn(q, k_pool, v_pool, block_table, seq_lens, scale: float, window: int, out=None,
+                                lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Decode attention over a sliding-window KV group (each query attends its
+    sequence's last ``window`` tokens); returns ``out`` (and ``lse``)."""
+    _require_i32(block_table, seq_lens)
+    B, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, H_q, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(ts_paged_decode_workspace_size(B, H_q, D), q.device)
+    _check(lib().ts_paged_decode_window_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                             block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, ps, P,
+                                             int(window), float(scale), _dt(q), _ptr(out), _ptr(lse),
+                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             _stream(stream)))
     return (out, lse) if return_lse else out
 
 

@@ -194,7 +194,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
                             int32_t page_size, int32_t num_pages, float scale, ts_dtype dtype,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream, const char* who, const PrefixInputs* pre,
-                            const Fp8Scales* f8 = nullptr) {
+                            const Fp8Scales* f8 = nullptr, int32_t window = 0) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
       bt_stride <= 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
@@ -205,6 +205,9 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
                 who, q_len);
   if (H_q % H_kv != 0)
     return fail(TS_ERR_INVALID_ARG, "%s: H_q=%d not a multiple of H_kv=%d", who, H_q, H_kv);
+  if (window < 0 || (window > 0 && (q_len != 1 || pre != nullptr || f8 != nullptr)))
+    return fail(TS_ERR_INVALID_ARG, "%s: window=%d (>= 1, one query token, no shared prefix, no fp8)", who,
+                window);
   if (dtype != TS_F32 && dtype != TS_BF16)
     return fail(TS_ERR_INVALID_ARG, "%s: bad dtype %d", who, static_cast<int>(dtype));
   if (!std::isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "%s: scale not finite", who);
@@ -230,6 +233,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
       return fail(TS_ERR_INVALID_ARG, "%s: scale arrays must be 16-byte aligned", who);
   }
   KernelFn fn = f8 != nullptr ? pick_paged_fp8_kernel(D, g)
+                : window > 0  ? pick_paged_window_kernel(dtype, D, g)
                 : q_len == 1  ? pick_kernel(dtype, D, g, pre != nullptr)
                               : pick_paged_multi_kernel(dtype, D, g * fold);
   if (!fn)
@@ -274,6 +278,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   prm.prefix_len = pre ? pre->prefix_len : nullptr;
   prm.prefix_o = pre ? pre->prefix_o : nullptr;
   prm.prefix_lse = pre ? pre->prefix_lse : nullptr;
+  prm.window = window;
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   prm.err_word = reinterpret_cast<uint32_t*>(wsb);
   prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
@@ -453,6 +458,20 @@ extern "C" ts_status ts_paged_decode_attn(const void* q, const void* k_pool, con
                                  D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                  workspace_bytes, static_cast<cudaStream_t>(stream),
                                  "ts_paged_decode_attn");
+}
+
+extern "C" ts_status ts_paged_decode_window_attn(const void* q, const void* k_pool, const void* v_pool,
+                                                 const int32_t* block_table, int32_t bt_stride,
+                                                 const int32_t* seq_lens, int32_t B, int32_t H_q,
+                                                 int32_t H_kv, int32_t D, int32_t page_size,
+                                                 int32_t num_pages, int32_t window, float scale,
+                                                 ts_dtype dtype, void* out, float* lse, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+  const char* who = "ts_paged_decode_window_attn";
+  if (window < 1) return ts::fail(TS_ERR_INVALID_ARG, "%s: window=%d (>= 1 token)", who, window);
+  return ts::paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, 1, H_q, H_kv, D,
+                               page_size, num_pages, scale, dtype, out, lse, workspace, workspace_bytes,
+                               static_cast<cudaStream_t>(stream), who, nullptr, nullptr, window);
 }
 
 extern "C" size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q, int32_t D) {

@@ -62,6 +62,9 @@ struct PagedParams {
   const float* k_scale;
   const float* v_scale;
   uint32_t scale_area;
+  // Sliding-window KV group (plain decode only): a sequence attends its last
+  // `window` tokens; 0 = the whole context.
+  int32_t window = 0;
 };
 
 using PagedKernelFn = void (*)(const PagedParams);
@@ -71,6 +74,9 @@ PagedKernelFn pick_paged_multi_kernel(ts_dtype dt, int D, int G);
 // Kernel for an fp8 (e4m3fn) cache with bf16 queries and G rows per kv head
 // (defined in ts_paged_decode_fp8.cu); nullptr if not compiled.
 PagedKernelFn pick_paged_fp8_kernel(int D, int G);
+// Kernel for a sliding-window KV group with G rows per kv head (defined in
+// ts_paged_decode_window.cu); nullptr if not compiled.
+PagedKernelFn pick_paged_window_kernel(ts_dtype dt, int D, int G);
 
 namespace {
 
@@ -189,15 +195,31 @@ __device__ __forceinline__ int real_seq(const PagedParams& p, int v) {
   return v;
 }
 
+// Tokens in the whole pages in front of a sliding window (TokenSpeed deep
+// dive, section 4.1: a sliding_window KV group; tokenspeed 딥다이브, section
+// 6-3: the slots in front of the window hold a placeholder block). Their
+// block-table slots are skipped, never read.
+template <bool kWin>
+__device__ __forceinline__ int window_skip(const PagedParams& p, int v) {
+  if constexpr (!kWin) {
+    return 0;
+  } else {
+    const int L = p.seq_lens[v];
+    return L > p.window ? (L - p.window) & -p.page_size : 0;  // page_size: a power of two
+  }
+}
+
 // Own tokens of virtual sequence v: those its last row attends (after the
 // shared prefix in prefix mode, where every sequence has one query token).
-template <bool kPfx, bool kMulti>
+// With a sliding window: the tokens from the window's first page on (its
+// rows in front of the window are not copied).
+template <bool kPfx, bool kMulti, bool kWin>
 __device__ __forceinline__ int vseq_len(const PagedParams& p, int v) {
   if constexpr (kMulti) {
     const int b = real_seq<kMulti>(p, v);
     return p.seq_lens[b] - p.q_len + (v - b * p.steps + 1) * p.fold;
   } else {
-    return p.seq_lens[v] - prefix_tokens<kPfx>(p, v);
+    return p.seq_lens[v] - prefix_tokens<kPfx>(p, v) - window_skip<kWin>(p, v);
   }
 }
 
@@ -216,9 +238,10 @@ __device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k) 
   p.split_info[b] = make_int2(k, 0);
 }
 
-template <typename T, int D, int G, bool kPfx, bool kMulti, bool kFp8>
+template <typename T, int D, int G, bool kPfx, bool kMulti, bool kFp8, bool kWin = false>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedParams p) {
   static_assert(!(kPfx && kMulti), "shared prefixes take one query token per sequence");
+  static_assert(!kWin || (!kPfx && !kMulti && !kFp8), "sliding windows: plain decode");
   static_assert(!kFp8 || (G <= 4 && sizeof(T) == 2 && !kPfx), "fp8 cache: bf16 queries, up to 4 rows");
   // K/V element type (the lane split follows it); T is the query / output type
   using KV = std::conditional_t<kFp8, uint8_t, T>;
@@ -270,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   long long mine = 0;
   bool has_empty = false;
   for (int b = lo; b < hi; ++b) {
-    const int L = vseq_len<kPfx, kMulti>(p, b);
+    const int L = vseq_len<kPfx, kMulti, kWin>(p, b);
     if (L > 0)
       mine += (L + ps - 1) / ps + A;
     else if (b % G_ctas == k)
@@ -279,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   if (has_empty) {  // sequences with no own tokens are written here, after the wait
     pdl_wait_primary();
     for (int b = lo; b < hi; ++b)
-      if (vseq_len<kPfx, kMulti>(p, b) <= 0 && b % G_ctas == k)
+      if (vseq_len<kPfx, kMulti, kWin>(p, b) <= 0 && b % G_ctas == k)
         write_empty_sequence<T, kPfx>(p, D, b, k);
   }
   long long incl = mine;
@@ -306,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
     for (int b = lo; b < hi; ++b) {
-      const int L = vseq_len<kPfx, kMulti>(p, b);
+      const int L = vseq_len<kPfx, kMulti, kWin>(p, b);
       const long long np = L > 0 ? (L + ps - 1) / ps + A : 0;
       if (start < off + np) {
         s_start[0] = b;
@@ -343,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         const int bb = base + lane;
         pre_out = 0;
         if (bb >= B) return -1;
-        pre_out = prefix_tokens<kPfx>(p, bb);
-        return max(vseq_len<kPfx, kMulti>(p, bb), 0);
+        pre_out = prefix_tokens<kPfx>(p, bb) + window_skip<kWin>(p, bb);
+        return max(vseq_len<kPfx, kMulti, kWin>(p, bb), 0);
       };
       int win_pre, nxt_pre;
       int win_len = load_len(wb, win_pre);
@@ -441,7 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
           const int page = __shfl_sync(0xffffffffu, pid, i);
           const int pidx = cur.pg0 + i;
           const bool ok = page >= 0 && page < p.num_pages;
-          const int rows = ok ? ((pidx == np_cur - 1) ? (cur.L - pidx * ps) : ps) : 0;
+          // rows [lo, rows_end) of the page: a sliding window's first page
+          // starts at the window's first token
+          const int lo = (kWin && pidx == 0) ? max(0, cur.L - p.window) : 0;
+          const int rows_end = ok ? ((pidx == np_cur - 1) ? (cur.L - pidx * ps) : ps) : 0;
+          const int rows = kWin ? max(0, rows_end - lo) : rows_end;
           const int nchunks = rows > 0 ? (rows + p.chunk_rows - 1) / p.chunk_rows : 1;
           for (int c = 0; c < nchunks; ++c) {
             if (lane == 0) {
@@ -450,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
                 set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
                 aborted = true;
               } else {
-                const int r0 = c * p.chunk_rows;
-                const int valid = max(0, min(rows - r0, p.chunk_rows));
+                const int r0 = lo + c * p.chunk_rows;
+                const int valid = max(0, min(rows_end - r0, p.chunk_rows));
                 uint32_t flags = ((cur.flags & kSegFirst) && i == 0 && c == 0 ? kFlagFirst : 0u) |
                                  ((cur.flags & kSegLast) && i == cur.cnt - 1 && c == nchunks - 1 ? kFlagLast : 0u);
                 if (!ok) {
