@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla",
                                            "spec_verify_q2", "spec_verify_q4", "llama3_8b_layer_fp8",
-                                           "cascade_nested"],
+                                           "cascade_nested", "sliding_window"],
                     default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -212,6 +212,8 @@ def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
         return workloads.nested_prefix_cascade(device=device, members=8 if small else n(256))
     if name == "llama3_8b_layer_fp8":
         return workloads.llama3_8b_layer_fp8(device=device, B=8 if small else n(64))
+    if name == "sliding_window":
+        return workloads.sliding_window(device=device, B=4 if small else n(64))
     if name.startswith("spec_verify_q"):
         return workloads.speculative_verify(device=device, B=8 if small else n(64), q_len=int(name[13:]))
     raise ValueError(name)
@@ -224,7 +226,7 @@ def algorithmic(case, groups=None):
     prefix once plus every sequence's own rows. MLA: every latent row once;
     flops of Q.C^T over 576 dims and P.V over 512."""
     es = 2 if case.dtype == "bf16" else 4
-    tokens = int(case.attn_lens.astype(np.int64).sum())
+    tokens = int(case.attended_lens.astype(np.int64).sum())
     if case.mla:
         return tokens * case.D * es, tokens * case.H_q * (case.D + case.Dv) * 2
     if case.kv_fp8:
@@ -287,6 +289,9 @@ def oracle_pass(view, case):
     if case.q_len > 1:
         return oracle.multi_query_decode_attention(view["q"], kp, vp, view["block_table"], view["seq_lens"],
                                                    case.scale)
+    if case.window > 0:
+        return oracle.decode_attention_window(view["q"], kp, vp, view["block_table"], view["seq_lens"], case.scale,
+                                              case.window)
     if case.append:
         kp, vp = oracle.kv_append(kp, vp, view["k_new"], view["v_new"], view["block_table"],
                                   view["positions"], case.page_size)
@@ -296,7 +301,7 @@ def oracle_pass(view, case):
 def sample_bytes(case, idx):
     """Flat (ungrouped) algorithmic bytes of the sampled sequences."""
     es = 4 if case.dtype == "f32" else 2
-    tokens = int(case.attn_lens[idx].astype(np.int64).sum())
+    tokens = int(case.attended_lens[idx].astype(np.int64).sum())
     if case.mla:
         return tokens * case.D * es
     if case.kv_fp8:
@@ -318,14 +323,14 @@ def time_oracle(case, idx, budget_s: float):
 
 def cpu_baseline(case, budget_s: float = 12.0):
     """The oracle (fp64 numpy, one BLAS thread) on a bounded sample of the workload."""
-    t1, _ = time_oracle(case, [int(np.argmin(case.attn_lens))], 0.0)
-    per_seq_est = max(t1, 1e-4) * case.attn_lens.mean() / max(1, case.attn_lens.min())
+    t1, _ = time_oracle(case, [int(np.argmin(case.attended_lens))], 0.0)
+    per_seq_est = max(t1, 1e-4) * case.attended_lens.mean() / max(1, case.attended_lens.min())
     n = int(max(1, min(case.B, budget_s / 2 / per_seq_est)))
     idx = workloads.sample_sequences(case, n)[:n] if n < case.B else np.arange(case.B)
     sec, reps = time_oracle(case, idx, budget_s)
     nbytes = sample_bytes(case, idx)
     return {"value": nbytes / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(idx)} of {case.B} sequences ({int(case.attn_lens[idx].sum())} tokens) x {reps} passes, "
+            "sample": f"{len(idx)} of {case.B} sequences ({int(case.attended_lens[idx].sum())} tokens) x {reps} passes, "
                       f"fp64 numpy, 1 BLAS thread; bytes counted flat (no prefix sharing)",
             "query_tokens_per_s": len(idx) * case.q_len / sec}
 
@@ -430,6 +435,9 @@ class DeviceStep:
         elif c.mla:
             ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=out, lse=self.lse,
                                    workspace=self.ws, stream=stream)
+        elif c.window > 0:
+            ts.ts_paged_decode_window_attn(q, kp, vp, bt, lens, c.scale, c.window, out=out, lse=self.lse,
+                                           workspace=self.ws, stream=stream)
         elif c.q_len > 1:
             ts.ts_paged_decode_multi_attn(q, kp, vp, bt, lens, c.scale, out=out, lse=self.lse,
                                           workspace=self.ws, stream=stream)
@@ -695,7 +703,7 @@ def run_ours(args):
                                        "bf16" if case.dtype == "bf16" else "f32"), "accumulate": "f32",
         "data": "synthetic",
         "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D,
-                   "Dv": case.Dv, "page_size": case.page_size, "tokens_attended": int(case.attn_lens.sum()),
+                   "Dv": case.Dv, "page_size": case.page_size, "tokens_attended": int(case.attended_lens.sum()),
                    "kv_bytes_per_step": nbytes, "append": case.append, "q_len": case.q_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {rotate} rotated pool cop{'y' if rotate == 1 else 'ies'} of "

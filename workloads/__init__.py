@@ -65,12 +65,19 @@ class PagedCase:
     k_scale: Optional[torch.Tensor] = None
     v_scale: Optional[torch.Tensor] = None
     prefix_pages_truth: int = 0
+    window: int = 0             # sliding-window KV group: tokens a query attends (0: all of them)
     meta: Dict = field(default_factory=dict)
 
     @property
     def attn_lens(self) -> np.ndarray:
         """Tokens attended by the step (one more than cached when appending)."""
         return (self.seq_lens + (1 if self.append else 0)).astype(np.int32)
+
+    @property
+    def attended_lens(self) -> np.ndarray:
+        """Tokens each query reads: the attended length, capped by the window."""
+        L = self.attn_lens
+        return np.minimum(L, self.window).astype(np.int32) if self.window > 0 else L
 
     @property
     def bt_stride(self) -> int:
@@ -84,7 +91,7 @@ class PagedCase:
     def kv_bytes_read(self) -> int:
         """Algorithmic K/V (or latent) bytes one attention pass must read."""
         esize = 4 if self.dtype == "f32" else 2
-        tokens = int(self.attn_lens.astype(np.int64).sum())
+        tokens = int(self.attended_lens.astype(np.int64).sum())
         if self.mla:
             return tokens * self.D * esize
         if self.kv_fp8:  # one-byte codes plus a float32 scale per row and kv head, K and V
@@ -347,6 +354,33 @@ def speculative_verify(device="cpu", seed: int = 6, B: int = 64, q_len: int = 4,
     return build_case(f"speculative_verify_B{B}_q{q_len}", seed, B=B, H_q=32, H_kv=8, D=128,
                       page_size=16, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128),
                       device=device, rng=rng, q_len=q_len)
+
+
+def sliding_window(device="cpu", seed: int = 8, B: int = 64, lo: int = 4096, hi: int = 32768,
+                   window: int = 4096) -> PagedCase:
+    """Llama-3-8B-shaped layer over a sliding-window KV group: 32/8 heads,
+    D=128, bf16, page 16, lens ~ U[lo, hi], each query attending its last
+    ``window`` tokens. As in such a group's block table (tokenspeed 딥다이브,
+    section 6-3), the slots wholly in front of the window hold a placeholder
+    page; only the window's pages are real (pool 1.25x of them)."""
+    rng = np.random.default_rng(seed)
+    ps = 16
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    slots = _pages_for(lens, ps)
+    first = np.maximum(0, lens.astype(np.int64) - window) // ps
+    need = slots - first
+    num_pages = int(np.ceil(need.sum() * 1.25)) + 1
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((B, int(slots.max())), perm[-1], dtype=np.int32)  # perm[-1]: the placeholder
+    c = 0
+    for b in range(B):
+        bt[b, first[b]:slots[b]] = perm[c:c + need[b]]
+        c += int(need[b])
+    case = build_case(f"sliding_window_B{B}_W{window}", seed, B=B, H_q=32, H_kv=8, D=128, page_size=ps,
+                      seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128), device=device, rng=rng,
+                      layout=(bt, num_pages))
+    case.window = int(window)
+    return case
 
 
 def mixed_lengths(device="cpu", seed: int = 3, repeat: int = 32) -> PagedCase:
