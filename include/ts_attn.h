@@ -296,6 +296,13 @@ TS_API ts_status ts_kv_append_fp8(const void* k_new, const void* v_new, void* k_
  *   workspace       >= ts_paged_decode_workspace_size(B, H_q, D)
  *   other arguments as ts_paged_decode_attn. Supported: D in {64, 128},
  *   H_q / H_kv in {1, 2, 4}, H_kv in {1, 2, 4, 8}, page_size in {8, 16, 32}.
+ *
+ * The CUDA-core split-KV kernel runs it. With the environment variable
+ * TS_FP8_DECODE_PATH=tensor a tensor-core kernel runs it instead where the
+ * shape allows (page 16, 2 or 4 kv heads per CTA): the codes are widened to
+ * f16 on chip and the probabilities rounded to f16 for the P V product (the
+ * row sum and the LSE stay float32). It is measured slower on the Llama-3-8B
+ * layer shape, hence not the default.
  */
 TS_API ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool, const void* v_pool,
                                           const float* k_scale, const float* v_scale,

@@ -177,6 +177,11 @@ int gqa_fold(int g, int q_len) {
 // Launches the paged split-KV kernel pair for q_len query tokens per
 // sequence; `pre` non-null selects prefix (cascade) mode (q_len 1 only).
 // Tensor-core path for several query tokens per sequence (ts_mq_tc.cu).
+ts_status launch_fp8_decode_tc(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+                               const float* v_scale, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                               int32_t page_size, int32_t num_pages, float scale, void* out, float* lse,
+                               uint32_t* err_word, cudaStream_t stream);
 ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                                 int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
                                 int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
@@ -535,6 +540,25 @@ extern "C" ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool,
                                               int32_t H_kv, int32_t D, int32_t page_size,
                                               int32_t num_pages, float scale, void* out, float* lse,
                                               void* workspace, size_t workspace_bytes, void* stream) {
+  // The tensor-core kernel when the shape suits it (one CTA per sequence and
+  // 2 or 4 kv heads; arguments it cannot judge are left to the CUDA-core
+  // path's checks), else the CUDA-core split-KV kernel.
+  if (B > 0 && H_q > 0 && H_kv > 0 && q && k_pool && v_pool && k_scale && v_scale && block_table && seq_lens &&
+      out && std::isfinite(scale) && reinterpret_cast<uintptr_t>(q) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(out) % 16 == 0 && reinterpret_cast<uintptr_t>(k_pool) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(v_pool) % 16 == 0 && reinterpret_cast<uintptr_t>(k_scale) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(v_scale) % 16 == 0) {
+    const size_t need = ts::paged_decode_workspace_bytes(B, H_q, D);
+    if (!workspace || need == 0 || workspace_bytes < need ||
+        reinterpret_cast<uintptr_t>(workspace) % ts::kWorkspaceAlign != 0)
+      return ts::fail(TS_ERR_WORKSPACE, "ts_paged_decode_fp8_attn: workspace %zu B < %zu B needed or misaligned",
+                      workspace_bytes, need);
+    const ts_status st = ts::launch_fp8_decode_tc(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,
+                                                  seq_lens, B, H_q, H_kv, D, page_size, num_pages, scale, out, lse,
+                                                  static_cast<uint32_t*>(workspace),
+                                                  static_cast<cudaStream_t>(stream));
+    if (st != TS_ERR_UNSUPPORTED) return st;
+  }
   return ts::launch_paged_decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,
                                      seq_lens, B, H_q, H_kv, D, page_size, num_pages, scale, out, lse,
                                      workspace, workspace_bytes, static_cast<cudaStream_t>(stream));

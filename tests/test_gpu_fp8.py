@@ -30,10 +30,18 @@ def _meta(case):
             torch.from_numpy(case.positions).to(DEV))
 
 
-def _decode(case, ctas=None):
+def _decode(case, ctas=None, path=None, hg=None, expect_kernel=None):
+    """path: None = the library's choice, "tensor" = the tcgen05 kernel where the
+    shape allows it, "cuda" = the CUDA-core split-KV kernel; hg: kv heads per
+    CTA of the tcgen05 kernel; expect_kernel: the decode kernel the launch
+    trace must show."""
     bt, lens, _ = _meta(case)
-    if ctas is not None:
-        os.environ["TS_PAGED_DECODE_CTAS"] = str(ctas)
+    env = {"TS_PAGED_DECODE_CTAS": ctas, "TS_FP8_DECODE_PATH": path, "TS_FP8_HEAD_GROUP": hg}
+    for k, v in env.items():
+        if v is not None:
+            os.environ[k] = str(v)
+    ts.ts_trace_collect()
+    ts.ts_trace_enable(expect_kernel is not None)
     try:
         ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D))
         out, lse = ts.ts_paged_decode_fp8_attn(case.q, case.k_pool, case.v_pool, case.k_scale, case.v_scale,
@@ -41,7 +49,12 @@ def _decode(case, ctas=None):
         torch.cuda.synchronize()
         assert ts.ts_read_device_error(ws) == 0
     finally:
-        os.environ.pop("TS_PAGED_DECODE_CTAS", None)
+        ts.ts_trace_enable(False)
+        for k in env:
+            os.environ.pop(k, None)
+    recs = ts.ts_trace_collect()
+    if expect_kernel is not None:
+        assert recs and recs[0][0] == expect_kernel, recs
     return out, lse
 
 
@@ -86,7 +99,7 @@ def test_decode_fp8_matches_oracle(D, H_q, H_kv, ps):
                                     page_size=ps, seq_lens=lens, scale=D ** -0.5, device=DEV)
     o_ref, l_ref = _oracle(case)
     for ctas in (None, 5):
-        out, lse = _decode(case, ctas)
+        out, lse = _decode(case, ctas, path="cuda")
         compare(out, o_ref, "bf16", lse, l_ref, f"fp8 D={D} {H_q}/{H_kv} ps={ps} ctas={ctas}")
 
 
@@ -95,7 +108,7 @@ def test_decode_fp8_independent_of_split_pattern(ctas):
     lens = [0, 1, 15, 16, 17, 700, 2049, 64]
     case = workloads.build_fp8_case("fp8_split", 85, B=len(lens), H_q=32, H_kv=8, D=128, page_size=16,
                                     seq_lens=lens, scale=0.0884, device=DEV)
-    out, lse = _decode(case, ctas)
+    out, lse = _decode(case, ctas, path="cuda")
     o_ref, l_ref = _oracle(case)
     compare(out, o_ref, "bf16", lse, l_ref, f"ctas={ctas}")
 
@@ -107,10 +120,44 @@ def test_llama_fp8_step_append_then_decode():
     view = workloads.oracle_view(case)
     bt, lens, pos = _meta(case)
     ts.ts_kv_append_fp8(case.k_new, case.v_new, case.k_pool, case.v_pool, case.k_scale, case.v_scale, bt, pos)
-    out, lse = _decode(case)
+    out, lse = _decode(case, expect_kernel="paged_decode_kernel")  # the library's choice: the CUDA-core kernel
     kp, vp, ks, vs = oracle.kv_append_fp8(view["k_pool"], view["v_pool"], view["k_scale"], view["v_scale"],
                                           view["k_new"], view["v_new"], view["block_table"], view["positions"],
                                           case.page_size)
     o_ref, l_ref = oracle.decode_attention_fp8(view["q"], kp, vp, ks, vs, view["block_table"], view["seq_lens"],
                                                case.scale)
     compare(out, o_ref, "bf16", lse, l_ref, "llama fp8 step")
+
+
+@pytest.mark.parametrize("D,H_q,H_kv,hg", [(128, 32, 8, 2), (128, 32, 8, 4), (64, 32, 8, 2), (64, 16, 4, 4),
+                                           (128, 16, 2, 2), (128, 64, 4, 2)])
+def test_decode_fp8_tensor_core_path(D, H_q, H_kv, hg):
+    """The tcgen05 kernel (2 or 4 kv heads per CTA, codes widened to f16 by
+    converter warps, scales on the scores and probabilities) against the
+    oracle: a one-token context, exact page and tile multiples, one key past
+    a tile, longer contexts; the launch trace shows the kernel ran."""
+    rng = np.random.default_rng(D * 7 + H_q + hg)
+    lens = rng.integers(1, 2500, size=10)
+    tile = 16 * (8 // hg)
+    lens[:5] = [1, 16, tile, tile + 1, 2 * tile - 1]
+    case = workloads.build_fp8_case(f"fp8_tc_{D}_{H_q}_{H_kv}_{hg}", 87, B=len(lens), H_q=H_q, H_kv=H_kv, D=D,
+                                    page_size=16, seq_lens=lens, scale=D ** -0.5, device=DEV)
+    o_ref, l_ref = _oracle(case)
+    out, lse = _decode(case, path="tensor", hg=hg, expect_kernel="fp8_tc_kernel")
+    compare(out, o_ref, "bf16", lse, l_ref, f"fp8 tensor core D={D} {H_q}/{H_kv} hg={hg}")
+
+
+def test_decode_fp8_paths_agree_on_the_llama_shape():
+    """The Llama-3-8B layer shape over an fp8 cache: the tensor-core and the
+    CUDA-core kernels against each other (every output) and the oracle on a
+    sample of 16 sequences."""
+    case = workloads.llama3_8b_layer_fp8(device=DEV, append=False)
+    o_tc, l_tc = _decode(case, path="tensor", expect_kernel="fp8_tc_kernel")
+    o_cc, l_cc = _decode(case, path="cuda")
+    assert (o_tc.float() - o_cc.float()).abs().max().item() <= 2e-2
+    assert (l_tc - l_cc).abs().max().item() <= 1e-3
+    idx = workloads.sample_sequences(case, 16)
+    view = workloads.oracle_view(case, idx)
+    o_ref, l_ref = _oracle(case, view)
+    dev_idx = torch.from_numpy(idx).to(DEV)
+    compare(o_tc[dev_idx], o_ref, "bf16", l_tc[dev_idx], l_ref, "llama fp8 tensor core sample")
