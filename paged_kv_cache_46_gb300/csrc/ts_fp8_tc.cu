@@ -24,7 +24,6 @@
 // producer (lane i < 8 / HG loads page i of a tile), warp 5 lane 0 MMA
 // issuer, warps 6-9 converters (a tile row per thread).
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <cmath>
 #include <cstdlib>

@@ -90,6 +90,28 @@ def test_pool_rows_beyond_int32_are_rejected_before_any_launch(lib):
                                    1 << 20, None) == ts.TS_ERR_INVALID_ARG
 
 
+def test_window_and_multi_query_entry_points_validate_before_any_launch(lib):
+    """Empty batches are no-ops on every newer entry point; a window below one
+    token and a non-finite scale are argument errors; nothing touches a device."""
+    vp = ctypes.c_void_p(16)
+    # ts_paged_decode_window_attn(q, k, v, bt, bt_stride, lens, B, H_q, H_kv, D, ps, P, window, scale, dt, ...)
+    assert lib.ts_paged_decode_window_attn(None, None, None, None, 4, None, 0, 32, 8, 128, 16, 8, 64, 1.0, 1,
+                                           None, None, None, 0, None) == ts.TS_OK
+    assert lib.ts_paged_decode_window_attn(vp, vp, vp, vp, 4, vp, 2, 32, 8, 128, 16, 8, 0, 1.0, 1,
+                                           vp, None, vp, 1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    assert b"window" in lib.ts_last_error_detail()
+    assert lib.ts_paged_decode_window_attn(vp, vp, vp, vp, 4, vp, 2, 32, 8, 128, 16, 8, 64, float("inf"), 1,
+                                           vp, None, vp, 1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    # ts_paged_decode_multi_attn: B = 0 with a tensor-core shape, then a non-finite scale
+    assert lib.ts_paged_decode_multi_attn(None, None, None, None, 4, None, 0, 4, 32, 8, 128, 16, 8, 1.0, 1,
+                                          None, None, None, 0, None) == ts.TS_OK
+    assert lib.ts_paged_decode_multi_attn(vp, vp, vp, vp, 4, vp, 2, 4, 32, 8, 128, 16, 8, float("nan"), 1,
+                                          vp, None, vp, 1 << 20, None) == ts.TS_ERR_INVALID_ARG
+    # ts_paged_decode_fp8_attn: B = 0
+    assert lib.ts_paged_decode_fp8_attn(None, None, None, None, None, None, 4, None, 0, 32, 8, 128, 16, 8, 1.0,
+                                        None, None, None, 0, None) == ts.TS_OK
+
+
 def test_python_binding_requires_int32_metadata():
     import torch
     q = torch.zeros(1, 8, 64)
