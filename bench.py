@@ -597,17 +597,20 @@ def run_ours(args):
         cp = torch.cuda.Stream(device=dev)
         ev_h2d, ev_comp, ev_d2h = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
-        def pipelined_steps(st):
-            """UNROLL decode steps, each with its own input upload and output
+        def pipelined_steps(st, n=UNROLL, groups=None):
+            """n decode steps, each with its own input upload and output
             read-back, on two streams: uploads and read-backs run on `cp`
-            beside the previous / next step's kernels (double-buffered)."""
+            beside the previous / next step's kernels (double-buffered). With
+            `groups` (cascade) each step also uploads its groups and forms the
+            next step's on the host while its kernels run; returns the groups
+            formed last."""
             cp.wait_stream(st)
             with torch.cuda.stream(cp):
                 d_packs[0].copy_(h_pack, non_blocking=True)
             ev_h2d[0].record(cp)
-            for k in range(UNROLL):
+            for k in range(n):
                 b = k & 1
-                if k + 1 < UNROLL:
+                if k + 1 < n:
                     if k >= 1:
                         cp.wait_event(ev_comp[b ^ 1])  # step k-1 has read its inputs
                     with torch.cuda.stream(cp):
@@ -616,13 +619,21 @@ def run_ours(args):
                 st.wait_event(ev_h2d[b])
                 if k >= 2:
                     st.wait_event(ev_d2h[b])  # step k-2's output is back on the host
-                runner.step(k, stream=st, inputs=dict(dins[b], out=d_outs[b]))
+                inputs = dict(dins[b], out=d_outs[b])
+                if groups is not None:
+                    with torch.cuda.stream(st):
+                        inputs["gdev"] = (ts.forest_to_device(groups, dev) if runner.forest is not None
+                                          else ts.groups_to_device(groups, dev))
+                runner.step(k, stream=st, inputs=inputs)
                 ev_comp[b].record(st)
                 cp.wait_event(ev_comp[b])
                 with torch.cuda.stream(cp):
                     h_outs[b].copy_(d_outs[b], non_blocking=True)
                 ev_d2h[b].record(cp)
+                if groups is not None:
+                    groups = group_on_host()
             st.wait_stream(cp)
+            return groups
 
         regroups = runner.groups is not None or runner.forest is not None
         n_e2e = min(args.steps, 50) if regroups else (args.steps + UNROLL - 1) // UNROLL * UNROLL
@@ -632,9 +643,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         # A serving loop replays its decode steps from a CUDA graph: capture
         # UNROLL pipelined steps (uploads, library calls, read-backs) once and
-        # replay them. Cascade regroups on the host every step and stays eager:
-        # each step's grouping runs on the host while the previous step's
-        # kernels run on the device.
+        # replay them. Cascade regroups on the host every step and runs the
+        # same pipeline eagerly: each step's grouping runs on the host while
+        # the previous step's kernels run on the device.
         graph = None
         if not regroups:
             cap = torch.cuda.Stream(device=dev)
@@ -654,8 +665,7 @@ def run_ours(args):
             for _ in range(n_e2e // UNROLL):
                 graph.replay()
         else:
-            for i in range(n_e2e):
-                groups = e2e_step(i, stream, groups)
+            groups = pipelined_steps(stream, n_e2e, groups)
         e2.record(stream)
         torch.cuda.synchronize()
         wall_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
@@ -664,7 +674,7 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
                "query_tokens_per_s": world * case.B * case.q_len / (e2e_ms * 1e-3),
                "cuda_graph": graph is not None,
-               "copies_overlap_compute": graph is not None}
+               "copies_overlap_compute": True}
         if host_group_ms:
             e2e["host_grouping_ms"] = statistics.median(host_group_ms)
 
