@@ -3,20 +3,26 @@
 //
 // TokenSpeed deep dive, section 7.2 (fold_sq_factor): folding query tokens
 // into the head dimension turns the rows of a decode step into a tile that
-// the tensor cores can take. Here one CTA takes one (sequence, kv head): its
-// R = q_len x g query rows (token j, head h*g + i at row j*g + i; rows past R
-// are zero) attend the sequence's pages as S = Q K^T and O += P V on tcgen05,
-// 128 keys per tile, with the online softmax between them and the causal
-// limit of each token (row of token j: keys before L - q_len + 1 + j).
+// the tensor cores can take. Here one CTA takes HG (1, 2 or 4) kv heads of
+// one sequence. The R = q_len x g query rows of head slot hs sit in TMEM
+// lanes [hs * 128/HG, ...) (token j, query head (h0+hs)*g + i at row
+// j*g + i; rows past R are zero). They attend the sequence's pages as
+// S = Q K^T and O += P V on tcgen05, with the online softmax between them and
+// the causal limit of each token (row of token j: keys before
+// L - q_len + 1 + j). A key tile is 128 pool rows: 8 / HG pages of all HG
+// heads, one TMA box per page and 64-column atom. A row scores only its own
+// head's keys, and P is zero in the other heads' columns, so the product is
+// block-diagonal over the heads.
 //
 // Roles (192 threads): warps 0-3 own one query row per thread (Q load,
 // softmax, epilogue; warps whose 32 rows are all padding skip the softmax),
-// warp 4 issues the TMA loads of K and V page boxes (its lanes hold the page
-// ids of the next key tile), warp 5 lane 0 issues the MMAs, S(j+1) or P V(j)
-// whichever is ready first. TMEM: S (128 fp32 columns), O (D columns), P (64
-// columns of bf16 pairs, the P V product's A operand). K and V tiles are
-// double-buffered; at D = 128 the K, V and Q tiles are two 64-column atoms
-// each and V's atoms are read by one N = 128 product.
+// warp 4 issues the TMA loads of K and V page boxes (one per lane; its lanes
+// hold the page ids of the next key tile), warp 5 lane 0 issues the MMAs,
+// S(j+1) or P V(j) whichever is ready first. TMEM: S (128 fp32 columns), O (D
+// columns), P (two buffers of 64 columns of bf16 pairs, the P V product's A
+// operand). K and V tiles sit in a 3-stage ring. At D = 128 the K, V and Q
+// tiles are two 64-column atoms each, and one N = 128 product reads both of
+// V's atoms.
 #include <cmath>
 #include <cstdlib>
 
