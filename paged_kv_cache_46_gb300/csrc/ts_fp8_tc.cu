@@ -9,7 +9,7 @@
 // - A CTA takes HG (2 or 4) kv heads of one sequence. A key tile is 128 pool
 //   rows: 8 / HG pages of the HG heads. TMA brings each page's codes of the
 //   HG heads in one box (landing [head][16 rows][D bytes]) and a bulk copy
-//   each page's K and V scale rows, into a two-stage staging ring.
+//   each page's K and V scale rows, into a three-stage staging ring.
 // - Four converter warps widen the codes to f16 (exactly, as their values
 //   times 2^-8; the scales take the 2^8) into the 128-byte swizzled layout
 //   the tensor cores read, zero the V rows past the sequence, and lay out
