@@ -149,3 +149,18 @@ def test_tensor_core_path_work_order(B, hg):
     out, lse = _run(case, 4, path="tensor", hg=hg)
     o_ref, l_ref = _oracle(case)
     compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B} hg={hg}")
+
+
+def test_full_speculative_verify_four_tokens_sampled():
+    """The benchmark's 4-draft-token workload at full size (B=64, 32/8 heads,
+    D=128) through the library's choice (the tensor-core kernel, 2 kv heads
+    per CTA, longest first): a seeded sample of 12 sequences against the
+    oracle."""
+    case = workloads.speculative_verify(device=DEV, q_len=4)
+    out, lse = _run(case, 4)
+    idx = workloads.sample_sequences(case, 12)
+    v = workloads.oracle_view(case, idx)
+    o_ref, l_ref = oracle.multi_query_decode_attention(v["q"], v["k_pool"], v["v_pool"], v["block_table"],
+                                                       v["seq_lens"], case.scale)
+    dev_idx = torch.from_numpy(idx).to(DEV)
+    compare(out[dev_idx], o_ref, "bf16", lse[dev_idx], l_ref, "speculative verify q4 full sample")

@@ -104,3 +104,24 @@ def test_window_below_one_is_an_argument_error():
     lens = torch.from_numpy(case.seq_lens).to(DEV)
     with pytest.raises(ts.TSError):
         ts.ts_paged_decode_window_attn(case.q, case.k_pool, case.v_pool, bt, lens, case.scale, 0)
+
+
+def test_window_full_workload_sampled():
+    """The benchmark's sliding-window workload at full size (B=64, contexts
+    U[4096, 32768], W=4096, placeholder slots in front of every window), in
+    the launch configuration bench.py times: a seeded sample of 8 sequences
+    (with the shortest and longest) against the oracle."""
+    case = workloads.sliding_window(device=DEV)
+    bt = torch.from_numpy(case.block_table).to(DEV)
+    lens = torch.from_numpy(case.seq_lens).to(DEV)
+    ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D), DEV)
+    out, lse = ts.ts_paged_decode_window_attn(case.q, case.k_pool, case.v_pool, bt, lens, case.scale, case.window,
+                                              workspace=ws, return_lse=True)
+    torch.cuda.synchronize()
+    assert ts.ts_read_device_error(ws) == 0
+    idx = workloads.sample_sequences(case, 8)
+    v = workloads.oracle_view(case, idx)
+    o_ref, l_ref = oracle.decode_attention_window(v["q"], v["k_pool"], v["v_pool"], v["block_table"],
+                                                  v["seq_lens"], case.scale, case.window)
+    dev_idx = torch.from_numpy(idx).to(DEV)
+    compare(out[dev_idx], o_ref, "bf16", lse[dev_idx], l_ref, "sliding window full workload sample")
