@@ -96,23 +96,79 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
   const int hgroups = p.H_kv / HG;
   const int h0 = static_cast<int>(blockIdx.x % hgroups) * HG;  // first kv head
   int b = static_cast<int>(blockIdx.x / hgroups);
-  if (p.B <= kLongestFirstMaxB) {
+  {
     // CTAs start roughly in index order: handing out the sequences by
-    // decreasing page count (ties by index) is the longest-first rule, which
-    // keeps the last wave short when the lengths differ.
-    auto tiles = [&](int s) {
+    // decreasing page count is the longest-first rule, which keeps the last
+    // wave short when the lengths differ. Up to kLongestFirstMaxB sequences
+    // each CTA ranks them exactly (ties by index), B^2 / 192 comparisons per
+    // thread; beyond, by 32 buckets of page count (within a bucket by index),
+    // three passes over the lengths. The scratch lies in the Q tile, which is
+    // written only after the last read of it.
+    auto pages = [&](int s) {
       const int len = p.seq_lens[s];
       return len > 0 ? min((len + kPS - 1) / kPS, p.bt_stride) : 0;
     };
     int* pick = reinterpret_cast<int*>(smem + Lay::kOffTmem + 8);
-    for (int s = tid; s < p.B; s += kThreads) {
-      const int ws = tiles(s);
-      int rank = 0;
-      for (int t = 0; t < p.B; ++t) {
-        const int wt = tiles(t);
-        rank += (wt > ws || (wt == ws && t < s)) ? 1 : 0;
+    if (p.B <= kLongestFirstMaxB) {
+      for (int s = tid; s < p.B; s += kThreads) {
+        const int ws = pages(s);
+        int rank = 0;
+        for (int t = 0; t < p.B; ++t) {
+          const int wt = pages(t);
+          rank += (wt > ws || (wt == ws && t < s)) ? 1 : 0;
+        }
+        if (rank == b) *pick = s;
       }
-      if (rank == b) *pick = s;
+    } else {
+      int* scratch = reinterpret_cast<int*>(smem + Lay::kOffQ);
+      int* mx_s = scratch;       // the largest page count
+      int* sel = scratch + 2;    // this CTA's bucket and its offset in it
+      int* hist = scratch + 32;  // [32] sequences per bucket
+      int* cnt = scratch + 64;   // [kThreads] bucket members in each thread's chunk
+      int mx = 0;
+      for (int s = tid; s < p.B; s += kThreads) mx = max(mx, pages(s));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (tid < 32) hist[tid] = 0;
+      if (tid == 0) *mx_s = 0;
+      __syncthreads();
+      if (lane == 0) atomicMax(mx_s, mx);
+      __syncthreads();
+      const int maxp = *mx_s;
+      auto bucket = [&](int s) { return 31 - min(31, pages(s) * 32 / (maxp + 1)); };  // 0: the longest
+      for (int s = tid; s < p.B; s += kThreads) atomicAdd(&hist[bucket(s)], 1);
+      __syncthreads();
+      if (tid == 0) {
+        int start = 0, k = 0;
+        for (; k < 31 && start + hist[k] <= b; ++k) start += hist[k];
+        sel[0] = k;
+        sel[1] = b - start;
+      }
+      const int chunk = (p.B + kThreads - 1) / kThreads;
+      const int s0 = min(p.B, tid * chunk), s1 = min(p.B, s0 + chunk);
+      __syncthreads();
+      const int kb = sel[0], off = sel[1];
+      int c = 0;
+      for (int s = s0; s < s1; ++s) c += bucket(s) == kb ? 1 : 0;
+      cnt[tid] = c;
+      __syncthreads();
+      if (tid == 0) {
+        int acc = 0;
+        for (int t = 0; t < kThreads; ++t) {
+          const int v = cnt[t];
+          cnt[t] = acc;
+          acc += v;
+        }
+      }
+      __syncthreads();
+      int before = cnt[tid];
+      if (off >= before && off < before + c) {
+        for (int s = s0; s < s1; ++s) {
+          if (bucket(s) != kb) continue;
+          if (before == off) *pick = s;
+          ++before;
+        }
+      }
     }
     __syncthreads();
     b = *pick;
