@@ -9,12 +9,15 @@
 // N=64 tensor-core product, but an fp32 accumulator of 128 x 512 would fill
 // all 512 TMEM columns. So a thread-block cluster of two CTAs (two SMs) shares
 // each page and splits the latent by columns:
-//   CTA 0: Q[:, 0:256]  . K[:, 0:256]^T   and O[:, 0:256]   += P V[:, 0:256]
-//   CTA 1: Q[:, 256:576] . K[:, 256:576]^T and O[:, 256:512] += P V[:, 256:512]
-// Each CTA loads only its latent columns (4 or 5 atoms of 64), so every byte
-// is read once; the two partial score tiles are swapped through distributed
-// shared memory and summed, so both CTAs hold the same full scores and the
-// same softmax. Q (the MMA's A operand) and P live in TMEM, which keeps the
+//   CTA 0: Q[:, 0:288]  . K[:, 0:288]^T   and O[:, 0:256]   += P V[:, 0:256]
+//   CTA 1: Q[:, 288:576] . K[:, 288:576]^T and O[:, 256:512] += P V[:, 256:512]
+// Each CTA loads five 64-column atoms of the latent: CTA 0 atoms 0-4, CTA 1
+// atoms 4-8. Atom 4 is loaded by both (the pair reads it at once, so the
+// second read hits L2), and each takes half of its 16-column steps, so both
+// issue 18 score products per page. Splitting at 256 would leave CTA 1 with 20
+// and CTA 0 with 16, and the tensor-core issue rate bounds the kernel. The
+// two partial score tiles are swapped through distributed shared memory and
+// summed, so both CTAs hold the same full scores and the same softmax. Q (the MMA's A operand) and P live in TMEM, which keeps the
 // small-N products from re-reading A from shared memory:
 //   TMEM columns: Q [0,160)  S [160,224)  P [224,256)  O [256,512).
 // Pages of the whole batch are cut into equal contiguous ranges, one per
@@ -155,9 +158,12 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   const uint32_t peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
-  const int n_atoms = rank == 0 ? 4 : 5;     // latent atoms this CTA loads
+  const int n_atoms = 5;                     // latent atoms this CTA loads
   const int atom0 = rank == 0 ? 0 : 4;       // first latent atom
-  const int q_words = rank == 0 ? 128 : 160; // TMEM columns of this CTA's Q part
+  const int q_words = 160;                   // TMEM columns of this CTA's Q part
+  // the shared atom 4 (stage atom 4 of CTA 0, 0 of CTA 1): CTA 0 takes its
+  // 16-column steps 0-1, CTA 1 steps 2-3
+  const int shared_atom = rank == 0 ? 4 : 0, shared_ks0 = rank == 0 ? 0 : 2;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   // [0,4) kv_full  [4,8) kv_empty  8 s_full  9 s_free  10 p_full  11 pv_done
@@ -292,11 +298,15 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       if (!mbar_wait(bar(s), (j / kStages) & 1)) return false;
       tc_fence_after();
       const uint32_t st = smem_u32(smem + kOffStages + s * kStageBytes);
-      for (int a = 0; a < n_atoms; ++a)
+      // the first product issued (atom 0, step 0 on CTA 0; step 2 on CTA 1)
+      // overwrites S, the others accumulate
+#pragma unroll
+      for (int a = 0; a < 5; ++a)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16_tmem_a(tmem + kTS, tmem + kTQ + a * 32 + ks * 8, desc_sw128(st + a * kAtomBytes + ks * 32),
-                          iS, (a | ks) != 0);
+          if (a != shared_atom || (ks >> 1) == (shared_ks0 >> 1))
+            mma_bf16_tmem_a(tmem + kTS, tmem + kTQ + a * 32 + ks * 8, desc_sw128(st + a * kAtomBytes + ks * 32),
+                            iS, (a == 0 && ks == shared_ks0) ? 0u : 1u);
       mma_commit(bar(8));
       return true;
     };
@@ -350,6 +360,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     auto load_q = [&](int b) {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<int64_t>(b) * kH + h) * kDqk + atom0 * 64 + hf * q_half * 2);
+#pragma unroll 1
       for (int c0 = 0; c0 < q_half; c0 += 16) {
         uint32_t u[16];
 #pragma unroll
