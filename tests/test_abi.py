@@ -37,6 +37,27 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
 
+def _declared_arity():
+    """Parameter count of every ts_* function the public headers declare."""
+    arity = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^TS_API\s+[\w\s\*]+?\b(ts_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+            params = m.group(2).strip()
+            arity[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return arity
+
+
+def test_binding_signatures_match_the_header():
+    """Every function the Python binding declares has the header's parameter
+    count (a mismatch would pass arguments into the wrong slots)."""
+    arity = _declared_arity()
+    assert len(arity) >= 13
+    for name, (_, args) in ts._SIGNATURES.items():
+        assert name in arity, f"{name} bound but not declared in include/"
+        assert len(args) == arity[name], f"{name}: binding has {len(args)} parameters, header {arity[name]}"
+
+
 def test_status_strings(lib):
     assert lib.ts_status_string(0) == b"TS_OK"
     assert lib.ts_status_string(1) == b"TS_ERR_INVALID_ARG"
