@@ -181,3 +181,64 @@ def test_forest_arguments():
         ts.ts_group_prefixes_nested(bt, lens, 4, 1)  # min_group < 2
     f = ts.ts_group_prefixes_nested(np.zeros((0, 1), np.int32), np.zeros(0, np.int32), 4)
     assert f["num_nodes"] == 0
+
+
+def _hand_forest_case():
+    ps = 4
+    bt = np.array([[0, 1, 2, 3, 10, 11, 20, 21],
+                   [0, 1, 2, 3, 10, 11, 22, 23],
+                   [0, 1, 2, 3, 12, 13, 24, 25],
+                   [0, 1, 2, 3, 14, 15, 26, 27],
+                   [30, 31, 32, 33, 34, 35, 36, 37]], np.int32)
+    lens = np.array([29, 32, 20, 30, 32], np.int32)
+    return bt, lens, ps
+
+
+def test_shared_depth_brute_force_hand_values():
+    """The brute-force shared depth on the hand example: sequences 0 and 1
+    share 6 pages, 2 and 3 only the 4-page system prompt, 4 nothing; with
+    min_group 3 the pair's deeper stretch no longer counts."""
+    bt, lens, ps = _hand_forest_case()
+    assert oracle.shared_depth_brute_force(bt, lens, ps, 2).tolist() == [6, 6, 4, 4, 0]
+    assert oracle.shared_depth_brute_force(bt, lens, ps, 3).tolist() == [4, 4, 4, 4, 0]
+    assert oracle.shared_depth_brute_force(bt, lens, ps, 5).tolist() == [0, 0, 0, 0, 0]
+
+
+def _copy_forest(f):
+    return {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in f.items()}
+
+
+def test_forest_checker_rejects_planted_mistakes():
+    """Mistakes planted in a valid forest are caught: a member dropped from
+    the deeper node (its sequence's shared depth is no longer the largest), a
+    node's stretch cut short, a sequence pointed at a shallower node, and a
+    member that does not share the node's pages."""
+    bt, lens, ps = _hand_forest_case()
+    good = ts.ts_group_prefixes_nested(bt, lens, ps, 2)
+    oracle.check_prefix_forest(bt, lens, ps, 2, good)
+
+    bad = _copy_forest(good)   # node 1 loses member 1
+    bad["member_ids"] = np.array([0, 1, 2, 3, 0], np.int32)
+    bad["member_indptr"] = np.array([0, 4, 5], np.int32)
+    bad["group_of"] = np.array([1, 0, 0, 0, -1], np.int32)
+    with pytest.raises(AssertionError):
+        oracle.check_prefix_forest(bt, lens, ps, 2, bad)
+
+    bad = _copy_forest(good)   # node 1's stretch cut to one page
+    bad["prefix_pages"] = np.array([0, 1, 2, 3, 10], np.int32)
+    bad["prefix_indptr"] = np.array([0, 4, 5], np.int32)
+    bad["prefix_len"] = np.array([16, 20], np.int32)
+    with pytest.raises(AssertionError):
+        oracle.check_prefix_forest(bt, lens, ps, 2, bad)
+
+    bad = _copy_forest(good)   # sequence 0 pointed at the root instead of its deepest node
+    bad["group_of"] = np.array([0, 1, 0, 0, -1], np.int32)
+    with pytest.raises(AssertionError):
+        oracle.check_prefix_forest(bt, lens, ps, 2, bad)
+
+    bad = _copy_forest(good)   # sequence 4 planted into the root it does not share
+    bad["member_ids"] = np.array([0, 1, 2, 3, 4, 0, 1], np.int32)
+    bad["member_indptr"] = np.array([0, 5, 7], np.int32)
+    bad["group_of"] = np.array([1, 1, 0, 0, 0], np.int32)
+    with pytest.raises(AssertionError):
+        oracle.check_prefix_forest(bt, lens, ps, 2, bad)
