@@ -17,6 +17,9 @@ compare what is unique, check the rest is valid):
 * a group's prefix is maximal: its members do not all share the next page too;
 * greedy longest-first: a sequence that starts with a group's whole prefix
   (and may share that many pages) is in that group or in a deeper one;
+* deepest first, at every depth d: no ``min_group`` sequences placed
+  shallower than d (ungrouped = depth 0) share their first d pages within
+  their caps, since the search would have grouped them at depth d first;
 * nothing is missed: among ungrouped sequences that could share a page, no
   ``min_group`` of them start with the same page id.
 """
@@ -117,6 +120,36 @@ def check_prefix_groups(block_table, seq_lens, page_size: int, min_group: int,
     for page, seqs in first_counts.items():
         if len(seqs) >= min_group:
             errors.append(f"{len(seqs)} ungrouped sequences share first page {page}")
+    errors.extend(_deepest_first_violations(bt, caps, depth, min_group))
+    return errors
+
+
+def _deepest_first_violations(bt, caps, depth, min_group: int) -> List[str]:
+    """Greedy deepest shared prefix first, checked at every depth d: among the
+    sequences placed shallower than d (ungrouped counts as depth 0) that may
+    share d pages, no ``min_group`` share the same first d page ids. If they
+    did, the greedy search would have formed their depth-d group before
+    settling any of them higher up.
+
+    Exhaustive over d; the first d pages of each row are identified by
+    interning (id of the first d-1 pages, page d-1) pairs, so every depth
+    costs one pass over the rows."""
+    B = bt.shape[0]
+    errors: List[str] = []
+    max_d = int(min(caps.max(initial=0), bt.shape[1]))
+    prefix_id = np.zeros(B, dtype=np.int64)
+    for d in range(1, max_d + 1):
+        pairs = np.stack([prefix_id, bt[:, d - 1].astype(np.int64)], axis=1)
+        _, prefix_id = np.unique(pairs, axis=0, return_inverse=True)
+        prefix_id = prefix_id.reshape(-1)
+        open_rows = np.nonzero((caps >= d) & (depth < d))[0]
+        if len(open_rows) < min_group:
+            continue
+        ids, counts = np.unique(prefix_id[open_rows], return_counts=True)
+        for pid in ids[counts >= min_group][:5]:
+            seqs = open_rows[prefix_id[open_rows] == pid]
+            errors.append(f"sequences {seqs[:8].tolist()} share their first {d} pages but are placed "
+                          f"shallower (not deepest-first)")
     return errors
 
 

@@ -69,10 +69,7 @@ def test_cascade_with_ungrouped_and_short_members():
     assert g["num_groups"] == 5
 
 
-@pytest.mark.parametrize("seed", range(6))
-def test_random_nested_prefix_trees(seed):
-    """Random nested sharing: sequences copy a random-length prefix of another
-    sequence's block-table row (a random tree of shared prefixes)."""
+def _random_tree_case(seed):
     rng = np.random.default_rng(seed)
     ps = int(rng.choice([4, 16]))
     B = int(rng.integers(2, 120))
@@ -90,8 +87,63 @@ def test_random_nested_prefix_trees(seed):
             bt[b, j] = next_page
             next_page += 1
     lens = rng.integers(0, max_pages * ps + 1, size=B).astype(np.int32)
+    return bt, lens, ps
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_nested_prefix_trees(seed):
+    """Random nested sharing: sequences copy a random-length prefix of another
+    sequence's block-table row (a random tree of shared prefixes)."""
+    bt, lens, ps = _random_tree_case(seed)
     for min_group in (2, 3):
         _check(bt, lens, ps, min_group)
+
+
+def _one_level_grouper(bt, lens, ps, min_group):
+    """A planted mistake: each run of sequences sharing a first page becomes one
+    group at the run's longest common prefix (within every member's cap), and
+    the search never goes deeper into sub-runs."""
+    caps = [(int(L) - 1) // ps if L > 0 else 0 for L in lens]
+    runs = {}
+    for b in range(len(lens)):
+        if caps[b] >= 1:
+            runs.setdefault(int(bt[b, 0]), []).append(b)
+    groups = []
+    for _, members in sorted(runs.items()):
+        if len(members) < min_group:
+            continue
+        n = 0
+        while n < min(caps[m] for m in members) and len({int(bt[m, n]) for m in members}) == 1:
+            n += 1
+        groups.append((bt[members[0], :n].tolist(), members))
+    pi, pp, pl, mi, mm = [0], [], [], [0], []
+    for pages, members in groups:
+        pp += pages
+        pi.append(len(pp))
+        pl.append(len(pages) * ps)
+        mm += members
+        mi.append(len(mm))
+    return PrefixGroups(np.array(pi), np.array(pp, np.int64), np.array(pl), np.array(mi),
+                        np.array(mm, np.int64), num_groups=len(groups))
+
+
+def test_one_level_grouper_fails_on_random_trees():
+    """The checker is not satisfied by a grouper that stops at the first level:
+    wherever its output differs from the greedy pass's, it is reported."""
+    differing = 0
+    for seed in range(6):
+        bt, lens, ps = _random_tree_case(seed)
+        for min_group in (2, 3):
+            good = _as_oracle(ts.ts_group_prefixes(bt, lens, ps, min_group))
+            shallow = _one_level_grouper(bt, lens, ps, min_group)
+            as_sets = lambda g: {(tuple(p.tolist()), tuple(sorted(m.tolist()))) for _, p, _, m in g.groups()}
+            if as_sets(good) == as_sets(shallow):
+                assert check_prefix_groups(bt, lens, ps, min_group, shallow) == []
+                continue
+            differing += 1
+            errs = check_prefix_groups(bt, lens, ps, min_group, shallow)
+            assert any("not deepest-first" in e for e in errs), (seed, min_group, errs[:3])
+    assert differing >= 6
 
 
 def test_capacity_and_argument_errors():

@@ -46,15 +46,34 @@ def test_valid_hand_grouping_passes():
 
 
 def test_shallow_grouping_is_rejected_as_not_greedy():
-    # one group at depth 2 for 0-3 is a valid cover but not longest-first
+    # One group at depth 2 for 0-3 covers every sequence and is maximal (0-3 do
+    # not all share page 12), but it is not deepest-first: 0 and 1 share three
+    # pages and sit at depth 2.
     shallow = [([10, 11], [0, 1, 2, 3]), ([20], [4, 5])]
     errs = check_prefix_groups(BT, LENS, 4, 2, _csr(shallow, 4))
-    assert errs == []  or any("deeper" in e or "maximal" in e for e in errs)
-    # 0-3 do not all share page 12, so that group is maximal; but 0 and 1 must
-    # then form the deeper group first:
+    assert any("[0, 1] share their first 3 pages" in e for e in errs), errs
+    assert not any("maximal" in e for e in errs)
+    # 0 and 1 left out entirely is caught as well
     only_deep_missing = [([10, 11], [2, 3]), ([20], [4, 5])]
     errs = check_prefix_groups(BT, LENS, 4, 2, _csr(only_deep_missing, 4))
-    assert any("share first page 10" in e or "not in it or deeper" in e for e in errs)
+    assert any("not in it or deeper" in e for e in errs)
+    assert any("[0, 1] share their first 3 pages" in e for e in errs)
+
+
+def test_deepest_first_keeps_a_leftover_ungrouped():
+    # 0 and 1 share [10, 11, 12]; 2 shares only [10, 11]. Deepest-first groups
+    # 0 and 1 at depth 3 and leaves 2 alone (fewer than min_group = 2), which is
+    # valid; pulling all three into [10, 11] is not.
+    bt = np.array([[10, 11, 12, 13], [10, 11, 12, 14], [10, 11, 15, 0]])
+    lens = np.array([16, 16, 12])
+    assert check_prefix_groups(bt, lens, 4, 2, _csr([([10, 11, 12], [0, 1])], 4)) == []
+    errs = check_prefix_groups(bt, lens, 4, 2, _csr([([10, 11], [0, 1, 2])], 4))
+    assert any("share their first 3 pages" in e for e in errs), errs
+    # with min_group 3 the pair does not qualify, so [10, 11] for all three is right
+    assert check_prefix_groups(bt, lens, 4, 3, _csr([([10, 11], [0, 1, 2])], 4)) == []
+    # the cap counts: if 1 may share only 2 pages, 0 alone is left at depth 3
+    lens_capped = np.array([16, 12, 12])
+    assert check_prefix_groups(bt, lens_capped, 4, 2, _csr([([10, 11], [0, 1, 2])], 4)) == []
 
 
 def test_planted_mistakes_are_reported():
