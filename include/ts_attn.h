@@ -168,9 +168,20 @@ TS_API ts_status ts_paged_decode_attn(const void* q, const void* k_pool, const v
  *     moderate batches (e.g. 32 x 128 with B up to ~1.4 million).
  *   - All calls on one device share the array: calls that may overlap on the
  *     GPU (unordered streams) race and give wrong results.
- *   - The error word in the array is cleared at the start of every call.
+ *   - The error word in the array is cleared at the start of every call;
+ *     ts_read_device_error(NULL, ...) reads it for the current device, so
+ *     device-side errors (page id out of range, timed-out wait) of the last
+ *     call are visible as with a workspace.
+ *   - Arguments and shape are checked first (TS_ERR_INVALID_ARG,
+ *     TS_ERR_UNSUPPORTED), then the scratch size (TS_ERR_WORKSPACE).
  *   - The first call on each device looks up the array's address with that
  *     device current; make it before any stream capture.
+ *   - Under CUDA's default lazy module loading, the array's memory is
+ *     committed on a device when the library's module is first loaded there:
+ *     at the first call (or ts_read_device_error(NULL, ...)). A caller that
+ *     hands all free HBM to its KV-cache pool must make that first call
+ *     before, or it fails with TS_ERR_CUDA (out of memory). Later calls
+ *     allocate nothing.
  */
 #define TS_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 TS_API ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_pool,
@@ -191,11 +202,6 @@ TS_API ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_pool,
  */
 TS_API int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t tile_rows);
 
-/*
- * ts_paged_decode_multi_workspace_size - workspace bytes for
- * ts_paged_decode_multi_attn (B sequences of q_len query tokens). Returns 0 on
- * invalid arguments.
- */
 /*
  * ts_paged_decode_window_attn - decode attention over a sliding-window KV
  * group: each sequence's query attends its last `window` tokens only.
@@ -222,6 +228,11 @@ TS_API ts_status ts_paged_decode_window_attn(const void* q, const void* k_pool, 
                                              float scale, ts_dtype dtype, void* out, float* lse,
                                              void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * ts_paged_decode_multi_workspace_size - workspace bytes for
+ * ts_paged_decode_multi_attn (B sequences of q_len query tokens). Returns 0 on
+ * invalid arguments.
+ */
 TS_API size_t ts_paged_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q, int32_t D);
 
 /*
@@ -502,7 +513,9 @@ TS_API ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const i
 
 /*
  * ts_read_device_error - copy the sticky error word of an attention
- * workspace to *error_bits (synchronises the stream).
+ * workspace to *error_bits (synchronises the stream). workspace == NULL
+ * reads the error word of ts_paged_decode_attn_noalloc's static scratch on
+ * the current device.
  */
 TS_API ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream);
 

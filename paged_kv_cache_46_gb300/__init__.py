@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(HERE, "libts_attn.so")
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_WORKSPACE, TS_ERR_CUDA, TS_ERR_CAPACITY = range(6)
 TS_F32, TS_BF16 = 0, 1
 TS_DEVERR_PAGE_RANGE, TS_DEVERR_TIMEOUT, TS_DEVERR_SMEM_ALIGN = 0x1, 0x2, 0x4
+TS_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # include/ts_attn.h
 
 
 class TSError(RuntimeError):
@@ -512,6 +513,8 @@ def ts_mla_paged_decode(q, kv_pool, block_table, seq_lens, scale: float, d_v: in
 
 
 def ts_read_device_error(workspace, stream=None) -> int:
+    """Sticky device error bits of a workspace; None reads those of the
+    allocation-free entry point's static scratch on the current device."""
     v = ctypes.c_uint32(0)
     _check(lib().ts_read_device_error(_ptr(workspace), ctypes.byref(v), _stream(stream)))
     return int(v.value)

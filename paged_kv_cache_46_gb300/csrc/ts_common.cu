@@ -172,8 +172,14 @@ int32_t ts_trace_collect(ts_launch_record* out, int32_t capacity) {
 }
 
 ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream) {
-  if (workspace == nullptr || error_bits == nullptr)
+  if (error_bits == nullptr)
     return ts::fail(TS_ERR_INVALID_ARG, "ts_read_device_error: null pointer");
+  if (workspace == nullptr) {   // the allocation-free entry point's static scratch
+    void* scratch = nullptr;
+    ts_status st0 = ts::noalloc_scratch_address(&scratch);
+    if (st0 != TS_OK) return st0;
+    workspace = scratch;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ts_status st = ts::cuda_check(
       cudaMemcpyAsync(error_bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s),

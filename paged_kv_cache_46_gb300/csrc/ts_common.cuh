@@ -17,6 +17,10 @@ namespace ts {
 ts_status fail(ts_status s, const char* fmt, ...);
 // Maps a CUDA error to TS_ERR_CUDA with a detail message (TS_OK if none).
 ts_status cuda_check(cudaError_t e, const char* what);
+
+// Device address of the allocation-free entry point's static scratch on the
+// current device (looked up once per device; defined beside that entry point).
+ts_status noalloc_scratch_address(void** addr);
 // SM count of the current device (cached per device).
 int device_sm_count();
 // Current device ordinal.

@@ -199,7 +199,8 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
                             int32_t page_size, int32_t num_pages, float scale, ts_dtype dtype,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream, const char* who, const PrefixInputs* pre,
-                            const Fp8Scales* f8 = nullptr, int32_t window = 0) {
+                            const Fp8Scales* f8 = nullptr, int32_t window = 0,
+                            bool check_only = false) {
   if (B < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 ||
       bt_stride <= 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
     return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)",
@@ -253,7 +254,9 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   const int n_ctas = paged_decode_ctas();
   if (n_ctas <= 0) return fail(TS_ERR_CUDA, "%s: cannot query the SM count", who);
   const WsLayout ws = workspace_layout(Bv, rows, D, n_ctas);
-  if (!workspace || workspace_bytes < ws.total)
+  if (check_only) {
+    workspace = nullptr;   // only the argument and support checks below run
+  } else if (!workspace || workspace_bytes < ws.total)
     return fail(TS_ERR_WORKSPACE, "%s: workspace %zu B < %zu B needed", who, workspace_bytes,
                 ws.total);
   if (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
@@ -284,11 +287,13 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   prm.prefix_o = pre ? pre->prefix_o : nullptr;
   prm.prefix_lse = pre ? pre->prefix_lse : nullptr;
   prm.window = window;
-  unsigned char* wsb = static_cast<unsigned char*>(workspace);
-  prm.err_word = reinterpret_cast<uint32_t*>(wsb);
-  prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
-  prm.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
-  prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  if (workspace != nullptr) {
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    prm.err_word = reinterpret_cast<uint32_t*>(wsb);
+    prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
+    prm.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
+    prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  }
   const size_t es_kv = f8 != nullptr ? 1 : es;  // K/V element bytes
   prm.row_bytes = static_cast<uint32_t>(H_kv * D * es_kv);
   prm.page_bytes = static_cast<uint32_t>(page_size) * prm.row_bytes;
@@ -357,6 +362,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   if (st != TS_OK) return st;
   if (smem > static_cast<size_t>(kSmemBudget))
     return fail(TS_ERR_UNSUPPORTED, "%s: shared memory plan %zu B exceeds %d B", who, smem, kSmemBudget);
+  if (check_only) return TS_OK;
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -428,6 +434,18 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
   return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q,
                                   H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                   workspace_bytes, stream, who, nullptr);
+}
+
+// Every argument and support check of ts_paged_decode_attn except the
+// workspace's; enqueues nothing.
+ts_status paged_decode_check_args(const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                  int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                  ts_dtype dtype, void* out, const char* who) {
+  return paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, 1, H_q, H_kv, D,
+                           page_size, num_pages, scale, dtype, out, nullptr, nullptr, 0, nullptr,
+                           who, nullptr, nullptr, 0, true);
 }
 
 size_t paged_decode_workspace_bytes(int B, int H_q, int D) {

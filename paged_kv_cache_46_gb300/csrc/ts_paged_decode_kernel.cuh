@@ -224,18 +224,19 @@ __device__ __forceinline__ int vseq_len(const PagedParams& p, int v) {
 }
 
 // Writes the output of a virtual sequence with no own tokens: O = 0,
-// LSE = -inf, or the prefix state alone in prefix mode.
+// LSE = -inf, or the prefix state alone in prefix mode. All 32 lanes of a
+// warp call it together; their stores are coalesced.
 template <typename T, bool kPfx>
-__device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k) {
+__device__ void write_empty_sequence(const PagedParams& p, int D, int b, int k, int lane) {
   const bool grouped = kPfx && p.group_of[b] >= 0;
   T* out = static_cast<T*>(p.out) + static_cast<int64_t>(b) * p.rows * D;
   const float* po = grouped ? p.prefix_o + static_cast<int64_t>(b) * p.rows * D : nullptr;
-  for (int i = 0; i < p.rows * D; ++i) out[i] = static_cast<T>(grouped ? po[i] : 0.0f);
+  for (int i = lane; i < p.rows * D; i += 32) out[i] = static_cast<T>(grouped ? po[i] : 0.0f);
   if (p.lse)
-    for (int h = 0; h < p.rows; ++h)
+    for (int h = lane; h < p.rows; h += 32)
       p.lse[static_cast<int64_t>(b) * p.rows + h] =
           grouped ? p.prefix_lse[static_cast<int64_t>(b) * p.rows + h] : -INFINITY;
-  p.split_info[b] = make_int2(k, 0);
+  if (lane == 0) p.split_info[b] = make_int2(k, 0);
 }
 
 template <typename T, int D, int G, bool kPfx, bool kMulti, bool kFp8, bool kWin = false>
@@ -299,11 +300,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
     else if (b % G_ctas == k)
       has_empty = true;
   }
-  if (has_empty) {  // sequences with no own tokens are written here, after the wait
+  // Sequences with no own tokens are written here, after the wait, each by a
+  // whole warp: the lanes that found some take turns handing their range to
+  // the warp (every thread runs this prologue, so the warps are converged).
+  unsigned todo = __ballot_sync(0xffffffffu, has_empty);
+  if (todo != 0u) {
     pdl_wait_primary();
-    for (int b = lo; b < hi; ++b)
-      if (vseq_len<kPfx, kMulti, kWin>(p, b) <= 0 && b % G_ctas == k)
-        write_empty_sequence<T, kPfx>(p, D, b, k);
+    while (todo != 0u) {
+      const int src = __ffs(todo) - 1;
+      todo &= todo - 1u;
+      const int slo = __shfl_sync(0xffffffffu, lo, src), shi = __shfl_sync(0xffffffffu, hi, src);
+      for (int b = slo; b < shi; ++b)
+        if (vseq_len<kPfx, kMulti, kWin>(p, b) <= 0 && b % G_ctas == k)
+          write_empty_sequence<T, kPfx>(p, D, b, k, lane);
+    }
   }
   long long incl = mine;
 #pragma unroll

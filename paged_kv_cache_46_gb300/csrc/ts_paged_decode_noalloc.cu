@@ -22,6 +22,14 @@
 //   * The first call on each device looks up the array's device address with
 //     that device current and caches it; make that first call before any
 //     stream capture.
+//   * Under CUDA's lazy module loading (the default) the array's memory is
+//     committed when its module is first loaded on a device, which is that
+//     first call (or ts_read_device_error(NULL, ...)); with eager loading it
+//     is committed when the library is loaded. A caller that reserves all
+//     free HBM for its KV-cache pool must make the first call before that.
+//   * Device-side problems (a page id out of range, a timed-out wait) set
+//     bits in the array's error word; ts_read_device_error(NULL, ...) reads
+//     it for the current device.
 #include <mutex>
 
 #include "ts_common.cuh"
@@ -36,6 +44,11 @@ ts_status launch_paged_decode(const void* q, const void* k_pool, const void* v_p
                               ts_dtype dtype, void* out, float* lse, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream, const char* who);
 size_t paged_decode_workspace_bytes(int B, int H_q, int D);
+ts_status paged_decode_check_args(const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv,
+                                  int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                  ts_dtype dtype, void* out, const char* who);
 
 namespace {
 
@@ -49,8 +62,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
+}  // namespace
+
 // Device address of g_noalloc_scratch on the current device (looked up once).
-ts_status scratch_address(void** addr) {
+ts_status noalloc_scratch_address(void** addr) {
   int dev = 0;
   ts_status st = cuda_check(cudaGetDevice(&dev), "ts_paged_decode_attn_noalloc: cudaGetDevice");
   if (st != TS_OK) return st;
@@ -71,7 +86,6 @@ ts_status scratch_address(void** addr) {
   return TS_OK;
 }
 
-}  // namespace
 }  // namespace ts
 
 extern "C" ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_pool,
@@ -84,8 +98,11 @@ extern "C" ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_p
   using namespace ts;
   const char* who = "ts_paged_decode_attn_noalloc";
   if (B == 0) return TS_OK;
-  if (B < 0 || H_q <= 0 || D <= 0)
-    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d H_q=%d D=%d)", who, B, H_q, D);
+  // The arguments and the shape are checked first, so that an unsupported
+  // shape is reported as such rather than as a scratch overflow.
+  ts_status st = paged_decode_check_args(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B,
+                                         H_q, H_kv, D, page_size, num_pages, scale, dtype, out, who);
+  if (st != TS_OK) return st;
   const size_t need = paged_decode_workspace_bytes(B, H_q, D);
   if (need == 0) return fail(TS_ERR_CUDA, "%s: cannot size the scratch (SM count query failed)", who);
   if (need > kScratchBytes)
@@ -94,7 +111,7 @@ extern "C" ts_status ts_paged_decode_attn_noalloc(const void* q, const void* k_p
                 "bytes; use ts_paged_decode_attn with a workspace",
                 who, B, H_q, D, need, kScratchBytes);
   void* scratch = nullptr;
-  ts_status st = scratch_address(&scratch);
+  st = noalloc_scratch_address(&scratch);
   if (st != TS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = cuda_check(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s), "clear the scratch error word");

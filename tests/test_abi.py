@@ -159,3 +159,14 @@ def test_fold_sq_factor_host_helper_matches_the_rule(lib):
             for tile in (8, 64, 128):
                 assert lib.ts_fold_sq_factor(H, q_len, tile) == oracle.fold_sq_factor(H, q_len, tile)
     assert lib.ts_fold_sq_factor(0, 4, 128) == 0 and lib.ts_fold_sq_factor(64, 0, 128) == 0
+
+
+def test_binding_constants_match_the_header():
+    text = open(os.path.join(ROOT, "include", "ts_attn.h")).read()
+    m = re.search(r"#define TS_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", text)
+    assert m, "TS_NOALLOC_SCRATCH_BYTES not found"
+    assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == ts.TS_NOALLOC_SCRATCH_BYTES
+    for name in ("TS_DEVERR_PAGE_RANGE", "TS_DEVERR_TIMEOUT", "TS_DEVERR_SMEM_ALIGN"):
+        v = re.search(rf"#define {name} (0x[0-9a-fA-F]+|\d+)u?", text) or re.search(rf"\b{name}\s*=\s*(0x[0-9a-fA-F]+|\d+)", text)
+        assert v, name
+        assert int(v.group(1), 0) == getattr(ts, name), name
