@@ -16,6 +16,8 @@ Each function restates the operation from the pages it cites:
   section 7.1: split-KV partial outputs carry a log-sum-exp and are reduced by it.
 * tokenspeed 딥다이브 (fiv.co.kr), section 6-4: fp8 token-group quantization
   (scale = group max / fp8 max, clamp, cast; reconstruction = code * scale).
+* TokenSpeed deep dive (wth2jhl.online), section 0 and the closing section:
+  tree speculation (draft tokens verified in one step under an ancestor mask).
 * TokenSpeed deep dive (wth2jhl.online), section 4.1, and tokenspeed 딥다이브
   (fiv.co.kr), section 6-3: sliding-window KV groups (the last
   ``sliding_window_tokens`` tokens, placeholders in front of the window).
@@ -32,7 +34,10 @@ from .attention import (
     decode_attention_window,
     fold_sq_factor,
     multi_query_decode_attention,
+    tree_ancestors,
+    tree_verify_decode_attention,
     mla_decode_attention,
+    mla_multi_query_decode_attention,
     merge_states,
     merge_states_many,
     kv_append,
@@ -45,6 +50,7 @@ from .fp8 import (
     dequantize,
     kv_append_fp8,
     decode_attention_fp8,
+    mla_decode_attention_fp8,
 )
 
 __all__ = [
@@ -52,7 +58,10 @@ __all__ = [
     "decode_attention",
     "fold_sq_factor",
     "multi_query_decode_attention",
+    "tree_ancestors",
+    "tree_verify_decode_attention",
     "mla_decode_attention",
+    "mla_multi_query_decode_attention",
     "merge_states",
     "merge_states_many",
     "kv_append",
@@ -65,5 +74,6 @@ __all__ = [
     "dequantize",
     "kv_append_fp8",
     "decode_attention_fp8",
+    "mla_decode_attention_fp8",
     "PrefixGroups",
 ]

@@ -226,6 +226,81 @@ def multi_query_decode_attention(q, k_pool, v_pool, block_table, seq_lens, scale
     return out, lse
 
 
+def tree_ancestors(parents) -> list:
+    """Ancestor-or-self sets of the nodes of a draft tree.
+
+    ``parents[j]`` is node ``j``'s parent among the draft tokens (``< j``), or
+    -1 for a node that hangs directly off the committed context. Returns, per
+    node, the sorted list of node indices on its path from the context down to
+    itself.
+    """
+    out = []
+    for j, par in enumerate(int(x) for x in parents):
+        if par >= j or par < -1:
+            raise ValueError(f"parents[{j}] = {par}: must be -1 or an earlier node")
+        out.append((out[par] if par >= 0 else []) + [j])
+    return out
+
+
+def tree_verify_decode_attention(q, k_pool, v_pool, block_table, seq_lens, parents, scale):
+    """Verify a tree of draft tokens in one decode step (tree speculation).
+
+    Each sequence carries ``n`` draft tokens that form a tree: node ``j`` has
+    parent ``parents[b, j]`` (an earlier node, or -1 for a child of the last
+    committed token). Their K/V rows are already in the cache at positions
+    ``L_b - n + j`` (``seq_lens[b]`` counts them), in node order. Node ``j``'s
+    query attends the committed context, positions ``0 .. L_b - n - 1``, and
+    the rows of the nodes on its own path (its ancestors and itself), and no
+    other draft token: a sibling branch is another candidate continuation.
+
+    TokenSpeed deep dive (wth2jhl.online), section 0 (the tree-speculation
+    design document) and the closing section (tree speculation as a serving
+    workload). The pages fix no mask; the ancestor mask above is the reading
+    listed in the design notes. A chain (``parents[j] = j - 1``) is causal
+    multi-token verification.
+
+    Args:
+        q: [B, n, H_q, D]; pools, block table as :func:`decode_attention`;
+        seq_lens: [B] context lengths including the n draft tokens (>= n);
+        parents: [B, n] integer array.
+
+    Returns:
+        (O [B, n, H_q, D] float64, LSE [B, n, H_q] float64).
+
+    Pinned by: the chain tree equal to :func:`multi_query_decode_attention`;
+    every node's row equal to :func:`decode_attention` over the context
+    followed by its path's rows, re-paged into fresh pages; torch's fp64
+    scaled_dot_product_attention with the explicit ancestor mask; rows
+    unchanged when rows off their path are overwritten; a planted causal
+    (sibling-visible) mask caught on a branching tree.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, n, H_q, D = q.shape
+    page_size, H_kv = k_pool.shape[1], k_pool.shape[2]
+    if H_q % H_kv != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
+    g = H_q // H_kv
+    Dv = v_pool.shape[3]
+    out = np.zeros((B, n, H_q, Dv), dtype=np.float64)
+    lse = np.full((B, n, H_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L < n:
+            raise ValueError("seq_lens must count the n draft tokens")
+        K = gather_sequence(k_pool, block_table[b], L, page_size).astype(np.float64)
+        V = gather_sequence(v_pool, block_table[b], L, page_size).astype(np.float64)
+        ctx = L - n
+        for j, path in enumerate(tree_ancestors(parents[b])):
+            keys = np.concatenate([np.arange(ctx), ctx + np.asarray(path, dtype=np.int64)])
+            for kh in range(H_kv):
+                heads = slice(kh * g, (kh + 1) * g)
+                scores = scale * (q[b, j, heads] @ K[keys, kh, :].T)
+                o, l = _softmax_attend(scores, V[keys, kh, :])
+                out[b, j, heads] = o
+                lse[b, j, heads] = l
+    return out, lse
+
+
 def mla_decode_attention(q, kv_pool, block_table, seq_lens, scale, d_v):
     """Absorbed-MLA decode: every query head attends one shared latent head.
 
@@ -260,6 +335,49 @@ def mla_decode_attention(q, kv_pool, block_table, seq_lens, scale, d_v):
         o, l = _softmax_attend(scores, C[:, :d_v])
         out[b] = o
         lse[b] = l
+    return out, lse
+
+
+def mla_multi_query_decode_attention(q, kv_pool, block_table, seq_lens, scale, d_v):
+    """Absorbed-MLA decode with ``q_len`` new query tokens per sequence.
+
+    Query token ``j`` of sequence ``b`` sits at position ``L_b - q_len + j``
+    (its latent row is already cached: ``seq_lens[b]`` counts the new tokens)
+    and, for every head, attends latent rows ``0 .. L_b - q_len + j``; each
+    (token, head) row is otherwise :func:`mla_decode_attention`.
+
+    TokenSpeed deep dive (wth2jhl.online), section 7, fig. 3 and 7.2: MLA
+    decode over ``q_seqlen`` query tokens, whose tokens are folded into the
+    head rows of a tile (``fold_sq_factor``); causal placement at the end of
+    the context is the same reading as :func:`multi_query_decode_attention`.
+
+    Args:
+        q: [B, q_len, H, Dqk]; kv_pool: [P, page_size, Dqk]; seq_lens >= q_len.
+
+    Returns:
+        (O [B, q_len, H, d_v] float64, LSE [B, q_len, H] float64).
+
+    Pinned by: q_len = 1 equal to :func:`mla_decode_attention`; every row
+    equal to :func:`mla_decode_attention` of that query over the shortened
+    context; torch's fp64 scaled_dot_product_attention with one kv head, a
+    value width of d_v and an explicit causal mask.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, q_len, H, Dqk = q.shape
+    page_size = kv_pool.shape[1]
+    out = np.zeros((B, q_len, H, d_v), dtype=np.float64)
+    lse = np.full((B, q_len, H), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L < q_len:
+            raise ValueError("seq_lens must count the q_len new tokens")
+        C = gather_sequence(kv_pool, block_table[b], L, page_size).astype(np.float64)
+        for j in range(q_len):
+            Lj = L - q_len + 1 + j
+            scores = scale * (q[b, j] @ C[:Lj].T)  # [H, Lj]
+            o, l = _softmax_attend(scores, C[:Lj, :d_v])
+            out[b, j] = o
+            lse[b, j] = l
     return out, lse
 
 

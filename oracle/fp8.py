@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import decode_attention
+from .attention import decode_attention, mla_decode_attention
 
 E4M3_MAX = 448.0
 SCALE_FLOOR = np.float32(1e-10)
@@ -129,3 +129,31 @@ def decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_l
     kd = dequantize(k_pool, k_scale).astype(np.float64)
     vd = dequantize(v_pool, v_scale).astype(np.float64)
     return decode_attention(q, kd, vd, block_table, seq_lens, scale)
+
+
+def mla_decode_attention_fp8(q_codes, q_scale, kv_codes, kv_scale, block_table, seq_lens, scale, d_v):
+    """Absorbed-MLA decode on the fp8 input path: attention (fp64) over the
+    page's float32 reconstruction of the query rows and the latent rows.
+
+    TokenSpeed deep dive (wth2jhl.online), section 1: the MLA decode kernel
+    takes bf16, fp16 or fp8 inputs. Reading (listed in the design notes): on
+    the fp8 path both inputs are e4m3fn codes with token-group scales by the
+    rule of tokenspeed 딥다이브 (fiv.co.kr), section 6-4, one group per row:
+    one float32 scale per (sequence, head) query row of 576 values and one
+    per cached latent row of 576 values. The values are the first ``d_v``
+    columns of the same reconstructed latent rows.
+
+    Args:
+        q_codes: uint8 [B, H, Dqk]; q_scale: float32 [B, H];
+        kv_codes: uint8 [P, page_size, Dqk]; kv_scale: float32 [P, page_size].
+
+    Returns:
+        (O [B, H, d_v] float64, LSE [B, H] float64).
+
+    Pinned by: equality with :func:`oracle.mla_decode_attention` on inputs
+    dequantized independently in the test (torch's float8_e4m3fn conversion),
+    and a planted mistake (the latent scale left out of the values) caught.
+    """
+    qd = dequantize(q_codes, q_scale).astype(np.float64)
+    cd = dequantize(kv_codes, kv_scale).astype(np.float64)
+    return mla_decode_attention(qd, cd, block_table, seq_lens, scale, d_v)
