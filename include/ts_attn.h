@@ -512,6 +512,42 @@ TS_API ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const i
                               size_t workspace_bytes, void* stream);
 
 /*
+ * ts_mla_multi_workspace_size - workspace bytes for ts_mla_paged_decode_multi
+ * (B sequences of q_len query tokens, H heads). 0 on invalid or unsupported
+ * arguments.
+ */
+TS_API size_t ts_mla_multi_workspace_size(int32_t B, int32_t q_len, int32_t H, int32_t D_v);
+
+/*
+ * ts_mla_paged_decode_multi - absorbed-MLA decode with q_len new query tokens
+ * per sequence (speculative or multi-token verification).
+ *
+ * TokenSpeed deep dive, section 7 fig. 3 and 7.2: decode over q_seqlen query
+ * tokens whose tokens are folded into the head rows of a 128-row tile,
+ * F = fold_sq_factor = the largest factor of q_len with H * F <= 128, so a
+ * tile holds F tokens x H heads and a sequence takes q_len / F tiles (64
+ * heads, 4 tokens: F = 2, two tiles). The new tokens' latent rows are already
+ * in the cache (seq_lens counts them): token j sits at position
+ * L - q_len + j and attends latent rows 0 .. L - q_len + j.
+ *
+ *   q        device bf16 [B, q_len, H, D_qk]
+ *   out      device bf16 [B, q_len, H, D_v];  lse device float32 [B, q_len, H] or NULL
+ *   workspace >= ts_mla_multi_workspace_size(B, q_len, H, D_v)
+ *   other arguments as ts_mla_paged_decode. A sequence with L < q_len gives
+ *   O = 0 and LSE = -inf for the rows that see no key.
+ * Supported: H * F == 128 (H = 128 with any q_len; 64 with even q_len; 32
+ * with q_len a multiple of 4, ...), D_qk == 576, D_v == 512, page_size 64,
+ * bf16; otherwise TS_ERR_UNSUPPORTED. q_len == 1 with H == 128 is
+ * ts_mla_paged_decode.
+ */
+TS_API ts_status ts_mla_paged_decode_multi(const void* q, const void* kv_pool, const int32_t* block_table,
+                                           int32_t bt_stride, const int32_t* seq_lens, int32_t B,
+                                           int32_t q_len, int32_t H, int32_t D_qk, int32_t D_v,
+                                           int32_t page_size, int32_t num_pages, float scale, void* out,
+                                           float* lse, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/*
  * ts_read_device_error - copy the sticky error word of an attention
  * workspace to *error_bits (synchronises the stream). workspace == NULL
  * reads the error word of ts_paged_decode_attn_noalloc's static scratch on

@@ -112,6 +112,9 @@ _SIGNATURES = {
     "ts_mla_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "ts_mla_paged_decode": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _I32,
                                            _F32, _VP, _VP, _VP, _SZ, _VP]),
+    "ts_mla_multi_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "ts_mla_paged_decode_multi": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _I32,
+                                                 _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_read_device_error": (ctypes.c_int, [_VP, _U32P, _VP]),
     "ts_trace_enable": (ctypes.c_int, [_I32]),
     "ts_trace_collect": (_I32, [ctypes.POINTER(LaunchRecordC), _I32]),
@@ -509,6 +512,30 @@ def ts_mla_paged_decode(q, kv_pool, block_table, seq_lens, scale: float, d_v: in
                                      _ptr(seq_lens), B, H, Dqk, d_v, ps, P, float(scale), _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def ts_mla_multi_workspace_size(B: int, q_len: int, H: int, D_v: int) -> int:
+    return int(lib().ts_mla_multi_workspace_size(B, q_len, H, D_v))
+
+
+def ts_mla_paged_decode_multi(q, kv_pool, block_table, seq_lens, scale: float, d_v: int = 512, out=None,
+                              lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Absorbed-MLA decode of q_len tokens per sequence: q [B, q_len, H, Dqk] bf16,
+    kv_pool [P, ps, Dqk] bf16 -> out [B, q_len, H, d_v]."""
+    _require_i32(block_table, seq_lens)
+    B, q_len, H, Dqk = q.shape
+    P, ps, _ = kv_pool.shape
+    if out is None:
+        out = torch.empty(B, q_len, H, d_v, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(B, q_len, H, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(ts_mla_multi_workspace_size(B, q_len, H, d_v), q.device)
+    _check(lib().ts_mla_paged_decode_multi(_ptr(q), _ptr(kv_pool), _ptr(block_table), block_table.shape[1],
+                                           _ptr(seq_lens), B, q_len, H, Dqk, d_v, ps, P, float(scale), _ptr(out),
+                                           _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
     return (out, lse) if return_lse else out
 
 

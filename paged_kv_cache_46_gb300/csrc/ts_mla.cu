@@ -27,6 +27,15 @@
 // Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
 // allocator, warps 4-11 softmax / epilogue (one head row and half of the
 // tile's tokens per thread). Four K/V stages keep three pages in flight.
+//
+// Several query tokens per sequence (section 7.2, fold_sq_factor): with H
+// heads and q_len tokens, F = the largest factor of q_len with H * F <= 128
+// tokens are folded into the 128 rows of a tile (row r = token r / H of the
+// step, head r % H), and the q_len / F steps of a sequence are separate
+// "virtual sequences" of the cut. With q laid out [B, q_len, H, 576], the
+// rows of virtual sequence v are the contiguous rows v * 128 .. v * 128 + 127,
+// and likewise for O and LSE. Row r of step st attends keys up to
+// L - q_len + st * F + r / H (causal among the new tokens).
 #include <cmath>
 
 #include "ts_tcgen05.cuh"
@@ -70,17 +79,26 @@ struct MlaParams {
   int2* split_info;         // per sequence: {first pair, (parts << 1) | slot of first part}
   float* part_o;            // [2 * pairs, 128, 512]
   float* part_lse;          // [2 * pairs, 128]
+  // query tokens per sequence, tokens folded per tile, steps = q_len / fold,
+  // log2 of the head count (B above counts virtual sequences: B_seq * steps)
+  int32_t q_len, fold, steps, h_shift;
 };
 
+// Context length of virtual sequence v (the length of its sequence).
+__device__ __forceinline__ int vlen(const int32_t* lens, int steps, int v) {
+  return max(lens[steps == 1 ? v : v / steps], 0);
+}
+
 struct Tile {
-  int b, pidx, valid, out_slot;
+  int b, pidx, rem, out_slot;  // rem: the sequence's tokens from this tile's first on
   bool first, last;
+  __device__ int valid() const { return min(rem, kTok); }
 };
 
 // Deterministic walk over a cluster's page range (identical in every role).
 struct Walker {
   const int32_t* lens;
-  int B, k;
+  int B, k, steps;
   long long g, end, q_pages, r_pages, total;
   int b, pg, np, L, seg_left, out_slot;
   bool first_seg;
@@ -89,6 +107,7 @@ struct Walker {
                        long long qp, long long rp, long long tot) {
     lens = p.seq_lens;
     B = p.B;
+    steps = p.steps;
     k = k_;
     g = start;
     end = end_;
@@ -104,7 +123,7 @@ struct Walker {
     if (b >= 0 && b < B) load();
   }
   __device__ void load() {
-    L = max(lens[b], 0);
+    L = vlen(lens, steps, b);
     np = (L + kPS - 1) / kPS;
   }
   // Next tile; false at the end of the range. `n_here` and the sequence's
@@ -131,7 +150,7 @@ struct Walker {
     }
     t.b = b;
     t.pidx = pg;
-    t.valid = (pg == np - 1) ? (L - pg * kPS) : kPS;
+    t.rem = L - pg * kPS;
     t.out_slot = out_slot;
     t.last = (seg_left == 1);
     ++g;
@@ -198,15 +217,28 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   const int chunk = (B + kThreadsMla - 1) / kThreadsMla;
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
   long long mine = 0;
+  bool has_empty = false;
   for (int b = lo; b < hi; ++b) {
-    const int L = p.seq_lens[b];
-    if (L > 0) {
+    const int L = vlen(p.seq_lens, p.steps, b);
+    if (L > 0)
       mine += (L + kPS - 1) / kPS;
-    } else if (b % n_pairs == pair && rank == 0) {
-      for (int i = 0; i < kH * kDv; ++i) p.out[static_cast<int64_t>(b) * kH * kDv + i] = __float2bfloat16(0.f);
+    else if (b % n_pairs == pair && rank == 0)
+      has_empty = true;
+  }
+  // Sequences with no tokens: O = 0, LSE = -inf, each written by a whole warp
+  // (the lanes that found some hand their range to the warp in turn).
+  unsigned todo = __ballot_sync(0xffffffffu, has_empty);
+  while (todo != 0u) {
+    const int src = __ffs(todo) - 1;
+    todo &= todo - 1u;
+    const int slo = __shfl_sync(0xffffffffu, lo, src), shi = __shfl_sync(0xffffffffu, hi, src);
+    for (int b = slo; b < shi; ++b) {
+      if (vlen(p.seq_lens, p.steps, b) > 0 || b % n_pairs != pair) continue;
+      uint4* o4 = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(b) * kH * kDv);
+      for (int i = lane; i < kH * kDv / 8; i += 32) o4[i] = make_uint4(0u, 0u, 0u, 0u);
       if (p.lse)
-        for (int h = 0; h < kH; ++h) p.lse[static_cast<int64_t>(b) * kH + h] = -INFINITY;
-      p.split_info[b] = make_int2(pair, 0);
+        for (int h = lane; h < kH; h += 32) p.lse[static_cast<int64_t>(b) * kH + h] = -INFINITY;
+      if (lane == 0) p.split_info[b] = make_int2(pair, 0);
     }
   }
   long long incl = mine;
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
     for (int b = lo; b < hi; ++b) {
-      const int L = p.seq_lens[b];
+      const int L = vlen(p.seq_lens, p.steps, b);
       const long long np = L > 0 ? (L + kPS - 1) / kPS : 0;
       if (start < off + np) {
         s_start[0] = b;
@@ -256,7 +288,9 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     int n_here = 0;
     long long first_pg = 0;
     auto page_of = [&](const Tile& x) {
-      return x.pidx < p.bt_stride ? p.block_table[static_cast<int64_t>(x.b) * p.bt_stride + x.pidx] : -1;
+      // the block table has one row per sequence, not per virtual sequence
+      const int seq = p.steps == 1 ? x.b : x.b / p.steps;
+      return x.pidx < p.bt_stride ? p.block_table[static_cast<int64_t>(seq) * p.bt_stride + x.pidx] : -1;
     };
     // the page id of the next tile is loaded one tile ahead
     Walker wa = w;
@@ -498,10 +532,14 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         s[4 * c + 3] = mine[4 * c + 3] + o.w;
       }
       if (has_nxt && !send_next(j + 1, has_nn && nn.first, nn.b)) { ok = false; break; }
+      // keys of this tile the row may see: the sequence's valid rows, and with
+      // several query tokens only those up to the row's own position
+      int lim = cur.rem;
+      if (p.q_len > 1) lim -= p.q_len - 1 - ((cur.b % p.steps) * p.fold + (h >> p.h_shift));
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kTokHalf; ++c) {
-        s[c] = hf * kTokHalf + c < cur.valid ? s[c] * p.scale_log2 : -INFINITY;
+        s[c] = hf * kTokHalf + c < lim ? s[c] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[c]);
       }
       {
@@ -550,15 +588,16 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       }
       tmem_wait_st();
       l += ls;
-      if (cur.valid < kTok) {
+      const int valid = cur.valid();
+      if (valid < kTok) {
         // rows past the sequence's end hold whatever the pool has there (NaN
         // sentinels included): zero them so 0-weight rows stay 0 in P V
         const int sj = j % kStages;
         ok = mbar_wait(bar(sj), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         unsigned char* st = smem + kOffStages + sj * kStageBytes;
-        for (int i = sw * 32 + lane; i < (kTok - cur.valid) * 4 * 8; i += 8 * 32) {
-          const int row = cur.valid + i / 32, a = (i / 8) & 3, c = i & 7;
+        for (int i = sw * 32 + lane; i < (kTok - valid) * 4 * 8; i += 8 * 32) {
+          const int row = valid + i / 32, a = (i / 8) & 3, c = i & 7;
           *reinterpret_cast<uint4*>(st + a * kAtomBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();  // each warp's zeros reach the MMA before its p_full arrive
@@ -668,24 +707,34 @@ int mla_pairs() {
 }  // namespace
 }  // namespace ts
 
-extern "C" size_t ts_mla_workspace_size(int32_t B, int32_t H, int32_t D_v) {
-  const int pairs = ts::mla_pairs();
-  if (B < 0 || H != ts::kH || D_v != ts::kDv || pairs <= 0) return 0;
-  return ts::mla_layout(B, pairs).total;
+namespace ts {
+namespace {
+
+// Tokens folded into the 128 rows of a tile (TokenSpeed deep dive, section
+// 7.2): the largest F with q_len % F == 0 and H * F <= 128. 0 if H * F != 128
+// (the kernel needs full tiles).
+int mla_fold(int H, int q_len) {
+  if (H <= 0 || q_len <= 0 || H > kH) return 0;
+  int best = 1;
+  for (int f = 1; f <= q_len; ++f)
+    if (q_len % f == 0 && H * f <= kH) best = f;
+  return H * best == kH ? best : 0;
 }
 
-extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const int32_t* block_table,
-                                         int32_t bt_stride, const int32_t* seq_lens, int32_t B,
-                                         int32_t H, int32_t D_qk, int32_t D_v, int32_t page_size,
-                                         int32_t num_pages, float scale, void* out, float* lse,
-                                         void* workspace, size_t workspace_bytes, void* stream) {
-  using namespace ts;
-  const char* who = "ts_mla_paged_decode";
-  if (B < 0 || num_pages <= 0 || bt_stride <= 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
-    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d P=%d bt=%d)", who, B, num_pages, bt_stride);
-  if (H != kH || D_qk != kDqk || D_v != kDv || page_size != kPS)
-    return fail(TS_ERR_UNSUPPORTED, "%s: needs H=128, D_qk=576, D_v=512, page_size=64 (got %d, %d, %d, %d)",
-                who, H, D_qk, D_v, page_size);
+ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_table, int32_t bt_stride,
+                     const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H, int32_t D_qk,
+                     int32_t D_v, int32_t page_size, int32_t num_pages, float scale, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+  if (B < 0 || q_len < 1 || num_pages <= 0 || bt_stride <= 0 ||
+      static_cast<long long>(num_pages) * page_size > INT32_MAX ||
+      static_cast<long long>(B) * q_len > INT32_MAX / kH)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d q_len=%d P=%d bt=%d)", who, B, q_len, num_pages,
+                bt_stride);
+  const int fold = mla_fold(H, q_len);
+  if (fold == 0 || D_qk != kDqk || D_v != kDv || page_size != kPS)
+    return fail(TS_ERR_UNSUPPORTED,
+                "%s: needs H * fold_sq_factor(H, q_len) == 128 (H=%d, q_len=%d), D_qk=576, D_v=512, "
+                "page_size=64 (got %d, %d, %d)", who, H, q_len, D_qk, D_v, page_size);
   if (!std::isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "%s: scale not finite", who);
   if (B == 0) return TS_OK;
   if (!q || !kv_pool || !block_table || !seq_lens || !out)
@@ -693,9 +742,11 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   for (const void* ptr : {q, kv_pool, static_cast<const void*>(out)})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
       return fail(TS_ERR_INVALID_ARG, "%s: q, kv_pool and out must be 16-byte aligned", who);
+  const int steps = q_len / fold;
+  const int Bv = B * steps;
   const int pairs = mla_pairs();
   if (pairs <= 0) return fail(TS_ERR_CUDA, "%s: cannot query the SM count", who);
-  const MlaWs ws = mla_layout(B, pairs);
+  const MlaWs ws = mla_layout(Bv, pairs);
   if (!workspace || workspace_bytes < ws.total)
     return fail(TS_ERR_WORKSPACE, "%s: workspace %zu B < %zu B needed", who, workspace_bytes, ws.total);
   if (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
@@ -717,7 +768,7 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.bt_stride = bt_stride;
-  prm.B = B;
+  prm.B = Bv;
   prm.num_pages = num_pages;
   prm.scale_log2 = scale * kLog2eM;
   prm.out = static_cast<__nv_bfloat16*>(out);
@@ -727,6 +778,12 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
   prm.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  prm.q_len = q_len;
+  prm.fold = fold;
+  prm.steps = steps;
+  int h_shift = 0;
+  while ((1 << h_shift) < H) ++h_shift;
+  prm.h_shift = h_shift;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ts_status st = prepare_once(reinterpret_cast<const void*>(mla_decode_kernel), [](const void* k) {
@@ -755,7 +812,7 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pattr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t mcfg = {};
-  const long long warps = static_cast<long long>(B) * kH;
+  const long long warps = static_cast<long long>(Bv) * kH;
   mcfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
   mcfg.blockDim = dim3(256);
   mcfg.stream = s;
@@ -763,4 +820,46 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   mcfg.numAttrs = 1;
   LaunchTrace trace("mla_merge_kernel", s);
   return cuda_check(cudaLaunchKernelEx(&mcfg, mla_merge_kernel, prm), "mla merge launch");
+}
+
+}  // namespace
+}  // namespace ts
+
+extern "C" size_t ts_mla_workspace_size(int32_t B, int32_t H, int32_t D_v) {
+  const int pairs = ts::mla_pairs();
+  if (B < 0 || H != ts::kH || D_v != ts::kDv || pairs <= 0) return 0;
+  return ts::mla_layout(B, pairs).total;
+}
+
+extern "C" size_t ts_mla_multi_workspace_size(int32_t B, int32_t q_len, int32_t H, int32_t D_v) {
+  const int pairs = ts::mla_pairs();
+  const int fold = ts::mla_fold(H, q_len);
+  if (B < 0 || fold == 0 || D_v != ts::kDv || pairs <= 0 ||
+      static_cast<long long>(B) * q_len > INT32_MAX / ts::kH)
+    return 0;
+  return ts::mla_layout(B * (q_len / fold), pairs).total;
+}
+
+extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, const int32_t* block_table,
+                                         int32_t bt_stride, const int32_t* seq_lens, int32_t B,
+                                         int32_t H, int32_t D_qk, int32_t D_v, int32_t page_size,
+                                         int32_t num_pages, float scale, void* out, float* lse,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "ts_mla_paged_decode";
+  if (H != ts::kH)
+    return ts::fail(TS_ERR_UNSUPPORTED, "%s: needs H=128 (got %d); ts_mla_paged_decode_multi folds "
+                    "fewer heads", who, H);
+  return ts::mla_launch(q, kv_pool, block_table, bt_stride, seq_lens, B, 1, H, D_qk, D_v, page_size,
+                        num_pages, scale, out, lse, workspace, workspace_bytes, stream, who);
+}
+
+extern "C" ts_status ts_mla_paged_decode_multi(const void* q, const void* kv_pool, const int32_t* block_table,
+                                               int32_t bt_stride, const int32_t* seq_lens, int32_t B,
+                                               int32_t q_len, int32_t H, int32_t D_qk, int32_t D_v,
+                                               int32_t page_size, int32_t num_pages, float scale, void* out,
+                                               float* lse, void* workspace, size_t workspace_bytes,
+                                               void* stream) {
+  return ts::mla_launch(q, kv_pool, block_table, bt_stride, seq_lens, B, q_len, H, D_qk, D_v, page_size,
+                        num_pages, scale, out, lse, workspace, workspace_bytes, stream,
+                        "ts_mla_paged_decode_multi");
 }

@@ -80,7 +80,7 @@ def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, dtype):
     o_ref, l_ref = _oracle(case)
     for ctas, path in ((None, "tensor"), (None, "cuda"), (5, "cuda")):
         out, lse = _run(case, q_len, ctas, path)
-        compare(out, o_ref, dtype, lse, l_ref, f"q_len={q_len} {H_q}/{H_kv} D={D} {dtype} ctas={ctas} path={path}")
+        compare(out, o_ref, dtype, lse, l_ref, f"q_len={q_len} {H_q}/{H_kv} D={D} {dtype} ctas={ctas} path={path}", margin=0.8 if dtype == "bf16" else 1.0)
 
 
 @pytest.mark.parametrize("ctas", [1, 7, None, 1000])
@@ -89,7 +89,7 @@ def test_multi_query_independent_of_split_pattern(ctas):
     case = _case("mq_split", 71, lens, 4)
     out, lse = _run(case, 4, ctas, "cuda")
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, f"ctas={ctas}")
+    compare(out, o_ref, "bf16", lse, l_ref, f"ctas={ctas}", margin=0.8)
 
 
 def test_q_len_one_equals_single_query_decode():
@@ -113,7 +113,7 @@ def test_full_llama_shape_with_two_draft_tokens():
     o_ref, l_ref = _oracle(case)
     for path in ("tensor", "cuda"):
         out, lse = _run(case, 2, path=path)
-        compare(out, o_ref, "bf16", lse, l_ref, f"llama shape q_len=2 path={path}")
+        compare(out, o_ref, "bf16", lse, l_ref, f"llama shape q_len=2 path={path}", margin=0.8)
 
 
 @pytest.mark.parametrize("q_len,H_q,H_kv,D,hg", [
@@ -131,7 +131,7 @@ def test_tensor_core_path_shapes(q_len, H_q, H_kv, D, hg):
     case = _case(f"mq_tc_{q_len}_{H_q}_{H_kv}_{D}", 91 + q_len, lens, q_len, H_q, H_kv, D)
     out, lse = _run(case, q_len, path="tensor", hg=hg)
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D} hg={hg}")
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc q_len={q_len} {H_q}/{H_kv} D={D} hg={hg}", margin=0.8)
 
 
 @pytest.mark.parametrize("B,hg", [(40, 1), (40, 4), (129, 2), (300, 2)])
@@ -148,7 +148,7 @@ def test_tensor_core_path_work_order(B, hg):
     case = _case(f"mq_tc_order_{B}", 300 + B, lens, 4)
     out, lse = _run(case, 4, path="tensor", hg=hg)
     o_ref, l_ref = _oracle(case)
-    compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B} hg={hg}")
+    compare(out, o_ref, "bf16", lse, l_ref, f"tc work order B={B} hg={hg}", margin=0.8)
 
 
 def test_full_speculative_verify_four_tokens_sampled():
@@ -163,4 +163,4 @@ def test_full_speculative_verify_four_tokens_sampled():
     o_ref, l_ref = oracle.multi_query_decode_attention(v["q"], v["k_pool"], v["v_pool"], v["block_table"],
                                                        v["seq_lens"], case.scale)
     dev_idx = torch.from_numpy(idx).to(DEV)
-    compare(out[dev_idx], o_ref, "bf16", lse[dev_idx], l_ref, "speculative verify q4 full sample")
+    compare(out[dev_idx], o_ref, "bf16", lse[dev_idx], l_ref, "speculative verify q4 full sample", margin=0.8)

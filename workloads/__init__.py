@@ -427,6 +427,19 @@ def absorbed_mla(device="cpu", seed: int = 5, B: int = 64, lo: int = 8192,
                       mla=True, device=device, rng=rng)
 
 
+def absorbed_mla_multi(device="cpu", seed: int = 9, B: int = 64, H: int = 64, q_len: int = 4,
+                       lo: int = 8192, hi: int = 50000) -> PagedCase:
+    """Absorbed-MLA decode verifying q_len draft tokens per sequence with H
+    heads (the fold example's 64 heads x 4 tokens by default): latent 576
+    (V = first 512), bf16, page 64, lens ~ U[lo, hi] counting the draft
+    tokens, scale 1/sqrt(192)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_case(f"absorbed_mla_B{B}_H{H}_q{q_len}", seed, B=B, H_q=H, H_kv=1, D=576, Dv=512,
+                      page_size=64, seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(192),
+                      mla=True, device=device, rng=rng, q_len=q_len)
+
+
 # --------------------------------------------------------------------------
 # Moving inputs to the oracle (data movement only)
 # --------------------------------------------------------------------------
