@@ -77,6 +77,9 @@ typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
 /* A kernel found its dynamic shared memory not aligned as its tile layout
  * needs (1024 bytes) and returned without computing anything. */
 #define TS_DEVERR_SMEM_ALIGN 0x4u
+/* A draft tree's parent index was not an earlier node or -1: the row's path
+ * stops there (ts_paged_decode_tree_attn). */
+#define TS_DEVERR_TREE 0x8u
 
 /* Human-readable name of a status code. Never NULL. */
 TS_API const char* ts_status_string(int status);
@@ -271,6 +274,40 @@ TS_API ts_status ts_paged_decode_multi_attn(const void* q, const void* k_pool, c
                                             int32_t num_pages, float scale, ts_dtype dtype, void* out,
                                             float* lse, void* workspace, size_t workspace_bytes,
                                             void* stream);
+
+/*
+ * ts_paged_decode_tree_attn - verify a tree of draft tokens in one decode
+ * step (tree speculation).
+ *
+ * TokenSpeed deep dive, section 0 (the tree-speculation design document) and
+ * its closing section (tree speculation as a serving workload). Each
+ * sequence brings n draft tokens that form a tree: parents[b, j] is token j's
+ * parent, an earlier token (< j) or -1 for a child of the last committed
+ * token. Their K/V rows are already in the cache at positions L - n + j, in
+ * token order (seq_lens counts them). Token j's query, for every query head,
+ * attends the committed context (positions 0 .. L - n - 1) and the draft
+ * tokens on its own path (its ancestors and itself), not its siblings'
+ * branches. A chain (parents[j] = j - 1) gives ts_paged_decode_multi_attn's
+ * causal result.
+ *
+ *   q        device bf16 [B, n, H_q, D];  out device bf16 [B, n, H_q, D]
+ *   lse      device float32 [B, n, H_q] or NULL
+ *   parents  device int32 [B, n]; a parent that is not -1 or an earlier token
+ *            sets TS_DEVERR_TREE and ends that row's path there
+ *   workspace >= 256 bytes, 256-byte aligned (its first 4 bytes are the
+ *            error word; zero it to check it later)
+ *   other arguments as ts_paged_decode_attn.
+ * Supported (tensor-core path): bf16, page_size 16, D 64 or 128, 1 <= n <= 64,
+ * n * H_q / H_kv <= 128; otherwise TS_ERR_UNSUPPORTED with nothing enqueued.
+ * A sequence with L < n attends only the rows that exist (L >= n expected).
+ */
+TS_API ts_status ts_paged_decode_tree_attn(const void* q, const void* k_pool, const void* v_pool,
+                                           const int32_t* block_table, int32_t bt_stride,
+                                           const int32_t* seq_lens, const int32_t* parents, int32_t B,
+                                           int32_t n, int32_t H_q, int32_t H_kv, int32_t D,
+                                           int32_t page_size, int32_t num_pages, float scale,
+                                           ts_dtype dtype, void* out, float* lse, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /*
  * ts_kv_append_fp8 - quantize one new token's K and V per sequence into an

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(HERE, "libts_attn.so")
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_WORKSPACE, TS_ERR_CUDA, TS_ERR_CAPACITY = range(6)
 TS_F32, TS_BF16 = 0, 1
-TS_DEVERR_PAGE_RANGE, TS_DEVERR_TIMEOUT, TS_DEVERR_SMEM_ALIGN = 0x1, 0x2, 0x4
+TS_DEVERR_PAGE_RANGE, TS_DEVERR_TIMEOUT, TS_DEVERR_SMEM_ALIGN, TS_DEVERR_TREE = 0x1, 0x2, 0x4, 0x8
 TS_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # include/ts_attn.h
 
 
@@ -115,6 +115,8 @@ _SIGNATURES = {
     "ts_mla_multi_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "ts_mla_paged_decode_multi": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _I32,
                                                  _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
+    "ts_paged_decode_tree_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _I32,
+                                                 _I32, _I32, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_read_device_error": (ctypes.c_int, [_VP, _U32P, _VP]),
     "ts_trace_enable": (ctypes.c_int, [_I32]),
     "ts_trace_collect": (_I32, [ctypes.POINTER(LaunchRecordC), _I32]),
@@ -512,6 +514,26 @@ def ts_mla_paged_decode(q, kv_pool, block_table, seq_lens, scale: float, d_v: in
                                      _ptr(seq_lens), B, H, Dqk, d_v, ps, P, float(scale), _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def ts_paged_decode_tree_attn(q, k_pool, v_pool, block_table, seq_lens, parents, scale: float, out=None,
+                              lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Tree verification: q [B, n, H_q, D] bf16, parents int32 [B, n] (-1 or an
+    earlier draft token) -> out [B, n, H_q, D]."""
+    _require_i32(block_table, seq_lens, parents)
+    B, n, H_q, D = q.shape
+    P, ps, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, n, H_q, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(256, q.device)
+    _check(lib().ts_paged_decode_tree_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                           block_table.shape[1], _ptr(seq_lens), _ptr(parents), B, n, H_q, H_kv, D,
+                                           ps, P, float(scale), _dt(q), _ptr(out), _ptr(lse), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
     return (out, lse) if return_lse else out
 
 

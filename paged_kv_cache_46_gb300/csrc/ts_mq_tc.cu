@@ -23,6 +23,13 @@
 // operand). K and V tiles sit in a 3-stage ring. At D = 128 the K, V and Q
 // tiles are two 64-column atoms each, and one N = 128 product reads both of
 // V's atoms.
+//
+// Tree verification (TokenSpeed deep dive, section 0: tree speculation): with
+// a parents array the q_len draft tokens form a tree, and the row of token j
+// sees the context (keys before L - q_len) and the draft keys of its own
+// path from the context down to itself. Each row walks its path once, in a
+// shared-memory copy of its sequence's parents, into a 64-bit mask; only the
+// key tiles that hold draft keys test it.
 #include <cmath>
 #include <cstdlib>
 
@@ -47,6 +54,8 @@ constexpr float kSlack = 8.0f;
 // Up to this many sequences the CTAs take them longest first (each CTA ranks
 // the key-tile counts itself, B^2 / 192 comparisons per thread).
 constexpr int kLongestFirstMaxB = 128;
+// Draft tokens of a verified tree: one bit per token in a row's mask.
+constexpr int kMaxTree = 64;
 
 template <int kHD>
 struct Layout {
@@ -56,7 +65,8 @@ struct Layout {
   static constexpr int kOffV = kOffK + kStages * kAtoms * kAtom;
   static constexpr int kOffBar = kOffV + kStages * kAtoms * kAtom;
   static constexpr int kOffTmem = kOffBar + 256;
-  static constexpr int kSmem = kOffTmem + 16;
+  static constexpr int kOffPar = kOffTmem + 16;             // tree: the sequence's parents
+  static constexpr int kSmem = kOffPar + kMaxTree * 4;
   static constexpr uint32_t kTmemO = 128;
   // two P buffers of 64 columns (bf16 pairs: key k of row r at column k/2):
   // the softmax writes P(j+1) while P V(j) still reads P(j)
@@ -71,6 +81,7 @@ struct MqParams {
   float* lse;                   // [B, q_len, H_q] or nullptr
   const int32_t* block_table;   // [B, bt_stride]
   const int32_t* seq_lens;      // [B], counting the q_len new tokens
+  const int32_t* parents;       // [B, q_len] draft-tree parents, or nullptr (causal)
   int32_t B, bt_stride, q_len, H_q, H_kv, g, num_pages;
   float scale_log2;
   uint32_t* err_word;
@@ -229,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
       }
     }
     fence_async_smem();
+    if (p.parents != nullptr && tid < p.q_len)
+      reinterpret_cast<int*>(smem + Lay::kOffPar)[tid] = p.parents[static_cast<int64_t>(b) * p.q_len + tid];
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
   tc_fence_before();
@@ -336,7 +349,25 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const uint32_t hcol = static_cast<uint32_t>(hs * kPS);
     const int jt = r / p.g;                            // this row's token
-    const int lim = r < R ? L - p.q_len + 1 + jt : 0;  // keys it may attend (padding: none)
+    const int ctx = L - p.q_len;                       // keys before the new tokens
+    const bool tree = p.parents != nullptr;
+    // keys below lim are visible (padding rows: none); with a tree, draft key
+    // ctx + i is visible when bit i of anc is set (i on this row's path)
+    const int lim = r >= R ? 0 : (tree ? ctx : ctx + 1 + jt);
+    unsigned long long anc = 0ull;
+    if (tree && r < R) {
+      const int* par = reinterpret_cast<const int*>(smem + Lay::kOffPar);
+      int a = jt;
+      for (int step = 0; step < p.q_len && a >= 0; ++step) {
+        anc |= 1ull << a;
+        const int up = par[a];
+        if (up >= a || up < -1) {  // not an earlier node: the path stops here
+          set_device_error(p.err_word, TS_DEVERR_TREE);
+          break;
+        }
+        a = up;
+      }
+    }
     // l: the row sum of exp2(s - m) for the LSE; lr: the same over P as
     // rounded to bf16 for the product, which normalises O, so that the
     // weights the product applied sum to one
@@ -379,10 +410,20 @@ __global__ void __launch_bounds__(kThreads, Layout<kHD>::kMinBlocks) mq_tc_kerne
         // causal limit of its token); the scale is folded into the exponent
         const float sl = p.scale_log2;
         float mx = -INFINITY;
+        if (tree && key0 + kKeys > ctx) {  // a tile holding draft keys (same for every row)
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          s[c] = key0 + c < lim ? s[c] * sl : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < kKeys; ++c) {
+            const int k = key0 + c, d = k - ctx;
+            const bool vis = k < lim || (d >= 0 && k < L && ((anc >> (d & 63)) & 1ull) != 0ull);
+            s[c] = vis ? s[c] * sl : -INFINITY;
+            mx = fmaxf(mx, s[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) {
+            s[c] = key0 + c < lim ? s[c] * sl : -INFINITY;
+            mx = fmaxf(mx, s[c]);
+          }
         }
         const bool need = mx > m + kSlack;
         if (j == 0) {
@@ -562,10 +603,11 @@ ts_status launch(const MqParams& prm, const CUtensorMap& kmap, const CUtensorMap
 ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                                 int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
                                 int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
-                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream) {
+                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream,
+                                const int32_t* parents) {
   const int g = H_q / H_kv;
   if (dtype != TS_BF16 || page_size != kPS || (D != 64 && D != 128) || q_len < 1 || q_len * g > kBM ||
-      static_cast<int64_t>(B) * H_kv > 0x7fffffff)
+      static_cast<int64_t>(B) * H_kv > 0x7fffffff || (parents != nullptr && q_len > kMaxTree))
     return TS_ERR_UNSUPPORTED;
   MqParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -573,6 +615,7 @@ ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v
   prm.lse = lse;
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
+  prm.parents = parents;
   prm.B = B;
   prm.bt_stride = bt_stride;
   prm.q_len = q_len;

@@ -185,7 +185,8 @@ ts_status launch_fp8_decode_tc(const void* q, const void* k_pool, const void* v_
 ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                                 int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
                                 int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
-                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream);
+                                ts_dtype dtype, void* out, float* lse, uint32_t* err_word, cudaStream_t stream,
+                                const int32_t* parents);
 
 // Group scales of an fp8 (e4m3fn) cache, [num_pages, page_size, H_kv] each.
 struct Fp8Scales {
@@ -534,13 +535,49 @@ extern "C" ts_status ts_paged_decode_multi_attn(const void* q, const void* k_poo
     const ts_status st = ts::launch_multi_query_tc(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, q_len,
                                                    H_q, H_kv, D, page_size, num_pages, scale, dtype, out, lse,
                                                    static_cast<uint32_t*>(workspace),
-                                                   static_cast<cudaStream_t>(stream));
+                                                   static_cast<cudaStream_t>(stream), nullptr);
     if (st != TS_ERR_UNSUPPORTED) return st;
   }
   return ts::paged_decode_core(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, q_len, H_q,
                                H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                workspace_bytes, static_cast<cudaStream_t>(stream),
                                "ts_paged_decode_multi_attn", nullptr);
+}
+
+extern "C" ts_status ts_paged_decode_tree_attn(const void* q, const void* k_pool, const void* v_pool,
+                                               const int32_t* block_table, int32_t bt_stride,
+                                               const int32_t* seq_lens, const int32_t* parents, int32_t B,
+                                               int32_t n, int32_t H_q, int32_t H_kv, int32_t D,
+                                               int32_t page_size, int32_t num_pages, float scale,
+                                               ts_dtype dtype, void* out, float* lse, void* workspace,
+                                               size_t workspace_bytes, void* stream) {
+  using namespace ts;
+  const char* who = "ts_paged_decode_tree_attn";
+  if (B < 0 || n < 1 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || num_pages <= 0 || bt_stride <= 0 ||
+      H_q % H_kv != 0 || static_cast<long long>(num_pages) * page_size > INT32_MAX)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad sizes (B=%d n=%d H_q=%d H_kv=%d D=%d ps=%d P=%d bt=%d)", who, B, n,
+                H_q, H_kv, D, page_size, num_pages, bt_stride);
+  if (dtype != TS_F32 && dtype != TS_BF16)
+    return fail(TS_ERR_INVALID_ARG, "%s: bad dtype %d", who, static_cast<int>(dtype));
+  if (!std::isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "%s: scale not finite", who);
+  if (B == 0) return TS_OK;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !parents || !out)
+    return fail(TS_ERR_INVALID_ARG, "%s: null pointer", who);
+  for (const void* ptr : {q, k_pool, v_pool, static_cast<const void*>(out)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+      return fail(TS_ERR_INVALID_ARG, "%s: q, pools and out must be 16-byte aligned", who);
+  if (!workspace || workspace_bytes < kWorkspaceAlign ||
+      reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
+    return fail(TS_ERR_WORKSPACE, "%s: workspace of >= 256 bytes, 256-byte aligned, needed", who);
+  const ts_status st = launch_multi_query_tc(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, n, H_q, H_kv,
+                                             D, page_size, num_pages, scale, dtype, out, lse,
+                                             static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream),
+                                             parents);
+  if (st == TS_ERR_UNSUPPORTED)
+    return fail(TS_ERR_UNSUPPORTED, "%s: needs bf16, page_size 16, D 64/128, n <= 64, n * H_q / H_kv <= 128 "
+                "(got dtype %d, ps %d, D %d, n %d, g %d)", who, static_cast<int>(dtype), page_size, D, n,
+                H_q / H_kv);
+  return st;
 }
 
 extern "C" int32_t ts_fold_sq_factor(int32_t num_heads, int32_t q_len, int32_t tile_rows) {

@@ -356,6 +356,40 @@ def speculative_verify(device="cpu", seed: int = 6, B: int = 64, q_len: int = 4,
                       device=device, rng=rng, q_len=q_len)
 
 
+def draft_trees(B: int, n: int, rng: np.random.Generator, shape: str = "random") -> np.ndarray:
+    """Parents [B, n] (int32) of B draft-token trees: node j's parent is an
+    earlier node or -1 (a child of the last committed token).
+
+    "random": each node hangs under a uniformly drawn earlier node or the
+    context; "chain": a single causal chain; "star": every node under the
+    context; "beam": levels of up to 4 children per node, breadth first."""
+    par = np.empty((B, n), dtype=np.int32)
+    for b in range(B):
+        if shape == "chain":
+            par[b] = np.arange(-1, n - 1)
+        elif shape == "star":
+            par[b] = -1
+        elif shape == "beam":
+            par[b, 0] = -1
+            for j in range(1, n):
+                par[b, j] = (j - 1) // 4
+        else:
+            par[b] = [int(rng.integers(-1, j)) if j > 0 else -1 for j in range(n)]
+    return par
+
+
+def speculative_tree(device="cpu", seed: int = 10, B: int = 64, n: int = 16, lo: int = 512,
+                     hi: int = 4096, shape: str = "random"):
+    """Llama-3-8B-shaped layer verifying a tree of n draft tokens per
+    sequence (32/8 heads, D=128, bf16, page 16, lens ~ U[lo, hi] counting
+    the draft tokens). Returns (case, parents int32 [B, n])."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    case = build_case(f"speculative_tree_B{B}_n{n}", seed, B=B, H_q=32, H_kv=8, D=128, page_size=16,
+                      seq_lens=lens, dtype="bf16", scale=1.0 / math.sqrt(128), device=device, rng=rng, q_len=n)
+    return case, draft_trees(B, n, rng, shape)
+
+
 def sliding_window(device="cpu", seed: int = 8, B: int = 64, lo: int = 4096, hi: int = 32768,
                    window: int = 4096) -> PagedCase:
     """Llama-3-8B-shaped layer over a sliding-window KV group: 32/8 heads,
