@@ -48,6 +48,11 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode-attn achieved HBM GB/s (% of ~8 TB/s) and query tokens/s, 1 GB300"
 UNIT = "GB/s"
+WORKLOADS = ["llama3_8b_layer", "mixed_lengths", "cascade", "mla", "spec_verify_q2", "spec_verify_q4",
+             "llama3_8b_layer_fp8", "cascade_nested", "sliding_window", "mla_fp8", "mla_spec_q4", "spec_tree"]
+# measured workloads whose kernels are tensor-bound: dense-peak ratio to bf16
+# of their operand type (e4m3 runs at twice the bf16 rate)
+FP8_TENSOR = ("mla_fp8",)
 
 
 def parse_args():
@@ -56,10 +61,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["llama3_8b_layer", "mixed_lengths", "cascade", "mla",
-                                           "spec_verify_q2", "spec_verify_q4", "llama3_8b_layer_fp8",
-                                           "cascade_nested", "sliding_window"],
-                    default="llama3_8b_layer")
+    ap.add_argument("--workload", choices=WORKLOADS, default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -216,6 +218,14 @@ def build_workload(name: str, device, small: bool = False, scale: float = 1.0):
         return workloads.sliding_window(device=device, B=4 if small else n(64))
     if name.startswith("spec_verify_q"):
         return workloads.speculative_verify(device=device, B=8 if small else n(64), q_len=int(name[13:]))
+    if name == "mla_fp8":
+        return workloads.absorbed_mla_fp8(device=device, B=2 if small else n(64))
+    if name == "mla_spec_q4":
+        return workloads.absorbed_mla_multi(device=device, B=2 if small else n(64))
+    if name == "spec_tree":
+        case, parents = workloads.speculative_tree(device=device, B=8 if small else n(64))
+        case.meta["parents"] = parents
+        return case
     raise ValueError(name)
 
 
@@ -227,8 +237,8 @@ def algorithmic(case, groups=None):
     flops of Q.C^T over 576 dims and P.V over 512."""
     es = 2 if case.dtype == "bf16" else 4
     tokens = int(case.attended_lens.astype(np.int64).sum())
-    if case.mla:
-        return tokens * case.D * es, tokens * case.H_q * (case.D + case.Dv) * 2
+    if case.mla:  # every query row of every token (q_len of them per sequence)
+        return case.kv_bytes_read(), tokens * case.q_len * case.H_q * (case.D + case.Dv) * 2
     if case.kv_fp8:
         return case.kv_bytes_read(), 0
     row = case.H_kv * (case.D + case.Dv) * es
@@ -275,9 +285,18 @@ def suffix_bytes(case, groups):
 
 def oracle_pass(view, case):
     import oracle
+    if case.mla and case.kv_fp8:
+        return oracle.mla_decode_attention_fp8(view["q"], view["q_scale"], view["k_pool"], view["k_scale"],
+                                               view["block_table"], view["seq_lens"], case.scale, case.Dv)
+    if case.mla and case.q_len > 1:
+        return oracle.mla_multi_query_decode_attention(view["q"], view["k_pool"], view["block_table"],
+                                                       view["seq_lens"], case.scale, case.Dv)
     if case.mla:
         return oracle.mla_decode_attention(view["q"], view["k_pool"], view["block_table"], view["seq_lens"],
                                            case.scale, case.Dv)
+    if "parents" in case.meta:
+        return oracle.tree_verify_decode_attention(view["q"], view["k_pool"], view["v_pool"], view["block_table"],
+                                                   view["seq_lens"], view["parents"], case.scale)
     kp, vp = view["k_pool"], view["v_pool"]
     if case.kv_fp8:
         ks, vs = view["k_scale"], view["v_scale"]
@@ -303,7 +322,7 @@ def sample_bytes(case, idx):
     es = 4 if case.dtype == "f32" else 2
     tokens = int(case.attended_lens[idx].astype(np.int64).sum())
     if case.mla:
-        return tokens * case.D * es
+        return tokens * (case.D + 4) if case.kv_fp8 else tokens * case.D * es
     if case.kv_fp8:
         return tokens * case.H_kv * (case.D + case.Dv) + tokens * case.H_kv * 2 * 4
     return tokens * case.H_kv * (case.D + case.Dv) * es
@@ -339,7 +358,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla", "cascade_nested") or
+    case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla", "cascade_nested",
+                                                                        "mla_spec_q4", "spec_tree") or
                           args.workload.startswith("spec_verify") or args.workload.endswith("fp8"))
     # size each step's sample so the whole run stays within ~2 minutes
     t1, _ = time_oracle(case, [0], 0.0)
@@ -387,14 +407,18 @@ class DeviceStep:
         self.lens = torch.from_numpy(c.attn_lens).to(dev)
         self.pos = torch.from_numpy(c.positions).to(dev)
         rows = (c.B, c.H_q) if c.q_len == 1 else (c.B, c.q_len, c.H_q)
-        self.out = torch.empty(*rows, c.Dv, dtype=c.q.dtype, device=dev)
+        out_dtype = torch.bfloat16 if c.q.dtype == torch.uint8 else c.q.dtype
+        self.out = torch.empty(*rows, c.Dv, dtype=out_dtype, device=dev)
+        self.parents = (torch.from_numpy(c.meta["parents"]).to(dev) if "parents" in c.meta else None)
         self.lse = torch.empty(*rows, dtype=torch.float32, device=dev)
         pools = [(c.k_pool, c.v_pool)]
         for _ in range(rotate - 1):
             pools.append((c.k_pool.clone(), c.v_pool.clone() if c.v_pool is not None else None))
         self.pools = pools
         # fp8 caches: each rotated pool copy has its own scale arrays
-        self.scales = [(c.k_scale, c.v_scale)] + [(c.k_scale.clone(), c.v_scale.clone())
+        def clone(t):
+            return t.clone() if t is not None else None
+        self.scales = [(c.k_scale, c.v_scale)] + [(clone(c.k_scale), clone(c.v_scale))
                                                   for _ in range(rotate - 1)] if c.kv_fp8 else None
         self.groups = None
         self.gdev = None
@@ -412,14 +436,16 @@ class DeviceStep:
             self.gdev = ts.groups_to_device(self.groups, dev)
             ws_bytes = ts.ts_cascade_decode_workspace_size(c.B, c.H_q, c.D)
         elif c.mla:
-            ws_bytes = ts.ts_mla_workspace_size(c.B, c.H_q, c.Dv)
+            ws_bytes = ts.ts_mla_multi_workspace_size(c.B, c.q_len, c.H_q, c.Dv)
+        elif self.parents is not None:
+            ws_bytes = 256
         elif c.q_len > 1:
             ws_bytes = ts.ts_paged_decode_multi_workspace_size(c.B, c.q_len, c.H_q, c.D)
         else:
             ws_bytes = ts.ts_paged_decode_workspace_size(c.B, c.H_q, c.D)
         self.ws = ts.new_workspace(ws_bytes, dev)
 
-    def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None, out=None):
+    def attention(self, i, q=None, bt=None, lens=None, stream=None, gdev=None, out=None, q_scale=None):
         ts, c = self.ts, self.case
         kp, vp = self.pools[i % len(self.pools)]
         out = self.out if out is None else out
@@ -432,9 +458,19 @@ class DeviceStep:
         elif self.groups is not None:
             ts.ts_cascade_decode_attn(q, kp, vp, gdev or self.gdev, bt, lens, c.scale, out=out, lse=self.lse,
                                       workspace=self.ws, stream=stream)
+        elif c.mla and c.kv_fp8:
+            ks, _ = self.scales[i % len(self.scales)]
+            ts.ts_mla_paged_decode_fp8(q, q_scale if q_scale is not None else c.meta["q_scale"], kp, ks, bt, lens,
+                                       c.scale, d_v=c.Dv, out=out, lse=self.lse, workspace=self.ws, stream=stream)
+        elif c.mla and c.q_len > 1:
+            ts.ts_mla_paged_decode_multi(q, kp, bt, lens, c.scale, d_v=c.Dv, out=out, lse=self.lse,
+                                         workspace=self.ws, stream=stream)
         elif c.mla:
             ts.ts_mla_paged_decode(q, kp, bt, lens, c.scale, d_v=c.Dv, out=out, lse=self.lse,
                                    workspace=self.ws, stream=stream)
+        elif self.parents is not None:
+            ts.ts_paged_decode_tree_attn(q, kp, vp, bt, lens, self.parents, c.scale, out=out, lse=self.lse,
+                                         workspace=self.ws, stream=stream)
         elif c.window > 0:
             ts.ts_paged_decode_window_attn(q, kp, vp, bt, lens, c.scale, c.window, out=out, lse=self.lse,
                                            workspace=self.ws, stream=stream)
@@ -463,7 +499,7 @@ class DeviceStep:
         if ev is not None:
             ev[0].record(stream)
         self.attention(i, q=inputs.get("q"), bt=inputs.get("bt"), lens=inputs.get("lens"), stream=stream,
-                       gdev=inputs.get("gdev"), out=inputs.get("out"))
+                       gdev=inputs.get("gdev"), out=inputs.get("out"), q_scale=inputs.get("q_scale"))
         if ev is not None:
             ev[1].record(stream)
 
@@ -547,6 +583,8 @@ def run_ours(args):
         if case.append:
             hin.update(k_new=case.k_new.cpu().pin_memory(), v_new=case.v_new.cpu().pin_memory(),
                        pos=torch.from_numpy(case.positions).pin_memory())
+        if case.mla and case.kv_fp8:
+            hin["q_scale"] = case.meta["q_scale"].cpu().pin_memory()
         # all of a step's inputs travel in one pinned buffer and one copy
         offs, total = {}, 0
         for k, v in hin.items():
@@ -706,8 +744,12 @@ def run_ours(args):
     traffic = kernel_traffic(f"{dom}__{args.workload}.md", source)
     if case.mla:
         tflops = dom_flops / (dom_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": tflops / tc_peak, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+        fp8 = args.workload in FP8_TENSOR
+        peak = tc_peak * (2.0 if fp8 else 1.0)
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tflops / peak,
+                    "peak_source": (f"{peak_kind} bf16_tflops (burst) x 2 (e4m3 / bf16 nominal dense ratio)"
+                                    if fp8 else f"{peak_kind} bf16_tflops (burst)"),
                     "kernel": dom, "kernel_ms": dom_ms, "flops_per_launch": dom_flops, "traffic": traffic,
                     "hbm": {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                             "frac": hbm_achieved / hbm_peak, "bytes_per_launch": dom_bytes}}
@@ -718,7 +760,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("e4m3 K/V, bf16 q" if case.kv_fp8 else
+        "vs_baseline": None, "dtype": ("e4m3 q and latent" if case.kv_fp8 and case.mla else
+                                       "e4m3 K/V, bf16 q" if case.kv_fp8 else
                                        "bf16" if case.dtype == "bf16" else "f32"), "accumulate": "f32",
         "data": "synthetic",
         "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D,

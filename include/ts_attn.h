@@ -585,6 +585,37 @@ TS_API ts_status ts_mla_paged_decode_multi(const void* q, const void* kv_pool, c
                                            void* stream);
 
 /*
+ * ts_mla_paged_decode_fp8 - absorbed-MLA decode on the fp8 input path.
+ *
+ * TokenSpeed deep dive, section 1: the MLA decode kernel takes bf16, fp16 or
+ * fp8 inputs. Here the query rows and the cached latent rows are e4m3fn codes
+ * with one float32 token-group scale per row (tokenspeed 딥다이브, section
+ * 6-4: value = code * scale). The result is ts_mla_paged_decode_multi's over
+ * the reconstructed rows: s[h,t] = scale * <q[h] * q_scale[h], C[t] *
+ * kv_scale[t]> over all 576 columns, O = softmax(s) C[:, 0:512]. Scores run on
+ * e4m3 tensor-core products (32 columns per instruction); for the product
+ * with the values the softmax weights, times the token scales, are carried
+ * as two e4m3 terms (hi and the remainder): relative error at most 2^-8, as
+ * with bf16 weights.
+ *
+ *   q_codes   device uint8 [B, q_len, H, 576] (q_len = 1: [B, H, 576])
+ *   q_scale   device float32 [B, q_len, H]: one scale per query row
+ *   kv_codes  device uint8 [num_pages, page_size, 576]
+ *   kv_scale  device float32 [num_pages, page_size], 16-byte aligned
+ *   out       device bf16 [B, q_len, H, 512];  lse float32 [B, q_len, H] or NULL
+ *   workspace >= ts_mla_multi_workspace_size(B, q_len, H, D_v)
+ *   other arguments and support (H * fold == 128, D_qk 576, D_v 512, page 64)
+ *   as ts_mla_paged_decode_multi. Rows past a sequence's end may hold any
+ *   codes and scales (NaN included); they are never weighted.
+ */
+TS_API ts_status ts_mla_paged_decode_fp8(const void* q_codes, const float* q_scale, const void* kv_codes,
+                                         const float* kv_scale, const int32_t* block_table, int32_t bt_stride,
+                                         const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                                         int32_t D_qk, int32_t D_v, int32_t page_size, int32_t num_pages,
+                                         float scale, void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
  * ts_read_device_error - copy the sticky error word of an attention
  * workspace to *error_bits (synchronises the stream). workspace == NULL
  * reads the error word of ts_paged_decode_attn_noalloc's static scratch on

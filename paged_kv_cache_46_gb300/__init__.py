@@ -117,6 +117,8 @@ _SIGNATURES = {
                                                  _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_paged_decode_tree_attn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _I32,
                                                  _I32, _I32, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "ts_mla_paged_decode_fp8": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32,
+                                               _I32, _I32, _F32, _VP, _VP, _VP, _SZ, _VP]),
     "ts_read_device_error": (ctypes.c_int, [_VP, _U32P, _VP]),
     "ts_trace_enable": (ctypes.c_int, [_I32]),
     "ts_trace_collect": (_I32, [ctypes.POINTER(LaunchRecordC), _I32]),
@@ -558,6 +560,33 @@ def ts_mla_paged_decode_multi(q, kv_pool, block_table, seq_lens, scale: float, d
                                            _ptr(seq_lens), B, q_len, H, Dqk, d_v, ps, P, float(scale), _ptr(out),
                                            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                            _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def ts_mla_paged_decode_fp8(q_codes, q_scale, kv_codes, kv_scale, block_table, seq_lens, scale: float,
+                            d_v: int = 512, out=None, lse=None, workspace=None, stream=None, return_lse: bool = False):
+    """Absorbed-MLA decode on e4m3 inputs: q_codes uint8 [B, H, 576] or [B, q_len, H, 576]
+    with q_scale float32 [B, (q_len,) H]; kv_codes uint8 [P, ps, 576] with kv_scale
+    float32 [P, ps] -> out bf16 [B, (q_len,) H, d_v]."""
+    _require_i32(block_table, seq_lens)
+    if q_codes.dtype != torch.uint8 or kv_codes.dtype != torch.uint8:
+        raise TypeError("fp8 codes travel as uint8 tensors")
+    if q_scale.dtype != torch.float32 or kv_scale.dtype != torch.float32:
+        raise TypeError("scales must be float32")
+    single = q_codes.dim() == 3
+    B, q_len, H, Dqk = (q_codes.shape[0], 1, *q_codes.shape[1:]) if single else q_codes.shape
+    P, ps, _ = kv_codes.shape
+    shape = (B, H) if single else (B, q_len, H)
+    if out is None:
+        out = torch.empty(*shape, d_v, dtype=torch.bfloat16, device=q_codes.device)
+    if lse is None and return_lse:
+        lse = torch.empty(*shape, dtype=torch.float32, device=q_codes.device)
+    if workspace is None:
+        workspace = new_workspace(ts_mla_multi_workspace_size(B, q_len, H, d_v), q_codes.device)
+    _check(lib().ts_mla_paged_decode_fp8(_ptr(q_codes), _ptr(q_scale), _ptr(kv_codes), _ptr(kv_scale),
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, q_len, H, Dqk,
+                                         d_v, ps, P, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))
     return (out, lse) if return_lse else out
 
 

@@ -28,6 +28,20 @@
 // allocator, warps 4-11 softmax / epilogue (one head row and half of the
 // tile's tokens per thread). Four K/V stages keep three pages in flight.
 //
+// fp8 input path (TokenSpeed deep dive, section 1: bf16 / fp16 / fp8 inputs):
+// the query rows and the latent rows arrive as e4m3fn codes with one float32
+// token-group scale per row (tokenspeed 딥다이브, section 6-4). The same
+// cluster design runs kind::f8f6f4 products with K = 32 per instruction, so a
+// page costs each CTA 9 score products instead of 18. The latent arrives in
+// 128-byte (128-code) atoms, three per CTA: CTA 0 dims 0-383, CTA 1 dims
+// 256-639 (the last 64 past the row zero-filled); each CTA scores 9 K-steps
+// of 32 dims. Scores take the query row's and the key token's scales. For
+// P V the key token's scale is folded into P, times a power-of-two gain G
+// that keeps P <= 2^8 under the largest scale seen (O is rescaled when G
+// changes, as when the running maximum grows); P is split into two e4m3
+// terms, hi = e4m3(P) and lo = e4m3(P - hi): 4 significant bits each, so P
+// keeps a relative error of at most 2^-8, as a bf16 P would. O = acc / (G * l).
+//
 // Several query tokens per sequence (section 7.2, fold_sq_factor): with H
 // heads and q_len tokens, F = the largest factor of q_len with H * F <= 128
 // tokens are folded into the 128 rows of a tile (row r = token r / H of the
@@ -36,6 +50,8 @@
 // rows of virtual sequence v are the contiguous rows v * 128 .. v * 128 + 127,
 // and likewise for O and LSE. Row r of step st attends keys up to
 // L - q_len + st * F + r / H (causal among the new tokens).
+#include <cuda_fp8.h>
+
 #include <cmath>
 
 #include "ts_tcgen05.cuh"
@@ -52,6 +68,12 @@ constexpr int kThreadsMla = 384;
 constexpr float kLog2eM = 1.4426950408889634f;
 constexpr float kLn2M = 0.6931471805599453f;
 constexpr float kSlackM = 8.0f;
+// fp8 path: stage = three 128-code atoms + the page's 64 scales (1024-aligned)
+constexpr int kStageBytesF8 = 25 * 1024;
+constexpr int kOffScalesF8 = 3 * kAtomBytes;
+constexpr uint32_t kTSF8 = 96, kTPF8 = 160;  // TMEM: Q [0,72) S [96,160) P hi|lo [160,192) O [256,512)
+// P <= 2^8 * 2^slack must stay below e4m3's largest finite value, 448
+constexpr float kSlackF8 = 0.5f;
 
 // Shared memory map (from a 1024-aligned base).
 constexpr int kOffStages = 0;
@@ -60,15 +82,21 @@ constexpr int kOffStages = 0;
 // swizzled by row, so that one bulk copy moves a warp's block.
 constexpr int kWarpX = 32 * kTokHalf * 4;                       // 4 KB
 constexpr int kXBufBytes = 8 * kWarpX;                          // a tile's 128 x 64 scores
-constexpr int kOffX = kOffStages + kStages * kStageBytes;       // score exchange, 2 tiles
-constexpr int kOffRed = kOffX + 2 * kXBufBytes;                 // pair exchange: [2][2][128] floats
-constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;              // 36 mbarriers
-constexpr int kOffMisc = kOffBars + 36 * 8;
-constexpr int kSmemMla = kOffMisc + 192;
-static_assert(kSmemMla <= 232448, "shared memory of one CTA");
+template <bool kF8>
+struct MlaSmem {
+  static constexpr int kStage = kF8 ? kStageBytesF8 : kStageBytes;
+  static constexpr int kOffX = kOffStages + kStages * kStage;   // score exchange, 2 tiles
+  static constexpr int kOffRed = kOffX + 2 * kXBufBytes;        // pair exchange: [2][2][128] floats
+  static constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;     // 36 mbarriers
+  static constexpr int kOffMisc = kOffBars + 36 * 8;
+  static constexpr int kSmem = kOffMisc + 192;
+  static_assert(kSmem <= 232448, "shared memory of one CTA");
+};
 
 struct MlaParams {
-  const __nv_bfloat16* q;   // [B, 128, 576]
+  const void* q;            // [B, 128, 576] bf16, or e4m3 codes on the fp8 path
+  const float* q_scale;     // fp8 path: [B, 128] one scale per query row
+  const float* kv_scale;    // fp8 path: [num_pages, 64] one scale per latent row
   const int32_t* block_table;
   const int32_t* seq_lens;
   int32_t bt_stride, B, num_pages;
@@ -161,8 +189,12 @@ struct Walker {
   }
 };
 
+template <bool kF8>
 __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaParams p,
                                                                     const __grid_constant__ CUtensorMap kvmap) {
+  using Sm = MlaSmem<kF8>;
+  constexpr int kOffX = Sm::kOffX, kOffRed = Sm::kOffRed, kOffBars = Sm::kOffBars, kOffMisc = Sm::kOffMisc;
+  constexpr int kStageB = Sm::kStage;
   // The whole 227 KB is in use, with no room to realign: the swizzled tiles
   // need a 1024-byte aligned base, which the declaration asks for and the
   // check below confirms (both CTAs of a cluster see the same offset).
@@ -177,9 +209,9 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   const uint32_t peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
-  const int n_atoms = 5;                     // latent atoms this CTA loads
-  const int atom0 = rank == 0 ? 0 : 4;       // first latent atom
-  const int q_words = 160;                   // TMEM columns of this CTA's Q part
+  const int n_atoms = kF8 ? 3 : 5;           // latent atoms this CTA loads
+  const int atom0 = rank == 0 ? 0 : (kF8 ? 2 : 4);  // first latent atom
+  const int q_words = kF8 ? 72 : 160;        // TMEM columns of this CTA's Q part
   // the shared atom 4 (stage atom 4 of CTA 0, 0 of CTA 1): CTA 0 takes its
   // 16-column steps 0-1, CTA 1 steps 2-3
   const int shared_atom = rank == 0 ? 4 : 0, shared_ks0 = rank == 0 ? 0 : 2;
@@ -316,31 +348,50 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         row = page * kPS;
       else
         set_device_error(p.err_word, TS_DEVERR_PAGE_RANGE);
-      mbar_arrive_expect_tx(bar(s), n_atoms * kAtomBytes);
-      const uint32_t st = smem_u32(smem + kOffStages + s * kStageBytes);
-      for (int a = 0; a < n_atoms; ++a) tma_load_2d(st + a * kAtomBytes, &kvmap, (atom0 + a) * 64, row, bar(s));
+      const uint32_t st = smem_u32(smem + kOffStages + s * kStageB);
+      if constexpr (kF8) {
+        // three 128-code atoms and the page's 64 token scales (a bad page
+        // reads page 0's scales against zero-filled codes; it is flagged)
+        mbar_arrive_expect_tx(bar(s), n_atoms * kAtomBytes + kPS * 4);
+        for (int a = 0; a < n_atoms; ++a) tma_load_2d(st + a * kAtomBytes, &kvmap, (atom0 + a) * 128, row, bar(s));
+        const int sp = (page >= 0 && page < p.num_pages) ? page : 0;
+        bulk_g2s(st + kOffScalesF8, p.kv_scale + static_cast<int64_t>(sp) * kPS, kPS * 4, bar(s));
+      } else {
+        mbar_arrive_expect_tx(bar(s), n_atoms * kAtomBytes);
+        for (int a = 0; a < n_atoms; ++a) tma_load_2d(st + a * kAtomBytes, &kvmap, (atom0 + a) * 64, row, bar(s));
+      }
     }
     if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
   } else if (have_work && warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t iS = idesc_bf16(kH, kTok, 0);
-    constexpr uint32_t iO = idesc_bf16(kH, 256, 1);
+    constexpr uint32_t iS = kF8 ? idesc_e4m3(kH, kTok, 0) : idesc_bf16(kH, kTok, 0);
+    constexpr uint32_t iO = kF8 ? idesc_e4m3(kH, 256, 1) : idesc_bf16(kH, 256, 1);
     Walker w;
     w.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
     auto issue_s = [&](int j) {
       const int s = j % kStages;
       if (!mbar_wait(bar(s), (j / kStages) & 1)) return false;
       tc_fence_after();
-      const uint32_t st = smem_u32(smem + kOffStages + s * kStageBytes);
-      // the first product issued (atom 0, step 0 on CTA 0; step 2 on CTA 1)
-      // overwrites S, the others accumulate
+      const uint32_t st = smem_u32(smem + kOffStages + s * kStageB);
+      if constexpr (kF8) {
+        // 9 K-steps of 32 dims from dim 288 * rank: atom d / 128, byte d % 128
 #pragma unroll
-      for (int a = 0; a < 5; ++a)
+        for (int i = 0; i < 9; ++i) {
+          const int d = static_cast<int>(rank) * 288 + 32 * i;
+          mma_e4m3_tmem_a(tmem + kTSF8, tmem + kTQ + i * 8,
+                          desc_sw128(st + (d / 128 - atom0) * kAtomBytes + d % 128), iS, i > 0 ? 1u : 0u);
+        }
+      } else {
+        // the first product issued (atom 0, step 0 on CTA 0; step 2 on CTA 1)
+        // overwrites S, the others accumulate
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          if (a != shared_atom || (ks >> 1) == (shared_ks0 >> 1))
-            mma_bf16_tmem_a(tmem + kTS, tmem + kTQ + a * 32 + ks * 8, desc_sw128(st + a * kAtomBytes + ks * 32),
-                            iS, (a == 0 && ks == shared_ks0) ? 0u : 1u);
+        for (int a = 0; a < 5; ++a)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            if (a != shared_atom || (ks >> 1) == (shared_ks0 >> 1))
+              mma_bf16_tmem_a(tmem + kTS, tmem + kTQ + a * 32 + ks * 8, desc_sw128(st + a * kAtomBytes + ks * 32),
+                              iS, (a == 0 && ks == shared_ks0) ? 0u : 1u);
+      }
       mma_commit(bar(8));
       return true;
     };
@@ -362,12 +413,23 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       if (!ok) break;
       tc_fence_after();
       const int s = j % kStages;
-      const uint32_t st = smem_u32(smem + kOffStages + s * kStageBytes);
-      // O[:, 0:256] += P V: V is MN-major over four 64-column atoms (LBO = atom stride)
+      const uint32_t st = smem_u32(smem + kOffStages + s * kStageB);
+      if constexpr (kF8) {
+        // O[:, 0:256] += (P_hi + P_lo) V: V is MN-major over this CTA's first two
+        // 128-code atoms (LBO = atom stride); K-steps of 32 tokens (4 KB)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_tmem_a(tmem + kTO, tmem + kTP + ks * 8, desc_sw128(st + ks * 2048, kAtomBytes, 1024), iO,
-                        !(cur.first && ks == 0));
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_e4m3_tmem_a(tmem + kTO, tmem + kTPF8 + t * 16 + ks * 8,
+                            desc_sw128(st + ks * 4096, kAtomBytes, 1024), iO, !(cur.first && t == 0 && ks == 0));
+      } else {
+        // O[:, 0:256] += P V: V is MN-major over four 64-column atoms (LBO = atom stride)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16_tmem_a(tmem + kTO, tmem + kTP + ks * 8, desc_sw128(st + ks * 2048, kAtomBytes, 1024), iO,
+                          !(cur.first && ks == 0));
+      }
       mma_commit(bar(11));
       mma_commit(bar(4 + s));
       cur = nxt;
@@ -392,22 +454,62 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     Walker w;
     w.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
     auto load_q = [&](int b) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(b) * kH + h) * kDqk + atom0 * 64 + hf * q_half * 2);
-#pragma unroll 1
-      for (int c0 = 0; c0 < q_half; c0 += 16) {
-        uint32_t u[16];
+      if constexpr (kF8) {
+        // this CTA's 288 codes of the row (from dim 288 * rank), four per TMEM
+        // column: warp hf 0 bytes 0-159 -> columns 0-39, hf 1 bytes 160-287 ->
+        // columns 40-71
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const unsigned char*>(p.q) + (static_cast<int64_t>(b) * kH + h) * kDqk + rank * 288 +
+            hf * 160);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint4 v = src[c0 / 4 + x];
-          u[4 * x] = v.x;
-          u[4 * x + 1] = v.y;
-          u[4 * x + 2] = v.z;
-          u[4 * x + 3] = v.w;
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+          uint32_t u[16];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint4 v = src[c0 / 4 + x];
+            u[4 * x] = v.x;
+            u[4 * x + 1] = v.y;
+            u[4 * x + 2] = v.z;
+            u[4 * x + 3] = v.w;
+          }
+          tmem_st16(trow + kTQ + hf * 40 + c0, u);
         }
-        tmem_st16(trow + kTQ + hf * q_half + c0, u);
+        if (hf == 0) {
+          uint32_t u[8];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const uint4 v = src[8 + x];
+            u[4 * x] = v.x;
+            u[4 * x + 1] = v.y;
+            u[4 * x + 2] = v.z;
+            u[4 * x + 3] = v.w;
+          }
+          tmem_st8(trow + kTQ + 32, u);
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(p.q) + (static_cast<int64_t>(b) * kH + h) * kDqk + atom0 * 64 +
+            hf * q_half * 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < q_half; c0 += 16) {
+          uint32_t u[16];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint4 v = src[c0 / 4 + x];
+            u[4 * x] = v.x;
+            u[4 * x + 1] = v.y;
+            u[4 * x + 2] = v.z;
+            u[4 * x + 3] = v.w;
+          }
+          tmem_st16(trow + kTQ + hf * q_half + c0, u);
+        }
       }
       tmem_wait_st();
+    };
+    // fp8: the query row's scale times scale * log2(e), for the tile being
+    // scored and the next one (loaded a tile ahead)
+    auto row_scale = [&](int b) {
+      return kF8 ? p.q_scale[static_cast<int64_t>(b) * kH + h] * p.scale_log2 : p.scale_log2;
     };
     // Swap one float per row with the other warp of this quarter (bounded
     // wait on the pair's mbarrier; the two warps make the same calls in the
@@ -424,11 +526,11 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       ++nx;
       return got;
     };
-    auto epilogue = [&](const Tile& t, float m, float l_half) {
+    auto epilogue = [&](const Tile& t, float m, float l_half, float ginv) {
       float l_other = 0.f;
       if (!pair_exchange(l_half, l_other)) return false;
       const float l = l_half + l_other;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const float inv = l > 0.f ? ginv / l : 0.f;
       for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t u[16];
         tmem_ld16(trow + kTO + hf * 128 + c0, u);
@@ -480,8 +582,9 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       tc_fence_after();
       {
         uint32_t u[2][16];
-        tmem_ld16(trow + kTS + hf * kTokHalf, u[0]);
-        tmem_ld16(trow + kTS + hf * kTokHalf + 16, u[1]);
+        constexpr uint32_t kTSc = kF8 ? kTSF8 : kTS;  // S columns of this path
+        tmem_ld16(trow + kTSc + hf * kTokHalf, u[0]);
+        tmem_ld16(trow + kTSc + hf * kTokHalf + 16, u[1]);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < kTokHalf; ++x) mine[x] = __uint_as_float(u[x / 16][x % 16]);
@@ -508,16 +611,22 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     Tile cur, nxt, nn, prev;
     bool has_cur = w.next(cur);
     if (has_cur) load_q(cur.b);
+    float qs_cur = has_cur ? row_scale(cur.b) : 0.f, qs_nxt = 0.f, qs_nn = 0.f;
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(12));
     bool has_nxt = has_cur && w.next(nxt);
+    if (has_nxt) qs_nxt = row_scale(nxt.b);
     if (has_cur) ok = send_next(0, has_nxt && nxt.first, nxt.b);
     float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
+    // fp8: gain G (a power of two) applied to P so that P <= 2^8 under the
+    // largest token scale of the segment so far
+    float G = 1.f;
     bool prev_last = false;
     int n_tiles = 0;
     for (int j = 0; ok && has_cur; ++j) {
       const bool has_nn = has_nxt && w.next(nn);
+      if (has_nn) qs_nn = row_scale(nn.b);
       // full scores of tile j: this thread's partial + the peer's
       const int xb = j & 1;
       ok = mbar_wait(bar(16 + 8 * xb + sw), (j >> 1) & 1);
@@ -537,10 +646,46 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       int lim = cur.rem;
       if (p.q_len > 1) lim -= p.q_len - 1 - ((cur.b % p.steps) * p.fold + (h >> p.h_shift));
       float mx = -INFINITY;
+      float Gt = 1.f;  // fp8: the gain this tile alone would take
+      // fp8: the stage's 64 token scales (landed with its codes; the wait on the
+      // stage's barrier makes them visible), read from shared memory each time
+      const float4* sc4 = reinterpret_cast<const float4*>(smem + kOffStages + (j % kStages) * kStageB +
+                                                          kOffScalesF8) + hf * 8;
+      if constexpr (kF8) {
+        ok = mbar_wait(bar(j % kStages), (j / kStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const float4* all4 = sc4 - hf * 8;
+        const int valid = cur.valid();
+        float cmax = 1e-30f;
 #pragma unroll
-      for (int c = 0; c < kTokHalf; ++c) {
-        s[c] = hf * kTokHalf + c < lim ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 v = all4[c4];
+          const int t0 = c4 * 4;
+          cmax = fmax3(cmax, t0 < valid ? v.x : 0.f, t0 + 1 < valid ? v.y : 0.f);
+          cmax = fmax3(cmax, t0 + 2 < valid ? v.z : 0.f, t0 + 3 < valid ? v.w : 0.f);
+        }
+        // 2^(8 - e) with 2^e the smallest power of two >= cmax
+        const uint32_t bits = __float_as_uint(cmax);
+        const int e = static_cast<int>((bits >> 23) & 0xffu) - 127 + ((bits & 0x7fffffu) != 0u ? 1 : 0);
+        Gt = __uint_as_float(static_cast<uint32_t>(127 + 8 - e) << 23);
+        const float qsc = qs_cur;
+#pragma unroll
+        for (int c4 = 0; c4 < kTokHalf / 4; ++c4) {
+          const float4 v = sc4[c4];
+          const float cv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = 4 * c4 + k;
+            s[c] = hf * kTokHalf + c < lim ? s[c] * (qsc * cv[k]) : -INFINITY;
+            mx = fmaxf(mx, s[c]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTokHalf; ++c) {
+          s[c] = hf * kTokHalf + c < lim ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
       }
       {
         float mo;
@@ -552,30 +697,68 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         ok = mbar_wait(bar(11), (j - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        if (prev_last && !epilogue(prev, m, l)) { ok = false; break; }
+        if (prev_last && !epilogue(prev, m, l, 1.0f / G)) { ok = false; break; }
       }
       if (cur.first) {
         m = mx;
         l = 0.f;
-      } else if (__any_sync(0xffffffffu, mx > m + kSlackM)) {
-        // both warps of the quarter see the same row maxima: same decision
-        const float mnew = fmaxf(m, mx);
-        const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
-        m = mnew;
-        l *= alpha;
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-          uint32_t u[16];
-          tmem_ld16(trow + kTO + hf * 128 + c0, u);
-          tmem_wait_ld();
+        G = Gt;
+      } else {
+        // both warps of the quarter see the same row maxima: same decision;
+        // fp8: a tile with a larger scale lowers G for every row alike
+        const bool grow = __any_sync(0xffffffffu, mx > m + (kF8 ? kSlackF8 : kSlackM));
+        if (grow || Gt < G) {
+          const float mnew = grow ? fmaxf(m, mx) : m;
+          const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
+          const float gnew = fminf(G, Gt);
+          const float beta = alpha * (gnew / G);  // O carries G, l does not
+          m = mnew;
+          l *= alpha;
+          G = gnew;
+          for (int c0 = 0; c0 < 128; c0 += 16) {
+            uint32_t u[16];
+            tmem_ld16(trow + kTO + hf * 128 + c0, u);
+            tmem_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
-          tmem_st16(trow + kTO + hf * 128 + c0, u);
+            for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * beta);
+            tmem_st16(trow + kTO + hf * 128 + c0, u);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
       const float ms = m == -INFINITY ? 0.f : m;
       float ls = 0.f;
-      {
+      if constexpr (kF8) {
+        // P = exp2(s - m) * scale * G in two e4m3 terms: hi = e4m3(P),
+        // lo = e4m3(P - hi); token t at byte t % 4 of column t / 4, hi in
+        // columns [0, 16), lo in [16, 32)
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          uint32_t hw = 0u, lw = 0u;
+          const float4 v = sc4[x];
+          const float cg[4] = {v.x * G, v.y * G, v.z * G, v.w * G};
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            const int t = 4 * x + k;
+            const float e0 = fast_exp2(s[t] - ms), e1 = fast_exp2(s[t + 1] - ms);
+            ls += e0 + e1;
+            // masked tokens (e = 0) may carry a NaN scale: their weight is 0
+            const float w0 = e0 > 0.f ? e0 * cg[k] : 0.f;
+            const float w1 = e1 > 0.f ? e1 * cg[k + 1] : 0.f;
+            const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(w0, w1), __NV_SATFINITE, __NV_E4M3);
+            const float2 hb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+            const __nv_fp8x2_storage_t l2 =
+                __nv_cvt_float2_to_fp8x2(make_float2(w0 - hb.x, w1 - hb.y), __NV_SATFINITE, __NV_E4M3);
+            hw |= static_cast<uint32_t>(h2) << (8 * k);
+            lw |= static_cast<uint32_t>(l2) << (8 * k);
+          }
+          hi[x] = hw;
+          lo[x] = lw;
+        }
+        tmem_st8(trow + kTPF8 + hf * 8, hi);
+        tmem_st8(trow + kTPF8 + 16 + hf * 8, lo);
+      } else {
         uint32_t u[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
@@ -595,9 +778,11 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         const int sj = j % kStages;
         ok = mbar_wait(bar(sj), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        unsigned char* st = smem + kOffStages + sj * kStageBytes;
-        for (int i = sw * 32 + lane; i < (kTok - valid) * 4 * 8; i += 8 * 32) {
-          const int row = valid + i / 32, a = (i / 8) & 3, c = i & 7;
+        unsigned char* st = smem + kOffStages + sj * kStageB;
+        // V: the first 4 (bf16) or 2 (fp8) atoms of the stage, 128-byte rows
+        constexpr int kVAtoms = kF8 ? 2 : 4;
+        for (int i = sw * 32 + lane; i < (kTok - valid) * kVAtoms * 8; i += 8 * 32) {
+          const int row = valid + i / (kVAtoms * 8), a = (i / 8) % kVAtoms, c = i & 7;
           *reinterpret_cast<uint4*>(st + a * kAtomBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();  // each warp's zeros reach the MMA before its p_full arrive
@@ -611,6 +796,8 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       has_cur = has_nxt;
       nxt = nn;
       has_nxt = has_nn;
+      qs_cur = qs_nxt;
+      qs_nxt = qs_nn;
       n_tiles = j + 1;
     }
     if (ok && prev_last) {
@@ -618,7 +805,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       ok = mbar_wait(bar(11), (n_tiles - 1) & 1);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        ok = epilogue(prev, m, l);
+        ok = epilogue(prev, m, l, 1.0f / G);
       } else {
         ok = false;
       }
@@ -721,10 +908,12 @@ int mla_fold(int H, int q_len) {
   return H * best == kH ? best : 0;
 }
 
-ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_table, int32_t bt_stride,
-                     const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H, int32_t D_qk,
-                     int32_t D_v, int32_t page_size, int32_t num_pages, float scale, void* out, float* lse,
-                     void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+template <bool kF8>
+ts_status mla_launch(const void* q, const float* q_scale, const void* kv_pool, const float* kv_scale,
+                     const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens, int32_t B,
+                     int32_t q_len, int32_t H, int32_t D_qk, int32_t D_v, int32_t page_size, int32_t num_pages,
+                     float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                     const char* who) {
   if (B < 0 || q_len < 1 || num_pages <= 0 || bt_stride <= 0 ||
       static_cast<long long>(num_pages) * page_size > INT32_MAX ||
       static_cast<long long>(B) * q_len > INT32_MAX / kH)
@@ -737,11 +926,11 @@ ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_ta
                 "page_size=64 (got %d, %d, %d)", who, H, q_len, D_qk, D_v, page_size);
   if (!std::isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "%s: scale not finite", who);
   if (B == 0) return TS_OK;
-  if (!q || !kv_pool || !block_table || !seq_lens || !out)
+  if (!q || !kv_pool || !block_table || !seq_lens || !out || (kF8 && (!q_scale || !kv_scale)))
     return fail(TS_ERR_INVALID_ARG, "%s: null pointer", who);
-  for (const void* ptr : {q, kv_pool, static_cast<const void*>(out)})
+  for (const void* ptr : {q, kv_pool, static_cast<const void*>(out), static_cast<const void*>(kv_scale)})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
-      return fail(TS_ERR_INVALID_ARG, "%s: q, kv_pool and out must be 16-byte aligned", who);
+      return fail(TS_ERR_INVALID_ARG, "%s: q, kv_pool, out (and kv_scale) must be 16-byte aligned", who);
   const int steps = q_len / fold;
   const int Bv = B * steps;
   const int pairs = mla_pairs();
@@ -754,17 +943,22 @@ ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_ta
   auto enc = tensor_map_encoder();
   if (!enc) return fail(TS_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", who);
   CUtensorMap kvmap;
+  // the latent pool as (column, pool row); a box is one page of 128 bytes of
+  // columns: 64 bf16 or 128 e4m3 codes (columns past 576 read as zero)
+  const size_t esz = kF8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(num_pages) * kPS};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk) * 2};
-  cuuint32_t box[2] = {64, kTok};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), kTok};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_pool), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(&kvmap, kF8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(kv_pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TS_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", who, static_cast<int>(r));
 
   MlaParams prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.q = q;
+  prm.q_scale = q_scale;
+  prm.kv_scale = kv_scale;
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.bt_stride = bt_stride;
@@ -786,8 +980,8 @@ ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_ta
   prm.h_shift = h_shift;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  ts_status st = prepare_once(reinterpret_cast<const void*>(mla_decode_kernel), [](const void* k) {
-    return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMla),
+  ts_status st = prepare_once(reinterpret_cast<const void*>(mla_decode_kernel<kF8>), [](const void* k) {
+    return cuda_check(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaSmem<kF8>::kSmem),
                       "mla smem attribute");
   });
   if (st != TS_OK) return st;
@@ -799,13 +993,13 @@ ts_status mla_launch(const void* q, const void* kv_pool, const int32_t* block_ta
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kThreadsMla);
-  cfg.dynamicSmemBytes = kSmemMla;
+  cfg.dynamicSmemBytes = MlaSmem<kF8>::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   {
     LaunchTrace trace("mla_decode_kernel", s);
-    st = cuda_check(cudaLaunchKernelEx(&cfg, mla_decode_kernel, prm, kvmap), "mla decode launch");
+    st = cuda_check(cudaLaunchKernelEx(&cfg, mla_decode_kernel<kF8>, prm, kvmap), "mla decode launch");
   }
   if (st != TS_OK) return st;
   cudaLaunchAttribute pattr[1];
@@ -849,8 +1043,8 @@ extern "C" ts_status ts_mla_paged_decode(const void* q, const void* kv_pool, con
   if (H != ts::kH)
     return ts::fail(TS_ERR_UNSUPPORTED, "%s: needs H=128 (got %d); ts_mla_paged_decode_multi folds "
                     "fewer heads", who, H);
-  return ts::mla_launch(q, kv_pool, block_table, bt_stride, seq_lens, B, 1, H, D_qk, D_v, page_size,
-                        num_pages, scale, out, lse, workspace, workspace_bytes, stream, who);
+  return ts::mla_launch<false>(q, nullptr, kv_pool, nullptr, block_table, bt_stride, seq_lens, B, 1, H, D_qk,
+                               D_v, page_size, num_pages, scale, out, lse, workspace, workspace_bytes, stream, who);
 }
 
 extern "C" ts_status ts_mla_paged_decode_multi(const void* q, const void* kv_pool, const int32_t* block_table,
@@ -859,7 +1053,18 @@ extern "C" ts_status ts_mla_paged_decode_multi(const void* q, const void* kv_poo
                                                int32_t page_size, int32_t num_pages, float scale, void* out,
                                                float* lse, void* workspace, size_t workspace_bytes,
                                                void* stream) {
-  return ts::mla_launch(q, kv_pool, block_table, bt_stride, seq_lens, B, q_len, H, D_qk, D_v, page_size,
-                        num_pages, scale, out, lse, workspace, workspace_bytes, stream,
-                        "ts_mla_paged_decode_multi");
+  return ts::mla_launch<false>(q, nullptr, kv_pool, nullptr, block_table, bt_stride, seq_lens, B, q_len, H, D_qk,
+                               D_v, page_size, num_pages, scale, out, lse, workspace, workspace_bytes, stream,
+                               "ts_mla_paged_decode_multi");
+}
+
+extern "C" ts_status ts_mla_paged_decode_fp8(const void* q_codes, const float* q_scale, const void* kv_codes,
+                                             const float* kv_scale, const int32_t* block_table, int32_t bt_stride,
+                                             const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                                             int32_t D_qk, int32_t D_v, int32_t page_size, int32_t num_pages,
+                                             float scale, void* out, float* lse, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
+  return ts::mla_launch<true>(q_codes, q_scale, kv_codes, kv_scale, block_table, bt_stride, seq_lens, B, q_len, H,
+                              D_qk, D_v, page_size, num_pages, scale, out, lse, workspace, workspace_bytes, stream,
+                              "ts_mla_paged_decode_fp8");
 }

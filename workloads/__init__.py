@@ -92,8 +92,8 @@ class PagedCase:
         """Algorithmic K/V (or latent) bytes one attention pass must read."""
         esize = 4 if self.dtype == "f32" else 2
         tokens = int(self.attended_lens.astype(np.int64).sum())
-        if self.mla:
-            return tokens * self.D * esize
+        if self.mla:  # fp8: one-byte codes plus a float32 scale per latent row
+            return tokens * (self.D + 4) if self.kv_fp8 else tokens * self.D * esize
         if self.kv_fp8:  # one-byte codes plus a float32 scale per row and kv head, K and V
             return kv_cache_bytes(tokens, self.H_kv, self.D, self.Dv, 1) + tokens * self.H_kv * 2 * 4
         return kv_cache_bytes(tokens, self.H_kv, self.D, self.Dv, esize)
@@ -274,6 +274,56 @@ def build_fp8_case(name: str, seed: int, *, B: int, H_q: int, H_kv: int, D: int,
     base.q, base.k_pool, base.v_pool, base.k_new, base.v_new = q, k_pool, v_pool, k_new, v_new
     base.kv_fp8, base.k_scale, base.v_scale = True, k_scale, v_scale
     return base
+
+
+def build_mla_fp8_case(name: str, seed: int, *, B: int, H: int, seq_lens: Sequence[int], scale: float,
+                       q_len: int = 1, page_size: int = 64, device="cpu",
+                       rng: Optional[np.random.Generator] = None) -> PagedCase:
+    """An absorbed-MLA case on the fp8 input path: the page placement of
+    :func:`build_case`; uniformly drawn non-NaN e4m3 codes for the latent rows
+    [P, ps, 576] and the query rows [B, (q_len,) H, 576], with one scale per
+    row drawn U[2.5, 3.5] / 448 (``k_scale`` [P, ps]; the query scales in
+    ``meta["q_scale"]``). Rows holding no cached token carry the NaN code 0x7F
+    and NaN scales."""
+    base = build_case(name, seed, B=B, H_q=H, H_kv=1, D=576, Dv=512, page_size=page_size, seq_lens=seq_lens,
+                      dtype="bf16", scale=scale, mla=True, device=device, rng=rng, values=False, q_len=q_len)
+    P = base.num_pages
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    def codes(shape):
+        c = torch.randint(0, 256, shape, generator=g, device=device, dtype=torch.int32)
+        return torch.where((c & 0x7F) == 0x7F, c - 1, c).to(torch.uint8)  # no NaN codes
+    def scales(shape):
+        return (torch.rand(shape, generator=g, device=device) + 2.5) / 448.0
+    kv = codes((P, page_size, 576))
+    kv_scale = scales((P, page_size))
+    qshape = (B, H) if q_len == 1 else (B, q_len, H)
+    q = codes(qshape + (576,))
+    q_scale = scales(qshape)
+    lens = base.seq_lens
+    sentinel_rows = np.ones((P, page_size), dtype=bool)
+    for b in range(B):
+        full, rem = divmod(int(lens[b]), page_size)
+        if full:
+            sentinel_rows[base.block_table[b, :full]] = False
+        if rem:
+            sentinel_rows[base.block_table[b, full], :rem] = False
+    mask = torch.from_numpy(sentinel_rows).to(device)
+    kv.masked_fill_(mask[:, :, None], 0x7F)
+    kv_scale.masked_fill_(mask, float("nan"))
+    base.q, base.k_pool, base.k_scale, base.q_len = q, kv, kv_scale, q_len
+    base.kv_fp8 = True
+    base.meta["q_scale"] = q_scale
+    return base
+
+
+def absorbed_mla_fp8(device="cpu", seed: int = 11, B: int = 64, lo: int = 8192, hi: int = 50000) -> PagedCase:
+    """The absorbed-MLA workload (B=64, 128 heads, latent 576, page 64, lens
+    U[lo, hi], scale 1/sqrt(192)) on the fp8 input path."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    return build_mla_fp8_case(f"absorbed_mla_fp8_B{B}", seed, B=B, H=128, seq_lens=lens,
+                              scale=1.0 / math.sqrt(192), device=device, rng=rng)
 
 
 def nested_prefix_cascade(device="cpu", seed: int = 8, roots: int = 4, subs: int = 4, members: int = 256,
@@ -507,8 +557,10 @@ def oracle_view(case: PagedCase, seq_idx: Optional[Sequence[int]] = None,
     dev_pages = torch.from_numpy(used.astype(np.int64)).to(kp.device)
     # fp8 caches travel as their raw codes (uint8) and float32 scales
     conv = (lambda t: t.cpu().numpy()) if case.kv_fp8 else _to_f64
+    dev_idx = torch.from_numpy(idx).to(case.q.device)
+    fp8_q = case.mla and case.kv_fp8   # MLA fp8 path: the queries are codes too
     out = {
-        "q": _to_f64(case.q[torch.from_numpy(idx).to(case.q.device)]),
+        "q": case.q[dev_idx].cpu().numpy() if fp8_q else _to_f64(case.q[dev_idx]),
         "k_pool": conv(kp.index_select(0, dev_pages)) if len(used) else None,
         "v_pool": conv(vp.index_select(0, dev_pages)) if (vp is not None and len(used)) else None,
         "block_table": bt,
@@ -518,7 +570,12 @@ def oracle_view(case: PagedCase, seq_idx: Optional[Sequence[int]] = None,
     }
     if case.kv_fp8:
         out["k_scale"] = case.k_scale.index_select(0, dev_pages).cpu().numpy() if len(used) else None
-        out["v_scale"] = case.v_scale.index_select(0, dev_pages).cpu().numpy() if len(used) else None
+        if case.v_scale is not None:
+            out["v_scale"] = case.v_scale.index_select(0, dev_pages).cpu().numpy() if len(used) else None
+    if fp8_q:
+        out["q_scale"] = case.meta["q_scale"][dev_idx].cpu().numpy()
+    if "parents" in case.meta:
+        out["parents"] = np.asarray(case.meta["parents"])[idx]
     if case.append:
         dev_idx = torch.from_numpy(idx).to(case.q.device)
         out["k_new"] = _to_f64(case.k_new[dev_idx])
