@@ -68,12 +68,16 @@ constexpr int kThreadsMla = 384;
 constexpr float kLog2eM = 1.4426950408889634f;
 constexpr float kLn2M = 0.6931471805599453f;
 constexpr float kSlackM = 8.0f;
-// fp8 path: stage = three 128-code atoms + the page's 64 scales (1024-aligned)
+// fp8 path: stage = three 128-code atoms + the page's 64 scales + the gain
+// G the tile takes (1024-aligned)
 constexpr int kStageBytesF8 = 25 * 1024;
 constexpr int kOffScalesF8 = 3 * kAtomBytes;
-constexpr uint32_t kTSF8 = 96, kTPF8 = 160;  // TMEM: Q [0,72) S [96,160) P hi|lo [160,192) O [256,512)
+constexpr int kOffGainF8 = kOffScalesF8 + kPS * 4;
+// TMEM: Q [0,72) S [96,160) P hi|lo of tiles j even / odd [160,192) [192,224) O [256,512)
+constexpr uint32_t kTSF8 = 96, kTPF8 = 160;
 // P <= 2^8 * 2^slack must stay below e4m3's largest finite value, 448
 constexpr float kSlackF8 = 0.5f;
+
 
 // Shared memory map (from a 1024-aligned base).
 constexpr int kOffStages = 0;
@@ -87,8 +91,8 @@ struct MlaSmem {
   static constexpr int kStage = kF8 ? kStageBytesF8 : kStageBytes;
   static constexpr int kOffX = kOffStages + kStages * kStage;   // score exchange, 2 tiles
   static constexpr int kOffRed = kOffX + 2 * kXBufBytes;        // pair exchange: [2][2][128] floats
-  static constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;     // 36 mbarriers
-  static constexpr int kOffMisc = kOffBars + 36 * 8;
+  static constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;     // 40 mbarriers
+  static constexpr int kOffMisc = kOffBars + 40 * 8;
   static constexpr int kSmem = kOffMisc + 192;
   static_assert(kSmem <= 232448, "shared memory of one CTA");
 };
@@ -220,8 +224,13 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
   // [0,4) kv_full  [4,8) kv_empty  8 s_full  9 s_free  10 p_full  11 pv_done
   // 12 q_ready  [16,32) xfull[buf][w]: the peer's half rows for softmax warp w
   // landed in inbound buffer buf  [32,36) pair[q]: both softmax warps of TMEM
-  // lane quarter q posted their value
+  // lane quarter q posted their value  [36,40) fp8: the stage's scales are
+  // prepared (scale x G, G stored)  13, 14: fp8 p_full and pv_done of the
+  // second P buffer (fp8 keeps two, tiles j even / odd)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto b_pfull = [&](int j) { return bar(kF8 && (j & 1) ? 13 : 10); };
+  auto b_pvdone = [&](int j) { return bar(kF8 && (j & 1) ? 14 : 11); };
+  auto ph = [](int j) { return kF8 ? (j >> 1) & 1 : j & 1; };  // parity of tile j's use of its buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(smem + kOffMisc + 16);  // warp sums (12)
   int* s_start = reinterpret_cast<int*>(smem + kOffMisc + 16 + 8 * (kThreadsMla / 32));
@@ -236,9 +245,12 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     mbar_init(bar(9), 8);
     mbar_init(bar(10), 8);
     mbar_init(bar(11), 1);
+    mbar_init(bar(13), 8);
+    mbar_init(bar(14), 1);
     mbar_init(bar(12), 8);
     for (int i = 16; i < 32; ++i) mbar_init(bar(i), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(32 + q), 2);
+    for (int i = 0; i < kStages; ++i) mbar_init(bar(36 + i), 1);
     s_start[0] = -1;
     s_start[1] = 0;
     fence_mbar_init();
@@ -409,7 +421,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         ok = mbar_wait(bar(9), (j + 1) & 1) && issue_s(j + 2);
         if (!ok) break;
       }
-      ok = mbar_wait(bar(10), j & 1);
+      ok = mbar_wait(b_pfull(j), ph(j));
       if (!ok) break;
       tc_fence_after();
       const int s = j % kStages;
@@ -421,7 +433,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
-            mma_e4m3_tmem_a(tmem + kTO, tmem + kTPF8 + t * 16 + ks * 8,
+            mma_e4m3_tmem_a(tmem + kTO, tmem + kTPF8 + (j & 1) * 32 + t * 16 + ks * 8,
                             desc_sw128(st + ks * 4096, kAtomBytes, 1024), iO, !(cur.first && t == 0 && ks == 0));
       } else {
         // O[:, 0:256] += P V: V is MN-major over four 64-column atoms (LBO = atom stride)
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
           mma_bf16_tmem_a(tmem + kTO, tmem + kTP + ks * 8, desc_sw128(st + ks * 2048, kAtomBytes, 1024), iO,
                           !(cur.first && ks == 0));
       }
-      mma_commit(bar(11));
+      mma_commit(b_pvdone(j));
       mma_commit(bar(4 + s));
       cur = nxt;
       has_cur = has_nxt;
@@ -438,6 +450,39 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       has_nxt = has_nn;
     }
     if (!ok) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
+  } else if (kF8 && have_work && warp == 3) {
+    // ---------------- fp8 scale warp ----------------------------------------
+    // Per tile: the largest token scale of the valid rows (two per lane, then
+    // across the warp), the gain G = 2^(8 - e) with 2^e the smallest power of
+    // two >= it (G of the segment: the smallest so far, reset at a segment's
+    // start), and each token's scale x G written back in place (0 for rows
+    // past the sequence's end, whose scales may be NaN). The softmax reads
+    // these products and G once they are marked ready.
+    Walker w;
+    w.init(p, pair, start, end, s_start[0], s_start[1], q_pages, r_pages, total);
+    Tile t;
+    float G = 1.f;
+    for (int j = 0; ok && w.next(t); ++j) {
+      const int s = j % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(s), (j / kStages) & 1));
+      if (!ok) break;
+      float* scl = reinterpret_cast<float*>(smem + kOffStages + s * kStageB + kOffScalesF8);
+      const int valid = t.valid();
+      const float c0 = lane < valid ? scl[lane] : 0.f, c1 = lane + 32 < valid ? scl[lane + 32] : 0.f;
+      float cmax = fmax3(1e-30f, c0, c1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      const uint32_t bits = __float_as_uint(cmax);
+      const int e = static_cast<int>((bits >> 23) & 0xffu) - 127 + ((bits & 0x7fffffu) != 0u ? 1 : 0);
+      const float Gt = __uint_as_float(static_cast<uint32_t>(127 + 8 - e) << 23);
+      G = t.first ? Gt : fminf(G, Gt);
+      scl[lane] = c0 * G;
+      scl[lane + 32] = c1 * G;
+      if (lane == 0) *reinterpret_cast<float*>(smem + kOffStages + s * kStageB + kOffGainF8) = G;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(36 + s));
+    }
+    if (!ok && lane == 0) set_device_error(p.err_word, TS_DEVERR_TIMEOUT);
   } else if (have_work && warp >= 4) {
     // ---------------- softmax / epilogue -------------------------------------
     // Eight warps: warp w reads TMEM lane quarter w % 4 (head rows 32(w%4) ..
@@ -611,7 +656,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     Tile cur, nxt, nn, prev;
     bool has_cur = w.next(cur);
     if (has_cur) load_q(cur.b);
-    float qs_cur = has_cur ? row_scale(cur.b) : 0.f, qs_nxt = 0.f, qs_nn = 0.f;
+    float qs_cur = has_cur ? row_scale(cur.b) : 0.f, qs_nxt = 0.f;
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(12));
@@ -626,7 +671,6 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     int n_tiles = 0;
     for (int j = 0; ok && has_cur; ++j) {
       const bool has_nn = has_nxt && w.next(nn);
-      if (has_nn) qs_nn = row_scale(nn.b);
       // full scores of tile j: this thread's partial + the peer's
       const int xb = j & 1;
       ok = mbar_wait(bar(16 + 8 * xb + sw), (j >> 1) & 1);
@@ -646,40 +690,33 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       int lim = cur.rem;
       if (p.q_len > 1) lim -= p.q_len - 1 - ((cur.b % p.steps) * p.fold + (h >> p.h_shift));
       float mx = -INFINITY;
-      float Gt = 1.f;  // fp8: the gain this tile alone would take
-      // fp8: the stage's 64 token scales (landed with its codes; the wait on the
-      // stage's barrier makes them visible), read from shared memory each time
+      float Gj = 1.f;  // fp8: the gain G of this tile (from the scale warp)
+      // fp8: the stage's 64 token scales x G (prepared by the scale warp; rows
+      // past the end hold 0), read from shared memory where needed
       const float4* sc4 = reinterpret_cast<const float4*>(smem + kOffStages + (j % kStages) * kStageB +
                                                           kOffScalesF8) + hf * 8;
+      float qg = 0.f;  // fp8: the query row's scale / G (its scores' factor in log2 units)
       if constexpr (kF8) {
-        ok = mbar_wait(bar(j % kStages), (j / kStages) & 1);
+        ok = mbar_wait(bar(36 + j % kStages), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const float4* all4 = sc4 - hf * 8;
-        const int valid = cur.valid();
-        float cmax = 1e-30f;
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 v = all4[c4];
-          const int t0 = c4 * 4;
-          cmax = fmax3(cmax, t0 < valid ? v.x : 0.f, t0 + 1 < valid ? v.y : 0.f);
-          cmax = fmax3(cmax, t0 + 2 < valid ? v.z : 0.f, t0 + 3 < valid ? v.w : 0.f);
-        }
-        // 2^(8 - e) with 2^e the smallest power of two >= cmax
-        const uint32_t bits = __float_as_uint(cmax);
-        const int e = static_cast<int>((bits >> 23) & 0xffu) - 127 + ((bits & 0x7fffffu) != 0u ? 1 : 0);
-        Gt = __uint_as_float(static_cast<uint32_t>(127 + 8 - e) << 23);
-        const float qsc = qs_cur;
+        Gj = *reinterpret_cast<const float*>(smem + kOffStages + (j % kStages) * kStageB + kOffGainF8);
+        qg = qs_cur * __frcp_rn(Gj);  // G is a power of two: exact
+        // s = S x key-token scale x G here; the row's factor qg (> 0) applies
+        // in the exponent and to the row maximum
 #pragma unroll
         for (int c4 = 0; c4 < kTokHalf / 4; ++c4) {
           const float4 v = sc4[c4];
-          const float cv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = 4 * c4 + k;
-            s[c] = hf * kTokHalf + c < lim ? s[c] * (qsc * cv[k]) : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-          }
+          const float2 a = make_float2(s[4 * c4] * v.x, s[4 * c4 + 1] * v.y);  // scalar: packed pairs spill
+          const float2 b = make_float2(s[4 * c4 + 2] * v.z, s[4 * c4 + 3] * v.w);
+          const int c = hf * kTokHalf + 4 * c4;
+          s[4 * c4] = c < lim ? a.x : -INFINITY;
+          s[4 * c4 + 1] = c + 1 < lim ? a.y : -INFINITY;
+          s[4 * c4 + 2] = c + 2 < lim ? b.x : -INFINITY;
+          s[4 * c4 + 3] = c + 3 < lim ? b.y : -INFINITY;
+          mx = fmax3(mx, s[4 * c4], s[4 * c4 + 1]);
+          mx = fmax3(mx, s[4 * c4 + 2], s[4 * c4 + 3]);
         }
+        mx *= qg;
       } else {
 #pragma unroll
         for (int c = 0; c < kTokHalf; ++c) {
@@ -692,72 +729,98 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         if (!pair_exchange(mx, mo)) { ok = false; break; }
         mx = fmaxf(mx, mo);
       }
-      // PV(j-1) done: P and O are free; finish the previous sequence if it ended
-      if (j > 0) {
-        ok = mbar_wait(bar(11), (j - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        if (prev_last && !epilogue(prev, m, l, 1.0f / G)) { ok = false; break; }
-      }
-      if (cur.first) {
-        m = mx;
-        l = 0.f;
-        G = Gt;
-      } else {
-        // both warps of the quarter see the same row maxima: same decision;
-        // fp8: a tile with a larger scale lowers G for every row alike
-        const bool grow = __any_sync(0xffffffffu, mx > m + (kF8 ? kSlackF8 : kSlackM));
-        if (grow || Gt < G) {
-          const float mnew = grow ? fmaxf(m, mx) : m;
-          const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
-          const float gnew = fminf(G, Gt);
-          const float beta = alpha * (gnew / G);  // O carries G, l does not
-          m = mnew;
-          l *= alpha;
-          G = gnew;
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t u[16];
-            tmem_ld16(trow + kTO + hf * 128 + c0, u);
-            tmem_wait_ld();
+      // Rescale O and l to a new maximum (both warps of the quarter see the
+      // same row maxima: same decision) and, fp8, to a lower gain G (a tile
+      // with a larger scale lowers G for every row alike).
+      auto rescale_to = [&](float mnew, float gnew) {
+        const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mnew);
+        const float beta = alpha * (gnew / G);  // O carries G, l does not
+        m = mnew;
+        l *= alpha;
+        G = gnew;
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+          uint32_t u[16];
+          tmem_ld16(trow + kTO + hf * 128 + c0, u);
+          tmem_wait_ld();
 #pragma unroll
-            for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * beta);
-            tmem_st16(trow + kTO + hf * 128 + c0, u);
-          }
-          tmem_wait_st();
+          for (int x = 0; x < 16; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * beta);
+          tmem_st16(trow + kTO + hf * 128 + c0, u);
+        }
+        tmem_wait_st();
+      };
+      if constexpr (kF8) {
+        const bool grow = !cur.first && __any_sync(0xffffffffu, mx > m + kSlackF8);
+        const bool rescale = !cur.first && (grow || Gj < G);
+        // O complete (PV(j-1) done) to finish the previous sequence or to
+        // rescale; otherwise only P's buffer must be free: PV(j-2)
+        if (j > 0 && (prev_last || rescale)) {
+          ok = mbar_wait(b_pvdone(j - 1), ph(j - 1));
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          if (prev_last && !epilogue(prev, m, l, 1.0f / G)) { ok = false; break; }
+        } else if (j > 1) {
+          ok = mbar_wait(b_pvdone(j - 2), ph(j - 2));
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (cur.first) {
+          m = mx;
+          l = 0.f;
+          G = Gj;
+        } else if (rescale) {
+          rescale_to(grow ? fmaxf(m, mx) : m, fminf(G, Gj));
+        }
+      } else {
+        // PV(j-1) done: P and O are free; finish the previous sequence if it ended
+        if (j > 0) {
+          ok = mbar_wait(b_pvdone(j - 1), ph(j - 1));
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          if (prev_last && !epilogue(prev, m, l, 1.0f)) { ok = false; break; }
+        }
+        if (cur.first) {
+          m = mx;
+          l = 0.f;
+        } else if (__any_sync(0xffffffffu, mx > m + kSlackM)) {
+          rescale_to(fmaxf(m, mx), 1.f);
         }
       }
       const float ms = m == -INFINITY ? 0.f : m;
       float ls = 0.f;
       if constexpr (kF8) {
-        // P = exp2(s - m) * scale * G in two e4m3 terms: hi = e4m3(P),
-        // lo = e4m3(P - hi); token t at byte t % 4 of column t / 4, hi in
-        // columns [0, 16), lo in [16, 32)
-        uint32_t hi[8], lo[8];
+        // P = exp2(s * row scale - m) * key scale * G in two e4m3 terms:
+        // hi = e4m3(P), lo = e4m3(P - hi), the difference taken in f16 (exact:
+        // hi has 4 significant bits, P in f16 11); token t at byte t % 4 of
+        // column t / 4, hi in columns [0, 16), lo in [16, 32)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          uint32_t hw = 0u, lw = 0u;
+        for (int half = 0; half < 2; ++half) {  // 16 tokens (4 columns of hi and of lo) at a time
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int xx = 0; xx < 4; ++xx) {
+          const int x = half * 4 + xx;
           const float4 v = sc4[x];
-          const float cg[4] = {v.x * G, v.y * G, v.z * G, v.w * G};
+          uint32_t hw[2], lw[2];
 #pragma unroll
-          for (int k = 0; k < 4; k += 2) {
-            const int t = 4 * x + k;
-            const float e0 = fast_exp2(s[t] - ms), e1 = fast_exp2(s[t + 1] - ms);
-            ls += e0 + e1;
-            // masked tokens (e = 0) may carry a NaN scale: their weight is 0
-            const float w0 = e0 > 0.f ? e0 * cg[k] : 0.f;
-            const float w1 = e1 > 0.f ? e1 * cg[k + 1] : 0.f;
-            const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(w0, w1), __NV_SATFINITE, __NV_E4M3);
-            const float2 hb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+          for (int k = 0; k < 2; ++k) {
+            const float2 ee = make_float2(fast_exp2(fmaf(s[4 * x + 2 * k], qg, -ms)),
+                                          fast_exp2(fmaf(s[4 * x + 2 * k + 1], qg, -ms)));
+            ls += ee.x + ee.y;
+            const float2 w = make_float2(ee.x * (k == 0 ? v.x : v.z), ee.y * (k == 0 ? v.y : v.w));
+            const __half2 wh = __floats2half2_rn(w.x, w.y);
+            const __nv_fp8x2_storage_t h2 =
+                __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(wh), __NV_SATFINITE, __NV_E4M3);
+            const __half2 r = __hsub2(wh, __half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
             const __nv_fp8x2_storage_t l2 =
-                __nv_cvt_float2_to_fp8x2(make_float2(w0 - hb.x, w1 - hb.y), __NV_SATFINITE, __NV_E4M3);
-            hw |= static_cast<uint32_t>(h2) << (8 * k);
-            lw |= static_cast<uint32_t>(l2) << (8 * k);
+                __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(r), __NV_SATFINITE, __NV_E4M3);
+            hw[k] = h2;
+            lw[k] = l2;
           }
-          hi[x] = hw;
-          lo[x] = lw;
+          hi[xx] = hw[0] | (hw[1] << 16);
+          lo[xx] = lw[0] | (lw[1] << 16);
         }
-        tmem_st8(trow + kTPF8 + hf * 8, hi);
-        tmem_st8(trow + kTPF8 + 16 + hf * 8, lo);
+        tmem_st4(trow + kTPF8 + (j & 1) * 32 + hf * 8 + half * 4, hi);
+        tmem_st4(trow + kTPF8 + (j & 1) * 32 + 16 + hf * 8 + half * 4, lo);
+        }
       } else {
         uint32_t u[16];
 #pragma unroll
@@ -789,20 +852,21 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(10));
+      if (lane == 0) mbar_arrive(b_pfull(j));
       prev = cur;
       prev_last = cur.last;
       cur = nxt;
       has_cur = has_nxt;
       nxt = nn;
       has_nxt = has_nn;
+      // the scale of the tile after next loads now, a whole tile ahead of its use
       qs_cur = qs_nxt;
-      qs_nxt = qs_nn;
+      if (kF8 && has_nxt) qs_nxt = row_scale(nxt.b);
       n_tiles = j + 1;
     }
     if (ok && prev_last) {
       // the last tile's PV, then the last sequence's epilogue
-      ok = mbar_wait(bar(11), (n_tiles - 1) & 1);
+      ok = mbar_wait(b_pvdone(n_tiles - 1), ph(n_tiles - 1));
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         ok = epilogue(prev, m, l, 1.0f / G);
