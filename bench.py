@@ -24,7 +24,8 @@ from __future__ import annotations
 import os
 import sys
 
-# The CPU oracle runs single-threaded: pin BLAS threads before numpy loads.
+# The CPU oracle runs one sequence chunk per host thread, each with a
+# single-threaded BLAS: pin BLAS threads before numpy loads.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -37,6 +38,7 @@ import re
 import statistics
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -63,6 +65,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="llama3_8b_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --workload (the default line also times every other workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run for ncu: one pool copy, no e2e / CPU baseline / clock sampling")
@@ -82,7 +86,7 @@ class ClockSampler:
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
-    def __init__(self, index: int, period_s: float = 0.002):
+    def __init__(self, index: int, period_s: float = 0.0005):
         self.ok = False
         self.samples = []
         self.period = period_s
@@ -328,29 +332,77 @@ def sample_bytes(case, idx):
     return tokens * case.H_kv * (case.D + case.Dv) * es
 
 
-def time_oracle(case, idx, budget_s: float):
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def host_cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else the Arm
+    implementer / part codes)."""
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    m = re.search(r"^model name\s*:\s*(.+)$", text, re.M)
+    if m:
+        return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)", text, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", text, re.M)
+    if imp and part:
+        return f"Arm CPU implementer {imp.group(1)} part {part.group(1)}"
+    return "unknown"
+
+
+class OraclePool:
+    """The oracle over a sample of sequences on all host threads: the sample
+    is split into one chunk per thread, and numpy's BLAS calls and array
+    operations (which release the interpreter lock) run concurrently."""
+
+    def __init__(self, case, idx, threads: int):
+        self.case = case
+        chunks = [c for c in np.array_split(np.asarray(idx), max(1, min(threads, len(idx)))) if len(c)]
+        self.views = [workloads.oracle_view(case, c) for c in chunks]
+        self.ex = ThreadPoolExecutor(max_workers=len(self.views))
+        self.threads = len(self.views)
+
+    def run(self):
+        list(self.ex.map(lambda v: oracle_pass(v, self.case), self.views))
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def time_oracle(case, idx, budget_s: float, threads: int = 1):
     """Seconds per oracle pass over sequences idx (repeated up to budget_s)."""
-    view = workloads.oracle_view(case, idx)
+    pool = OraclePool(case, idx, threads)
     reps, t_total = 0, 0.0
     while (t_total < budget_s or reps == 0) and reps < 1000:
         t = time.perf_counter()
-        oracle_pass(view, case)
+        pool.run()
         t_total += time.perf_counter() - t
         reps += 1
+    pool.close()
     return t_total / reps, reps
 
 
 def cpu_baseline(case, budget_s: float = 12.0):
-    """The oracle (fp64 numpy, one BLAS thread) on a bounded sample of the workload."""
+    """The oracle (fp64 numpy) on all host threads over a bounded sample of the workload."""
+    threads = host_threads()
     t1, _ = time_oracle(case, [int(np.argmin(case.attended_lens))], 0.0)
     per_seq_est = max(t1, 1e-4) * case.attended_lens.mean() / max(1, case.attended_lens.min())
-    n = int(max(1, min(case.B, budget_s / 2 / per_seq_est)))
+    n = int(max(min(case.B, threads), min(case.B, threads * budget_s / 3 / per_seq_est)))
     idx = workloads.sample_sequences(case, n)[:n] if n < case.B else np.arange(case.B)
-    sec, reps = time_oracle(case, idx, budget_s)
+    sec, reps = time_oracle(case, idx, budget_s, threads)
+    used = min(threads, len(idx))
     nbytes = sample_bytes(case, idx)
-    return {"value": nbytes / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": nbytes / sec / 1e9, "unit": UNIT, "cores": used, "kind": "oracle", "cpu": host_cpu_model(),
+            "host_threads": threads,
             "sample": f"{len(idx)} of {case.B} sequences ({int(case.attended_lens[idx].sum())} tokens) x {reps} passes, "
-                      f"fp64 numpy, 1 BLAS thread; bytes counted flat (no prefix sharing)",
+                      f"fp64 numpy split over {used} threads (one BLAS thread each); bytes counted flat "
+                      f"(no prefix sharing)",
             "query_tokens_per_s": len(idx) * case.q_len / sec}
 
 
@@ -361,22 +413,27 @@ def run_reference(args):
     case = build_workload(args.workload, "cpu", small=args.workload in ("cascade", "mla", "cascade_nested",
                                                                         "mla_spec_q4", "spec_tree") or
                           args.workload.startswith("spec_verify") or args.workload.endswith("fp8"))
-    # size each step's sample so the whole run stays within ~2 minutes
+    # size each step's sample so the whole run stays within ~2 minutes, on
+    # all host threads (one chunk of the step's sequences each)
+    threads = host_threads()
     t1, _ = time_oracle(case, [0], 0.0)
     per_seq = max(t1, 1e-4)
-    n_seq = int(max(1, min(case.B, 120.0 / max(1, args.steps + args.warmup) / per_seq)))
-    views = []
+    n_seq = int(max(1, min(case.B, threads * 120.0 / max(1, args.steps + args.warmup) / per_seq)))
+    pools = []
     for s in range(min(case.B, 8)):
         idx = (np.arange(n_seq) + s * n_seq) % case.B
-        views.append((idx, workloads.oracle_view(case, idx)))
+        pools.append((idx, OraclePool(case, idx, threads)))
     for i in range(args.warmup):
-        oracle_pass(views[i % len(views)][1], case)
+        pools[i % len(pools)][1].run()
     total_bytes, t0 = 0, time.perf_counter()
     for i in range(args.steps):
-        idx, v = views[i % len(views)]
-        oracle_pass(v, case)
+        idx, pool = pools[i % len(pools)]
+        pool.run()
         total_bytes += sample_bytes(case, idx)
     el = time.perf_counter() - t0
+    used = pools[0][1].threads
+    for _, pool in pools:
+        pool.close()
     value = total_bytes / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -385,8 +442,9 @@ def run_reference(args):
         "data": "synthetic", "config": {"workload": case.name, "B": case.B, "H_q": case.H_q, "H_kv": case.H_kv,
                                         "D": case.D, "page_size": case.page_size,
                                         "sample_sequences_per_step": n_seq},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n_seq} of {case.B} sequences per step, fp64 numpy, 1 BLAS thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "cpu": host_cpu_model(),
+                         "sample": f"{n_seq} of {case.B} sequences per step, fp64 numpy split over {used} "
+                                   f"threads (one BLAS thread each)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -515,9 +573,39 @@ def run_ours(args):
         ts_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    case = build_workload(args.workload, dev, scale=args.batch_scale)
     if args.profile:
         args.no_e2e = args.no_cpu_baseline = True
+    line = measure(ts, args, args.workload, args.steps, args.warmup, dev, rank, world, dist, headline=True)
+    # Every other workload in the same process (the default invocation, one
+    # GPU): each entry is timed like the headline (warm-up, K timed steps with
+    # CUDA events, inputs larger than L2, clocks sampled during the timed
+    # region, the launch trace in a separate pass), without the end-to-end and
+    # CPU legs.
+    if line is not None and world == 1 and not args.profile and not args.no_extra and \
+            args.workload == "llama3_8b_layer":
+        extra = {}
+        for w in WORKLOADS:
+            if w == args.workload:
+                continue
+            torch.cuda.empty_cache()
+            d = measure(ts, args, w, min(args.steps, 50), max(3, min(args.warmup, 5)), dev, rank, world, dist,
+                        headline=False)
+            extra[w] = {k: d[k] for k in ("ms_per_step", "value", "unit", "query_tokens_per_s", "roofline",
+                                          "kernels", "clocks", "config", "gpu_launches", "device_error_word",
+                                          "tensor", "flat_equivalent_gbs", "dtype") if k in d}
+            extra[w]["steps"] = min(args.steps, 50)
+            extra[w]["warmup"] = max(3, min(args.warmup, 5))
+        line["workloads"] = extra
+    if line is not None:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure(ts, args, workload, steps, warmup, dev, rank, world, dist, headline):
+    """Time one workload on this rank; returns the bench line (rank 0) or None."""
+    case = build_workload(workload, dev, scale=args.batch_scale)
     pool_bytes = case.k_pool.numel() * case.k_pool.element_size() * (2 if case.v_pool is not None else 1)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     rotate = 1 if args.profile else max(2, int(math.ceil(4 * l2 / pool_bytes)) if pool_bytes < 4 * l2 else 2)
@@ -531,7 +619,7 @@ def run_ours(args):
     else:
         nbytes, flops = algorithmic(case, runner.groups)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         runner.step(i, stream=stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
@@ -543,7 +631,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         # no events between steps: consecutive kernels may overlap through
         # programmatic dependent launch, as in a serving loop
         runner.step(i, stream=stream)
@@ -552,14 +640,14 @@ def run_ours(args):
     t_wall1 = time.perf_counter()
     barrier(dist)
     sampler.stop()
-    ms_step = max_over_ranks(start.elapsed_time(end), dist, dev) / args.steps
+    ms_step = max_over_ranks(start.elapsed_time(end), dist, dev) / steps
     err_word = ts.ts_read_device_error(runner.ws)
 
     # per-kernel device times: a second timed pass with the library's launch
     # trace on (CUDA events recorded around each of its launches, on the
     # launching stream); kept apart from the pass above, whose step time the
     # extra event records would perturb
-    n_tr = min(args.steps, 50)
+    n_tr = min(steps, 50)
     ts.ts_trace_collect()
     ts.ts_trace_enable(True)
     for i in range(n_tr):
@@ -577,7 +665,7 @@ def run_ours(args):
     # end to end through the public API with host buffers (pinned): the step's
     # inputs go up, its output comes back, every step
     e2e = None
-    if not args.no_e2e:
+    if headline and not args.no_e2e:
         hin = {"q": case.q.cpu().pin_memory(), "bt": torch.from_numpy(case.block_table).pin_memory(),
                "lens": torch.from_numpy(case.attn_lens).pin_memory()}
         if case.append:
@@ -674,9 +762,9 @@ def run_ours(args):
             return groups
 
         regroups = runner.groups is not None or runner.forest is not None
-        n_e2e = min(args.steps, 50) if regroups else (args.steps + UNROLL - 1) // UNROLL * UNROLL
+        n_e2e = min(steps, 50) if regroups else (steps + UNROLL - 1) // UNROLL * UNROLL
         groups = group_on_host() if regroups else None
-        for i in range(min(args.warmup, 3)):
+        for i in range(min(warmup, 3)):
             groups = e2e_step(i, stream, groups)
         torch.cuda.synchronize()
         # A serving loop replays its decode steps from a CUDA graph: capture
@@ -717,9 +805,7 @@ def run_ours(args):
             e2e["host_grouping_ms"] = statistics.median(host_group_ms)
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return 0
+        return None
     peaks = {}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -741,10 +827,10 @@ def run_ours(args):
     source = {"mla_decode_kernel": "ts_mla.cu", "cascade_prefix_kernel": "ts_cascade.cu",
               "mq_tc_kernel": "ts_mq_tc.cu"}.get(dom, "ts_paged_decode_kernel.cuh")
     hbm_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(f"{dom}__{args.workload}.md", source)
+    traffic = kernel_traffic(f"{dom}__{workload}.md", source)
     if case.mla:
         tflops = dom_flops / (dom_ms * 1e-3) / 1e12
-        fp8 = args.workload in FP8_TENSOR
+        fp8 = workload in FP8_TENSOR
         peak = tc_peak * (2.0 if fp8 else 1.0)
         roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                     "frac": tflops / peak,
@@ -758,8 +844,8 @@ def run_ours(args):
                     "frac": hbm_achieved / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
                     "kernel": dom, "kernel_ms": dom_ms, "bytes_per_launch": dom_bytes, "traffic": traffic}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": ("e4m3 q and latent" if case.kv_fp8 and case.mla else
                                        "e4m3 K/V, bf16 q" if case.kv_fp8 else
                                        "bf16" if case.dtype == "bf16" else "f32"), "accumulate": "f32",
@@ -774,7 +860,7 @@ def run_ours(args):
         "hbm_frac_of_8tbs": value / world / 8000.0,
         "roofline": roofline,
         "kernels": kernels,
-        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "gpu_launches": int(round(launches_per_step * steps)),
         "device_error_word": err_word,
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
@@ -799,12 +885,9 @@ def run_ours(args):
         line["flat_equivalent_gbs"] = flat / (ms_step * 1e-3) / 1e9
     if e2e is not None:
         line["e2e"] = e2e
-    if not args.no_cpu_baseline and world == 1:
+    if headline and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(case)
-    print(json.dumps(line))
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
 def main():

@@ -59,3 +59,16 @@ def test_two_gloo_ranks_agree_on_the_slowest_time():
     assert all(o[1] == world for o in out)
     assert all(o[2] == 2.0 for o in out)  # max over ranks of 1.0 + rank
     assert out[1][3] == 0                  # rank 1 returns 0 from the reference arm without work
+
+
+def test_cpu_baseline_uses_host_threads_and_names_the_cpu():
+    """The oracle baseline runs on every host thread it may use and records
+    the thread count and the CPU model."""
+    import workloads
+    bench = _bench()
+    case = workloads.build_case("cpu_base", 3, B=6, H_q=8, H_kv=2, D=64, page_size=16, seq_lens=[40, 17, 90, 5, 64, 33],
+                                dtype="f32", scale=0.125)
+    b = bench.cpu_baseline(case, budget_s=0.2)
+    assert b["kind"] == "oracle" and b["value"] > 0
+    assert 1 <= b["cores"] <= bench.host_threads() and b["cores"] == min(bench.host_threads(), 6)
+    assert isinstance(b["cpu"], str) and b["cpu"]
