@@ -551,8 +551,8 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       }
       tmem_wait_st();
     };
-    // fp8: the query row's scale times scale * log2(e), for the tile being
-    // scored and the next one (loaded a tile ahead)
+    // fp8: the query row's scale times scale * log2(e) (read where it is used:
+    // a register kept a tile ahead made the softmax spill more)
     auto row_scale = [&](int b) {
       return kF8 ? p.q_scale[static_cast<int64_t>(b) * kH + h] * p.scale_log2 : p.scale_log2;
     };
@@ -656,12 +656,10 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
     Tile cur, nxt, nn, prev;
     bool has_cur = w.next(cur);
     if (has_cur) load_q(cur.b);
-    float qs_cur = has_cur ? row_scale(cur.b) : 0.f, qs_nxt = 0.f;
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(12));
     bool has_nxt = has_cur && w.next(nxt);
-    if (has_nxt) qs_nxt = row_scale(nxt.b);
     if (has_cur) ok = send_next(0, has_nxt && nxt.first, nxt.b);
     float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
     // fp8: gain G (a power of two) applied to P so that P <= 2^8 under the
@@ -700,7 +698,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
         ok = mbar_wait(bar(36 + j % kStages), (j / kStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         Gj = *reinterpret_cast<const float*>(smem + kOffStages + (j % kStages) * kStageB + kOffGainF8);
-        qg = qs_cur * __frcp_rn(Gj);  // G is a power of two: exact
+        qg = row_scale(cur.b) * __frcp_rn(Gj);  // G is a power of two: exact
         // s = S x key-token scale x G here; the row's factor qg (> 0) applies
         // in the exponent and to the row maximum
 #pragma unroll
@@ -859,9 +857,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1) mla_decode_kernel(const MlaPar
       has_cur = has_nxt;
       nxt = nn;
       has_nxt = has_nn;
-      // the scale of the tile after next loads now, a whole tile ahead of its use
-      qs_cur = qs_nxt;
-      if (kF8 && has_nxt) qs_nxt = row_scale(nxt.b);
+
       n_tiles = j + 1;
     }
     if (ok && prev_last) {
