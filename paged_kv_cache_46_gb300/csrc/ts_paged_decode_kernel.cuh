@@ -571,7 +571,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int l = lane % C::kLPT;
   const int tokens_per_pass = C::kNG * C::kTPG;
   const int npass = (p.chunk_rows + tokens_per_pass - 1) / tokens_per_pass;
-  const int H_kv = p.H_kv;
 
   int dim_off[C::kNV];
   uint32_t lane_off[C::kNV];  // byte offset of this lane's vectors within a token row

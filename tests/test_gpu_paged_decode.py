@@ -137,6 +137,8 @@ def test_one_workspace_serves_calls_with_different_cuts(ctas):
 @pytest.mark.parametrize("dtype,D,H_q,H_kv,ps", [
     ("f32", 64, 8, 2, 16), ("f32", 128, 8, 8, 16), ("bf16", 64, 8, 8, 16), ("bf16", 64, 16, 2, 32),
     ("bf16", 128, 64, 8, 16), ("bf16", 128, 8, 1, 8), ("bf16", 64, 4, 4, 16), ("f32", 64, 16, 8, 32),
+    # head dim 64, four query rows per kv head, with 2, 1 and 4 kv heads
+    ("bf16", 64, 8, 2, 16), ("bf16", 64, 4, 1, 8), ("bf16", 64, 16, 4, 32),
 ])
 def test_shapes(dtype, D, H_q, H_kv, ps):
     rng = np.random.default_rng(D + H_q + H_kv + ps)
@@ -158,10 +160,11 @@ def test_edge_cases():
     o_ref, l_ref = oracle_decode(case)
     compare(out, o_ref, "bf16", lse, l_ref, "one token")
     # all sequences empty
-    case = workloads.build_case("all_empty", 42, B=5, H_q=8, H_kv=2, D=64, page_size=16, seq_lens=[0] * 5,
-                                dtype="f32", scale=0.1, device=DEV)
-    out, lse, _ = _run_decode(case)
-    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+    for dt in ("f32", "bf16"):
+        case = workloads.build_case("all_empty", 42, B=5, H_q=8, H_kv=2, D=64, page_size=16, seq_lens=[0] * 5,
+                                    dtype=dt, scale=0.1, device=DEV)
+        out, lse, _ = _run_decode(case)
+        assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
     # one long sequence among short ones: cut across most CTAs
     lens = [3] * 20 + [60000] + [7] * 20
     case = workloads.build_case("long_among_short", 43, B=len(lens), H_q=32, H_kv=8, D=64, page_size=16,
@@ -171,18 +174,19 @@ def test_edge_cases():
     compare(out, o_ref, "bf16", lse, l_ref, "long among short")
 
 
-def test_out_of_range_page_is_flagged_not_dereferenced():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_out_of_range_page_is_flagged_not_dereferenced(dtype):
     """A bad page id is caught by the kernel's bounds check: the error word gets
     TS_DEVERR_PAGE_RANGE, nothing faults, other sequences stay correct."""
     case = workloads.build_case("bad_page", 51, B=4, H_q=8, H_kv=2, D=64, page_size=16,
-                                seq_lens=[40, 20, 33, 9], dtype="f32", scale=0.125, device=DEV)
+                                seq_lens=[40, 20, 33, 9], dtype=dtype, scale=0.125, device=DEV)
     case.block_table = case.block_table.copy()
     case.block_table[1, 0] = case.num_pages + 5
     out, lse, err = _run_decode(case, check_error_word=False)
     assert err & ts.TS_DEVERR_PAGE_RANGE
     good = np.array([0, 2, 3])
     o_ref, l_ref = oracle_decode(case, seq_idx=good)
-    compare(out[torch.from_numpy(good).to(DEV)], o_ref, "f32", lse[torch.from_numpy(good).to(DEV)], l_ref,
+    compare(out[torch.from_numpy(good).to(DEV)], o_ref, dtype, lse[torch.from_numpy(good).to(DEV)], l_ref,
             "bad page neighbours")
 
 
