@@ -140,6 +140,24 @@ class ClockSampler:
         return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside)}
 
 
+def device_clock(a, b):
+    """Median over SMs of the average SM clock between two clock-stamp
+    calls (cycle difference / timer difference, matched by SM)."""
+    first = {}
+    for sm, clk, ns in a.cpu().tolist():
+        first.setdefault(sm, (clk, ns))
+    mhz, window = [], []
+    for sm, clk, ns in b.cpu().tolist():
+        if sm in first and ns > first[sm][1]:
+            mhz.append((clk - first[sm][0]) / (ns - first[sm][1]) * 1e3)
+            window.append((ns - first[sm][1]) / 1e3)
+            del first[sm]
+    if not mhz:
+        return {"sm_mhz_device": None}
+    return {"sm_mhz_device": round(statistics.median(mhz), 1), "sm_mhz_device_min": round(min(mhz), 1),
+            "device_sms": len(mhz), "device_window_us": round(statistics.median(window), 1)}
+
+
 # --------------------------------------------------------------------------
 # helpers
 # --------------------------------------------------------------------------
@@ -626,16 +644,22 @@ def measure(ts, args, workload, steps, warmup, dev, rank, world, dist, headline)
     if args.profile:
         sampler.ok = False
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # per-SM clock stamps right before and after the timed work (outside its
+    # events): each SM's average clock over the timed region
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    stamps = [torch.zeros(2 * n_sm, 3, dtype=torch.int64, device=dev) for _ in range(2)]
     sampler.start()
     barrier(dist)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
+    ts.ts_clock_stamp(stamps[0], stream)
     start.record(stream)
     for i in range(steps):
         # no events between steps: consecutive kernels may overlap through
         # programmatic dependent launch, as in a serving loop
         runner.step(i, stream=stream)
     end.record(stream)
+    ts.ts_clock_stamp(stamps[1], stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     barrier(dist)
@@ -862,7 +886,7 @@ def measure(ts, args, workload, steps, warmup, dev, rank, world, dist, headline)
         "kernels": kernels,
         "gpu_launches": int(round(launches_per_step * steps)),
         "device_error_word": err_word,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": {**sampler.summary(t_wall0, t_wall1), **device_clock(stamps[0], stamps[1])},
     }
     if flops and "cascade_prefix_kernel" in kernels:
         # all prefix launches of a step (one per level of a nested forest)

@@ -648,6 +648,22 @@ typedef struct {
 TS_API ts_status ts_trace_enable(int32_t on);
 TS_API int32_t ts_trace_collect(ts_launch_record* out, int32_t capacity);
 
+/*
+ * ts_clock_stamp - a measurement aid (the pages have no counterpart):
+ * enqueues on `stream` a kernel of n CTAs whose first thread each writes
+ * three uint64 values to stamps[3 i], stamps[3 i + 1], stamps[3 i + 2]: the
+ * SM it ran on (%smid), that SM's cycle counter (%clock64) and the global
+ * nanosecond timer (%globaltimer), read back to back. Two calls around a
+ * stretch of work on the same stream give each SM's average clock over it:
+ * the cycle difference over the timer difference, matched by SM. The CTAs
+ * of one call usually land on distinct SMs; with n = 2 x the SM count
+ * nearly every SM is covered.
+ * stamps: device memory of 3 n uint64, 8-byte aligned, owned by the caller;
+ * n in [1, 65535]. TS_ERR_INVALID_ARG for a null or unaligned pointer or n
+ * out of range (nothing is enqueued); TS_ERR_CUDA if the launch fails.
+ */
+TS_API ts_status ts_clock_stamp(void* stamps, int32_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

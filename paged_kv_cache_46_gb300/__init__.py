@@ -122,6 +122,7 @@ _SIGNATURES = {
     "ts_read_device_error": (ctypes.c_int, [_VP, _U32P, _VP]),
     "ts_trace_enable": (ctypes.c_int, [_I32]),
     "ts_trace_collect": (_I32, [ctypes.POINTER(LaunchRecordC), _I32]),
+    "ts_clock_stamp": (ctypes.c_int, [_VP, _I32, _VP]),
 }
 
 _lib = None
@@ -600,6 +601,14 @@ def ts_read_device_error(workspace, stream=None) -> int:
 
 def ts_trace_enable(on: bool) -> None:
     _check(lib().ts_trace_enable(1 if on else 0))
+
+
+def ts_clock_stamp(stamps, stream=None) -> None:
+    """Enqueues one clock stamp per row of ``stamps`` (an int64 device tensor
+    [n, 3]): SM id, that SM's cycle counter, global timer in ns."""
+    if stamps.dtype != torch.int64 or stamps.dim() != 2 or stamps.shape[1] != 3 or not stamps.is_contiguous():
+        raise TSError(TS_ERR_INVALID_ARG, "ts_clock_stamp: stamps must be a contiguous int64 tensor [n, 3]")
+    _check(lib().ts_clock_stamp(_ptr(stamps), stamps.shape[0], _stream(stream)))
 
 
 def ts_trace_collect(capacity: int = 4096):

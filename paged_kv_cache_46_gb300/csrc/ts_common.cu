@@ -115,6 +115,23 @@ int device_sm_count() {
 
 }  // namespace ts
 
+namespace ts {
+namespace {
+// One stamp per CTA: the SM it runs on, that SM's cycle counter and the
+// global nanosecond timer, read back to back by the CTA's first thread.
+__global__ void clock_stamp_kernel(unsigned long long* out) {
+  if (threadIdx.x != 0) return;
+  unsigned int sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  const unsigned long long clk = clock64();
+  const unsigned long long ns = globaltimer_ns();
+  out[3 * blockIdx.x] = sm;
+  out[3 * blockIdx.x + 1] = clk;
+  out[3 * blockIdx.x + 2] = ns;
+}
+}  // namespace
+}  // namespace ts
+
 extern "C" {
 
 const char* ts_status_string(int status) {
@@ -169,6 +186,16 @@ int32_t ts_trace_collect(ts_launch_record* out, int32_t capacity) {
     return -1;
   }
   return n;
+}
+
+ts_status ts_clock_stamp(void* stamps, int32_t n, void* stream) {
+  if (stamps == nullptr || n < 1 || n > 65535)
+    return ts::fail(TS_ERR_INVALID_ARG, "ts_clock_stamp: stamps=%p n=%d (n in [1, 65535])", stamps, n);
+  if (reinterpret_cast<uintptr_t>(stamps) % 8 != 0)
+    return ts::fail(TS_ERR_INVALID_ARG, "ts_clock_stamp: stamps must be 8-byte aligned");
+  ts::clock_stamp_kernel<<<n, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long*>(stamps));
+  return ts::cuda_check(cudaGetLastError(), "ts_clock_stamp launch");
 }
 
 ts_status ts_read_device_error(const void* workspace, uint32_t* error_bits, void* stream) {

@@ -170,3 +170,12 @@ def test_binding_constants_match_the_header():
         v = re.search(rf"#define {name} (0x[0-9a-fA-F]+|\d+)u?", text) or re.search(rf"\b{name}\s*=\s*(0x[0-9a-fA-F]+|\d+)", text)
         assert v, name
         assert int(v.group(1), 0) == getattr(ts, name), name
+
+
+def test_clock_stamp_validates_before_any_launch(lib):
+    """The measurement aid rejects a null or unaligned buffer and a count out
+    of range without enqueueing anything."""
+    assert lib.ts_clock_stamp(None, 4, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_clock_stamp(ctypes.c_void_p(16), 0, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_clock_stamp(ctypes.c_void_p(16), 65536, None) == ts.TS_ERR_INVALID_ARG
+    assert lib.ts_clock_stamp(ctypes.c_void_p(20), 4, None) == ts.TS_ERR_INVALID_ARG
