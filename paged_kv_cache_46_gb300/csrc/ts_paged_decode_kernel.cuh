@@ -65,6 +65,11 @@ struct PagedParams {
   // Sliding-window KV group (plain decode only): a sequence attends its last
   // `window` tokens; 0 = the whole context.
   int32_t window = 0;
+  // Byte offset in dynamic shared memory of an int2 [B] cache of each virtual
+  // sequence's (own length, tokens in front of its own pages), filled by the
+  // prologue and read by the cut and the producer instead of global memory;
+  // 0 = no cache (large batches).
+  uint32_t len_cache_off = 0;
 };
 
 using PagedKernelFn = void (*)(const PagedParams);
@@ -223,6 +228,19 @@ __device__ __forceinline__ int vseq_len(const PagedParams& p, int v) {
   }
 }
 
+// vseq_len, also returning the tokens in front of the sequence's own pages
+// (its shared prefix, or the whole pages in front of its window).
+template <bool kPfx, bool kMulti, bool kWin>
+__device__ __forceinline__ int vseq_len_pre(const PagedParams& p, int v, int& pre) {
+  if constexpr (kMulti) {
+    pre = 0;
+    return vseq_len<kPfx, kMulti, kWin>(p, v);
+  } else {
+    pre = prefix_tokens<kPfx>(p, v) + window_skip<kWin>(p, v);
+    return p.seq_lens[v] - pre;
+  }
+}
+
 // Writes the output of a virtual sequence with no own tokens: O = 0,
 // LSE = -inf, or the prefix state alone in prefix mode. All 32 lanes of a
 // warp call it together; their stores are coalesced.
@@ -262,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   StageDesc* desc = reinterpret_cast<StageDesc*>(smem + 128);
   long long* warp_tot = reinterpret_cast<long long*>(smem + 512);
   int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
+  int2* s_len = p.len_cache_off != 0 ? reinterpret_cast<int2*>(smem + p.len_cache_off) : nullptr;
   unsigned char* stages = smem + p.stages_off;
 
   // Programmatic dependent launch: this kernel may start while the previous
@@ -294,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   long long mine = 0;
   bool has_empty = false;
   for (int b = lo; b < hi; ++b) {
-    const int L = vseq_len<kPfx, kMulti, kWin>(p, b);
+    int pre;
+    const int L = vseq_len_pre<kPfx, kMulti, kWin>(p, b, pre);
+    if (s_len != nullptr) s_len[b] = make_int2(L, pre);
     if (L > 0)
       mine += (L + ps - 1) / ps + A;
     else if (b % G_ctas == k)
@@ -338,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const long long end = start + q_pages + (k < r_pages ? 1 : 0);
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
-    for (int b = lo; b < hi; ++b) {
-      const int L = vseq_len<kPfx, kMulti, kWin>(p, b);
+    for (int b = lo; b < hi; ++b) {  // this thread's own cache entries: no barrier needed
+      const int L = s_len != nullptr ? s_len[b].x : vseq_len<kPfx, kMulti, kWin>(p, b);
       const long long np = L > 0 ? (L + ps - 1) / ps + A : 0;
       if (start < off + np) {
         s_start[0] = b;
@@ -376,6 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         const int bb = base + lane;
         pre_out = 0;
         if (bb >= B) return -1;
+        if (s_len != nullptr) {  // filled by the prologue, before its barriers
+          const int2 e = s_len[bb];
+          pre_out = e.y;
+          return max(e.x, 0);
+        }
         pre_out = prefix_tokens<kPfx>(p, bb) + window_skip<kWin>(p, bb);
         return max(vseq_len<kPfx, kMulti, kWin>(p, bb), 0);
       };
