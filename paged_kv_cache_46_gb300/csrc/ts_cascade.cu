@@ -609,6 +609,7 @@ extern "C" ts_status ts_cascade_decode_attn(const void* q, const void* k_pool, c
   pre.prefix_len = groups->prefix_len;
   pre.prefix_o = prefix_o;
   pre.prefix_lse = prefix_lse;
+  pre.num_groups = G;
   return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q,
                                   H_kv, D, page_size, num_pages, scale, dtype, out, lse, workspace,
                                   ws.tile_offset, s, who, G > 0 ? &pre : nullptr);
@@ -679,6 +680,7 @@ extern "C" ts_status ts_cascade_nested_decode_attn(const void* q, const void* k_
   pre.prefix_len = forest->prefix_len;  // tokens shared through it
   pre.prefix_o = prefix_o;
   pre.prefix_lse = prefix_lse;
+  pre.num_groups = N;
   return launch_paged_decode_impl(q, k_pool, v_pool, block_table, bt_stride, seq_lens, B, H_q, H_kv, D, page_size,
                                   num_pages, scale, dtype, out, lse, workspace, ws.tile_offset, s, who,
                                   N > 0 ? &pre : nullptr);

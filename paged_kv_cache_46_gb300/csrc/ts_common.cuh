@@ -34,6 +34,7 @@ struct PrefixInputs {
   const int32_t* prefix_len;  // [groups] shared tokens (whole pages)
   const float* prefix_o;      // [B, H_q, D] normalised prefix output (fp32)
   const float* prefix_lse;    // [B, H_q] prefix LSE (natural log)
+  int32_t num_groups;         // entries of prefix_len
 };
 
 // Paged split-KV decode (ts_paged_decode.cu); `pre` selects cascade mode.
@@ -94,6 +95,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 // Makes mbarrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy ones (bulk copies, tensor-core operand reads) after a barrier.
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx_bytes) {

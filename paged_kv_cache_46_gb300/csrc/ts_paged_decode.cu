@@ -356,6 +356,20 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
                 who, prm.stage_bytes);
   prm.num_stages = stages;
   const size_t smem = prm.stages_off + static_cast<size_t>(stages) * prm.stage_bytes;
+  // the prologue's entries: the cache, else the stage area if they fit there
+  const uint64_t stage_area = static_cast<uint64_t>(stages) * prm.stage_bytes;
+  const uint64_t entries = 8ull * static_cast<uint64_t>(Bv);
+  prm.len_scratch_off = cache ? prm.len_cache_off : (entries <= stage_area ? prm.stages_off : 0u);
+  // prefix mode: the groups' prefix lengths staged behind the entries
+  prm.num_groups = pre ? pre->num_groups : 0;
+  {
+    const uint64_t at = cache ? 0ull : align_up(entries, 16);
+    prm.plen_scratch_off =
+        (pre != nullptr && prm.len_scratch_off != 0 && pre->num_groups > 0 &&
+         at + 4ull * static_cast<uint64_t>(pre->num_groups) <= stage_area)
+            ? prm.stages_off + static_cast<uint32_t>(at)
+            : 0u;
+  }
 
   // Once per kernel and device: allow the whole stage budget, and check that
   // the kernel was compiled to launch with kLaunchRegs registers per thread

@@ -70,6 +70,14 @@ struct PagedParams {
   // prologue and read by the cut and the producer instead of global memory;
   // 0 = no cache (large batches).
   uint32_t len_cache_off = 0;
+  // Where the prologue keeps the same int2 [B] entries while it cuts the
+  // batch: the cache above, else the stage area (free until the producer's
+  // first copy) when they fit there; 0 = read them from global memory.
+  uint32_t len_scratch_off = 0;
+  // Prefix mode: entries of prefix_len, and where the prologue stages them in
+  // the stage area for its gather (0: read from global memory).
+  int32_t num_groups = 0;
+  uint32_t plen_scratch_off = 0;
 };
 
 using PagedKernelFn = void (*)(const PagedParams);
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   long long* warp_tot = reinterpret_cast<long long*>(smem + 512);
   int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
   int2* s_len = p.len_cache_off != 0 ? reinterpret_cast<int2*>(smem + p.len_cache_off) : nullptr;
+  int2* s_pro = p.len_scratch_off != 0 ? reinterpret_cast<int2*>(smem + p.len_scratch_off) : nullptr;
   unsigned char* stages = smem + p.stages_off;
 
   // Programmatic dependent launch: this kernel may start while the previous
@@ -312,10 +321,64 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const int A = p.seq_units;
   long long mine = 0;
   bool has_empty = false;
+  // More sequences than threads: gather the entries first with consecutive
+  // threads on consecutive sequences (coalesced, independent loads), then sum
+  // each thread's contiguous chunk from shared memory.
+  const bool gathered = s_pro != nullptr && B > static_cast<int>(blockDim.x);
+  if (gathered) {
+    // prefix mode: the groups' prefix lengths first, so that each sequence's
+    // entry needs only independent loads (its length and its group)
+    const int* s_plen = nullptr;
+    if constexpr (kPfx) {
+      if (p.plen_scratch_off != 0) {
+        int* w = reinterpret_cast<int*>(smem + p.plen_scratch_off);
+        for (int g = tid; g < p.num_groups; g += blockDim.x) w[g] = p.prefix_len[g];
+        __syncthreads();
+        s_plen = w;
+      }
+    }
+    // eight sequences per thread at a time: all their loads are issued before
+    // any entry is stored (stores through a generic pointer would otherwise
+    // keep the next loads waiting)
+    constexpr int kBatch = 8;
+    const int nthr = static_cast<int>(blockDim.x);
+    for (int b0 = tid; b0 < B; b0 += kBatch * nthr) {
+      int raw[kBatch], grp[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int b = b0 + u * nthr;
+        raw[u] = b < B ? p.seq_lens[real_seq<kMulti>(p, b)] : 0;
+        grp[u] = (kPfx && b < B) ? p.group_of[b] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int b = b0 + u * nthr;
+        if (b >= B) break;
+        int pre = 0, L;
+        if constexpr (kMulti) {
+          L = raw[u] - p.q_len + (b - real_seq<kMulti>(p, b) * p.steps + 1) * p.fold;
+        } else {
+          if constexpr (kPfx) {
+            const int g = grp[u];
+            pre = g < 0 ? 0 : (s_plen != nullptr ? (g < p.num_groups ? s_plen[g] : 0) : p.prefix_len[g]);
+          }
+          if constexpr (kWin) pre += raw[u] > p.window ? (raw[u] - p.window) & -p.page_size : 0;
+          L = raw[u] - pre;
+        }
+        s_pro[b] = make_int2(L, pre);
+      }
+    }
+    __syncthreads();
+  }
   for (int b = lo; b < hi; ++b) {
-    int pre;
-    const int L = vseq_len_pre<kPfx, kMulti, kWin>(p, b, pre);
-    if (s_len != nullptr) s_len[b] = make_int2(L, pre);
+    int L;
+    if (gathered) {
+      L = s_pro[b].x;
+    } else {
+      int pre;
+      L = vseq_len_pre<kPfx, kMulti, kWin>(p, b, pre);
+      if (s_pro != nullptr) s_pro[b] = make_int2(L, pre);
+    }
     if (L > 0)
       mine += (L + ps - 1) / ps + A;
     else if (b % G_ctas == k)
@@ -359,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   const long long end = start + q_pages + (k < r_pages ? 1 : 0);
   if (start < end && excl <= start && start < excl + mine) {
     long long off = excl;
-    for (int b = lo; b < hi; ++b) {  // this thread's own cache entries: no barrier needed
-      const int L = s_len != nullptr ? s_len[b].x : vseq_len<kPfx, kMulti, kWin>(p, b);
+    for (int b = lo; b < hi; ++b) {  // entries this thread wrote, or gathered before a barrier
+      const int L = s_pro != nullptr ? s_pro[b].x : vseq_len<kPfx, kMulti, kWin>(p, b);
       const long long np = L > 0 ? (L + ps - 1) / ps + A : 0;
       if (start < off + np) {
         s_start[0] = b;
@@ -370,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       off += np;
     }
   }
+  // the stage area's scratch entries are read through the generic proxy; the
+  // producer's bulk copies (async proxy) overwrite them after this barrier
+  if (gathered || (s_pro != nullptr && s_len == nullptr)) fence_async_smem();
   __syncthreads();
 
   if (warp < kFirstConsumerWarp) {

@@ -138,9 +138,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // TMEM allocation (one full warp) and release.
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
