@@ -132,8 +132,6 @@ KernelFn pick_kernel(ts_dtype dt, int D, int g, bool prefix) {
 }
 
 constexpr int kSmemBudget = 227 * 1024;
-// Batches up to this many virtual sequences get the shared-memory length cache.
-constexpr int kLenCacheMaxSeqs = 4096;
 
 // CTAs of the persistent grid: one per SM. TS_PAGED_DECODE_CTAS overrides it
 // (tests use it to sweep how sequences are cut across CTAs).
@@ -319,12 +317,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   while (chunk_rows > 1 &&
          (kSmemBudget - kHeaderBytes - align_up(prm.row_bytes, 128)) / stage_of(chunk_rows) < 2)
     chunk_rows = (chunk_rows + 1) / 2;
-  // The prologue caches every virtual sequence's length in shared memory for
-  // the cut and the producer (saving two dependent global reads at the start
-  // of a launch), when the batch is small enough that the cache costs no stage.
-  const uint32_t fixed_off = static_cast<uint32_t>(kHeaderBytes + align_up(prm.row_bytes, 128));
-  const uint32_t cache_bytes =
-      Bv <= kLenCacheMaxSeqs ? static_cast<uint32_t>(align_up(8ull * static_cast<uint64_t>(Bv), 128)) : 0u;
+
   prm.chunk_rows = chunk_rows;
   // A sequence's fixed cost (query load, epilogue) measured on GB300 is about
   // what its consumers spend on 16 to 24 token rows; one 16-row page came out
@@ -345,25 +338,21 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
     return fail(TS_ERR_UNSUPPORTED, "%s: fp8 stage of %d rows x %d kv heads: scales not a multiple of 16 B",
                 who, chunk_rows, H_kv);
   prm.stage_bytes = stage_of(chunk_rows);
-  const int stages_plain = std::min<int>(kMaxStages, (kSmemBudget - fixed_off) / prm.stage_bytes);
-  const bool cache = cache_bytes != 0 &&
-                     std::min<int>(kMaxStages, (kSmemBudget - fixed_off - cache_bytes) / prm.stage_bytes) == stages_plain;
-  prm.len_cache_off = cache ? fixed_off : 0u;
-  prm.stages_off = fixed_off + (cache ? cache_bytes : 0u);
+  prm.stages_off = static_cast<uint32_t>(kHeaderBytes + align_up(prm.row_bytes, 128));
   const int stages = std::min<int>(kMaxStages, (kSmemBudget - prm.stages_off) / prm.stage_bytes);
   if (stages < 2 || prm.row_bytes > 4096)
     return fail(TS_ERR_UNSUPPORTED, "%s: one token row of K+V plus the query rows (%u B) exceeds the stage budget",
                 who, prm.stage_bytes);
   prm.num_stages = stages;
   const size_t smem = prm.stages_off + static_cast<size_t>(stages) * prm.stage_bytes;
-  // the prologue's entries: the cache, else the stage area if they fit there
+  // the prologue's entries: in the stage area, if they fit there
   const uint64_t stage_area = static_cast<uint64_t>(stages) * prm.stage_bytes;
   const uint64_t entries = 8ull * static_cast<uint64_t>(Bv);
-  prm.len_scratch_off = cache ? prm.len_cache_off : (entries <= stage_area ? prm.stages_off : 0u);
+  prm.len_scratch_off = entries <= stage_area ? prm.stages_off : 0u;
   // prefix mode: the groups' prefix lengths staged behind the entries
   prm.num_groups = pre ? pre->num_groups : 0;
   {
-    const uint64_t at = cache ? 0ull : align_up(entries, 16);
+    const uint64_t at = align_up(entries, 16);
     prm.plen_scratch_off =
         (pre != nullptr && prm.len_scratch_off != 0 && pre->num_groups > 0 &&
          at + 4ull * static_cast<uint64_t>(pre->num_groups) <= stage_area)

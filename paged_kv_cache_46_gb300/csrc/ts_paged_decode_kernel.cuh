@@ -65,14 +65,10 @@ struct PagedParams {
   // Sliding-window KV group (plain decode only): a sequence attends its last
   // `window` tokens; 0 = the whole context.
   int32_t window = 0;
-  // Byte offset in dynamic shared memory of an int2 [B] cache of each virtual
-  // sequence's (own length, tokens in front of its own pages), filled by the
-  // prologue and read by the cut and the producer instead of global memory;
-  // 0 = no cache (large batches).
-  uint32_t len_cache_off = 0;
-  // Where the prologue keeps the same int2 [B] entries while it cuts the
-  // batch: the cache above, else the stage area (free until the producer's
-  // first copy) when they fit there; 0 = read them from global memory.
+  // Byte offset in dynamic shared memory where the prologue keeps an int2 [B]
+  // array of each virtual sequence's (own length, tokens in front of its own
+  // pages) while it cuts the batch: the stage area, free until the producer's
+  // first copy; 0 = the entries do not fit there (read from global memory).
   uint32_t len_scratch_off = 0;
   // Prefix mode: entries of prefix_len, and where the prologue stages them in
   // the stage area for its gather (0: read from global memory).
@@ -288,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   StageDesc* desc = reinterpret_cast<StageDesc*>(smem + 128);
   long long* warp_tot = reinterpret_cast<long long*>(smem + 512);
   int* s_start = reinterpret_cast<int*>(smem + 640);  // b0, p0
-  int2* s_len = p.len_cache_off != 0 ? reinterpret_cast<int2*>(smem + p.len_cache_off) : nullptr;
   int2* s_pro = p.len_scratch_off != 0 ? reinterpret_cast<int2*>(smem + p.len_scratch_off) : nullptr;
   unsigned char* stages = smem + p.stages_off;
 
@@ -435,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
   }
   // the stage area's scratch entries are read through the generic proxy; the
   // producer's bulk copies (async proxy) overwrite them after this barrier
-  if (gathered || (s_pro != nullptr && s_len == nullptr)) fence_async_smem();
+  if (s_pro != nullptr) fence_async_smem();
   __syncthreads();
 
   if (warp < kFirstConsumerWarp) {
@@ -463,11 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         const int bb = base + lane;
         pre_out = 0;
         if (bb >= B) return -1;
-        if (s_len != nullptr) {  // filled by the prologue, before its barriers
-          const int2 e = s_len[bb];
-          pre_out = e.y;
-          return max(e.x, 0);
-        }
         pre_out = prefix_tokens<kPfx>(p, bb) + window_skip<kWin>(p, bb);
         return max(vseq_len<kPfx, kMulti, kWin>(p, bb), 0);
       };
