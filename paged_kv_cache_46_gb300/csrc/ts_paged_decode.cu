@@ -43,19 +43,36 @@
 namespace ts {
 namespace {
 
-// Reduces the partial states of sequences cut across CTAs (one warp per
-// (sequence, query head)); sequences written whole by the main kernel are
-// skipped.
+// Reduces the partial states of sequences cut across CTAs, one warp per
+// (sequence, query row). Either every row of the batch has a warp (rows of
+// sequences written whole by the main kernel are skipped), or, `compact`,
+// each CTA of the main kernel has ceil(rows / 8) blocks for the one cut
+// sequence whose first part it holds (split_seq): far fewer blocks when the
+// batch has many more sequences than CTAs.
 // In prefix mode a grouped sequence's shared-prefix state is one more part.
 template <typename T, bool kPfx>
-__global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, int D) {
+__global__ void __launch_bounds__(256) split_merge_kernel(const PagedParams p, int D, int compact) {
   pdl_wait_primary();
   pdl_launch_dependents();  // a following PDL-aware kernel may start its prologue
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = warp / p.rows, hq = warp % p.rows;  // virtual sequence, query row
-  if (b >= p.B) return;
-  const int2 info = p.split_info[b];
+  int b, hq;  // virtual sequence, query row
+  int2 info;  // {first CTA, (parts << 1) | slot of first part}
+  if (compact) {
+    const int per_cta = (p.rows + 7) / 8 * 8;  // warps per CTA entry
+    const int k = warp / per_cta;
+    hq = warp % per_cta;
+    if (hq >= p.rows) return;
+    const int2 e = p.split_seq[k];
+    if (e.x < 0) return;
+    b = e.x;
+    info = make_int2(k, e.y);
+  } else {
+    b = warp / p.rows;
+    hq = warp % p.rows;
+    if (b >= p.B) return;
+    info = p.split_info[b];
+  }
   const int nparts = info.y >> 1;
   if (nparts <= 1) return;
   const int k0 = info.x, slot0 = info.y & 1;
@@ -144,7 +161,7 @@ int paged_decode_ctas() {
 }
 
 struct WsLayout {
-  size_t split_info, part_o, part_lse, total;
+  size_t split_info, split_seq, part_o, part_lse, total;
 };
 
 WsLayout workspace_layout(int B, int H_q, int D, int n_ctas) {
@@ -152,6 +169,8 @@ WsLayout workspace_layout(int B, int H_q, int D, int n_ctas) {
   size_t off = kWorkspaceAlign;  // error word + pad
   w.split_info = off;
   off = align_up(off + static_cast<size_t>(B) * sizeof(int2), kWorkspaceAlign);
+  w.split_seq = off;
+  off = align_up(off + static_cast<size_t>(n_ctas) * sizeof(int2), kWorkspaceAlign);
   w.part_o = off;
   off = align_up(off + static_cast<size_t>(2) * n_ctas * H_q * D * sizeof(float), kWorkspaceAlign);
   w.part_lse = off;
@@ -292,6 +311,7 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
     unsigned char* wsb = static_cast<unsigned char*>(workspace);
     prm.err_word = reinterpret_cast<uint32_t*>(wsb);
     prm.split_info = reinterpret_cast<int2*>(wsb + ws.split_info);
+    prm.split_seq = reinterpret_cast<int2*>(wsb + ws.split_seq);
     prm.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
     prm.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   }
@@ -397,8 +417,13 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
   if (st != TS_OK) return st;
 
   const long long warps = static_cast<long long>(Bv) * rows;
+  const long long warps_compact = static_cast<long long>(n_ctas) * ((rows + 7) / 8 * 8);
+  // the per-CTA grid only where it is several times smaller (the cascade
+  // suffix: 16,384 sequences); at a few hundred sequences the plain grid
+  // measured as fast
+  const int compact = warps_compact * 4 <= warps ? 1 : 0;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
+  mcfg.gridDim = dim3(static_cast<unsigned>(((compact ? warps_compact : warps) + 7) / 8));
   mcfg.blockDim = dim3(256);
   mcfg.dynamicSmemBytes = 0;
   mcfg.stream = stream;
@@ -409,10 +434,10 @@ ts_status paged_decode_core(const void* q, const void* k_pool, const void* v_poo
     st = cuda_check(cudaLaunchKernelEx(&mcfg,
                                        pre ? split_merge_kernel<__nv_bfloat16, true>
                                            : split_merge_kernel<__nv_bfloat16, false>,
-                                       prm, D),
+                                       prm, D, compact),
                     "split merge launch");
   else
-    st = cuda_check(cudaLaunchKernelEx(&mcfg, split_merge_kernel<float, false>, prm, D),
+    st = cuda_check(cudaLaunchKernelEx(&mcfg, split_merge_kernel<float, false>, prm, D, compact),
                     "split merge launch");
   return st;
 }

@@ -39,6 +39,9 @@ struct PagedParams {
   float* lse;
   uint32_t* err_word;
   int2* split_info;  // per virtual sequence: {first CTA, (parts << 1) | slot of first part}
+  // per CTA: {the cut sequence whose first part it holds (or -1), its
+  // (parts << 1) | slot of first part} (its first CTA is this one)
+  int2* split_seq;
   float* part_o;     // [2 * gridDim.x, rows, D]
   float* part_lse;   // [2 * gridDim.x, rows]
   // Shared-prefix (cascade) mode: a grouped sequence's own pages start after
@@ -548,9 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
       Chunk cur, nxt;
       int pid = next_chunk(cur);
       pdl_wait_primary();  // the metadata of the first chunk is loaded; copies and writes follow
+      // this CTA's split_seq entry: none, unless a cut sequence starts here
+      if (lane == 0) p.split_seq[k] = make_int2(-1, 0);
       while (cur.cnt > 0 && !aborted) {
         const int pid_nxt = next_chunk(nxt);
         if (cur.split >= 0 && lane == 0) p.split_info[cur.b] = make_int2(k, cur.split);
+        if (cur.split >= 0 && (cur.split >> 1) > 1 && lane == 0) p.split_seq[k] = make_int2(cur.b, cur.split);
         const int np_cur = (cur.L + ps - 1) / ps;
         for (int i = 0; i < cur.cnt; ++i) {
           const int page = __shfl_sync(0xffffffffu, pid, i);
@@ -623,6 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const PagedPa
         cur = nxt;
         pid = pid_nxt;
       }
+    } else if (lane == 0) {
+      pdl_wait_primary();  // before the write
+      p.split_seq[k] = make_int2(-1, 0);  // an empty range holds no cut sequence
     }
     if (lane == 0) {
       if (!aborted) {
