@@ -111,18 +111,19 @@ def test_result_independent_of_split_pattern(ctas):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_many_sequences_few_ctas(dtype):
-    """200 sequences over 7 CTAs: the merge takes its per-CTA grid (each CTA
-    records the one cut sequence it starts) and the prologue gathers the
-    lengths through shared memory; every cut sequence is merged once."""
+    """500 sequences (more than a CTA's 384 threads) over 7 and 3 CTAs: the
+    prologue gathers the lengths through shared memory, and the merge takes
+    its per-CTA grid (each CTA records the one cut sequence it starts); every
+    cut sequence is merged once."""
     rng = np.random.default_rng(61)
-    lens = rng.integers(0, 300, size=200)
+    lens = rng.integers(0, 300, size=500)
     lens[::17] = 0
     case = workloads.build_case(f"many_few_{dtype}", 62, B=len(lens), H_q=32, H_kv=8, D=64, page_size=16,
                                 seq_lens=lens, dtype=dtype, scale=0.125, device=DEV)
     for ctas in (7, 3):
         out, lse, _ = _run_decode(case, ctas=ctas)
         o_ref, l_ref = oracle_decode(case)
-        compare(out, o_ref, dtype, lse, l_ref, f"{dtype} 200 sequences over {ctas} CTAs")
+        compare(out, o_ref, dtype, lse, l_ref, f"{dtype} 500 sequences over {ctas} CTAs")
 
 
 @pytest.mark.parametrize("ctas", [7, None])
