@@ -349,8 +349,14 @@ TS_API ts_status ts_kv_append_fp8(const void* k_new, const void* v_new, void* k_
  * TS_FP8_DECODE_PATH=tensor a tensor-core kernel runs it instead where the
  * shape allows (page 16, 2 or 4 kv heads per CTA): the codes are widened to
  * f16 on chip and the probabilities rounded to f16 for the P V product (the
- * row sum and the LSE stay float32). It is measured slower on the Llama-3-8B
- * layer shape, hence not the default.
+ * row sum and the LSE stay float32). With TS_FP8_DECODE_PATH=mma, at 32
+ * query heads over 8 kv heads, head dim 128 and page 16, a kernel that
+ * multiplies the codes themselves (kind::f8f6f4) runs it: the query and the
+ * probabilities enter as three e4m3 terms each (relative error at most
+ * 2^-12, below bf16's rounding), the scores take the key scales, the
+ * probabilities the value scales and a power-of-two gain; cut sequences are
+ * merged inside the kernel. Both are measured slower than the CUDA-core
+ * kernel on the Llama-3-8B layer shape, hence not the default.
  */
 TS_API ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool, const void* v_pool,
                                           const float* k_scale, const float* v_scale,

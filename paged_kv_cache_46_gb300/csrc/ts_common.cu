@@ -2,6 +2,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -111,6 +112,14 @@ int device_sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
+}
+
+int paged_decode_ctas() {
+  if (const char* env = getenv("TS_PAGED_DECODE_CTAS")) {
+    const int n = atoi(env);
+    if (n > 0 && n <= 65535) return n;
+  }
+  return device_sm_count();
 }
 
 }  // namespace ts

@@ -23,6 +23,10 @@ ts_status cuda_check(cudaError_t e, const char* what);
 ts_status noalloc_scratch_address(void** addr);
 // SM count of the current device (cached per device).
 int device_sm_count();
+// CTAs of a persistent grid over the batch's pages: one per SM.
+// TS_PAGED_DECODE_CTAS overrides it (tests use it to sweep how sequences are
+// cut across CTAs).
+int paged_decode_ctas();
 // Current device ordinal.
 int current_device();
 

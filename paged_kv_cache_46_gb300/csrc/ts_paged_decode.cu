@@ -150,16 +150,6 @@ KernelFn pick_kernel(ts_dtype dt, int D, int g, bool prefix) {
 
 constexpr int kSmemBudget = 227 * 1024;
 
-// CTAs of the persistent grid: one per SM. TS_PAGED_DECODE_CTAS overrides it
-// (tests use it to sweep how sequences are cut across CTAs).
-int paged_decode_ctas() {
-  if (const char* env = getenv("TS_PAGED_DECODE_CTAS")) {
-    const int n = atoi(env);
-    if (n > 0 && n <= 65535) return n;
-  }
-  return device_sm_count();
-}
-
 struct WsLayout {
   size_t split_info, split_seq, part_o, part_lse, total;
 };
@@ -201,6 +191,11 @@ ts_status launch_fp8_decode_tc(const void* q, const void* k_pool, const void* v_
                                const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
                                int32_t page_size, int32_t num_pages, float scale, void* out, float* lse,
                                uint32_t* err_word, cudaStream_t stream);
+ts_status launch_fp8_decode_mma(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+                                const float* v_scale, const int32_t* block_table, int32_t bt_stride,
+                                const int32_t* seq_lens, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                                int32_t page_size, int32_t num_pages, float scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 ts_status launch_multi_query_tc(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                                 int32_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H_q,
                                 int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
@@ -635,9 +630,10 @@ extern "C" ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool,
                                               int32_t H_kv, int32_t D, int32_t page_size,
                                               int32_t num_pages, float scale, void* out, float* lse,
                                               void* workspace, size_t workspace_bytes, void* stream) {
-  // The tensor-core kernel when the shape suits it (one CTA per sequence and
-  // 2 or 4 kv heads; arguments it cannot judge are left to the CUDA-core
-  // path's checks), else the CUDA-core split-KV kernel.
+  // The CUDA-core split-KV kernel, unless TS_FP8_DECODE_PATH asks for one of
+  // the tensor-core kernels (=mma: the code-multiplying one, =tensor: the
+  // widening one) and the shape suits it; arguments the tensor-core kernels
+  // cannot judge are left to the CUDA-core path's checks.
   if (B > 0 && H_q > 0 && H_kv > 0 && q && k_pool && v_pool && k_scale && v_scale && block_table && seq_lens &&
       out && std::isfinite(scale) && reinterpret_cast<uintptr_t>(q) % 16 == 0 &&
       reinterpret_cast<uintptr_t>(out) % 16 == 0 && reinterpret_cast<uintptr_t>(k_pool) % 16 == 0 &&
@@ -648,10 +644,13 @@ extern "C" ts_status ts_paged_decode_fp8_attn(const void* q, const void* k_pool,
         reinterpret_cast<uintptr_t>(workspace) % ts::kWorkspaceAlign != 0)
       return ts::fail(TS_ERR_WORKSPACE, "ts_paged_decode_fp8_attn: workspace %zu B < %zu B needed or misaligned",
                       workspace_bytes, need);
-    const ts_status st = ts::launch_fp8_decode_tc(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,
-                                                  seq_lens, B, H_q, H_kv, D, page_size, num_pages, scale, out, lse,
-                                                  static_cast<uint32_t*>(workspace),
-                                                  static_cast<cudaStream_t>(stream));
+    ts_status st = ts::launch_fp8_decode_mma(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,
+                                             seq_lens, B, H_q, H_kv, D, page_size, num_pages, scale, out, lse,
+                                             workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+    if (st != TS_ERR_UNSUPPORTED) return st;
+    st = ts::launch_fp8_decode_tc(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride, seq_lens, B, H_q,
+                                  H_kv, D, page_size, num_pages, scale, out, lse, static_cast<uint32_t*>(workspace),
+                                  static_cast<cudaStream_t>(stream));
     if (st != TS_ERR_UNSUPPORTED) return st;
   }
   return ts::launch_paged_decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, bt_stride,

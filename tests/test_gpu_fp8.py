@@ -161,3 +161,110 @@ def test_decode_fp8_paths_agree_on_the_llama_shape():
     o_ref, l_ref = _oracle(case, view)
     dev_idx = torch.from_numpy(idx).to(DEV)
     compare(o_tc[dev_idx], o_ref, "bf16", l_tc[dev_idx], l_ref, "llama fp8 tensor core sample")
+
+
+@pytest.mark.parametrize("ctas", [None, 1, 3, 7, 64, 1000])
+def test_decode_fp8_code_mma_kernel(ctas):
+    """The kernel that multiplies the codes on the tensor cores
+    (TS_FP8_DECODE_PATH=mma; 32/8 heads, head dim 128, page 16) against the oracle: empty
+    sequences, one key, a page minus one, one page, a page plus one, long
+    contexts. The CTA count sweeps the cut: one CTA holds every page,
+    sequences cut across several CTAs (merged by the last to arrive), more
+    CTAs than pages. The launch trace shows the kernel ran."""
+    lens = [0, 1, 15, 16, 17, 700, 2049, 64, 5000, 0, 333]
+    case = workloads.build_fp8_case("fp8_mma", 89, B=len(lens), H_q=32, H_kv=8, D=128, page_size=16,
+                                    seq_lens=lens, scale=128 ** -0.5, device=DEV)
+    o_ref, l_ref = _oracle(case)
+    out, lse = _decode(case, ctas, path="mma", expect_kernel="fp8_mma_kernel")
+    compare(out, o_ref, "bf16", lse, l_ref, f"fp8 code products ctas={ctas}")
+
+
+def test_decode_fp8_code_mma_bad_page_is_flagged_without_fault():
+    """A page id past the pool: the error word reports it, the page reads as
+    zeros (no out-of-range access), every output stays finite and the other
+    sequences are unaffected."""
+    lens = [40, 300, 33, 900]
+    case = workloads.build_fp8_case("fp8_mma_bad", 90, B=len(lens), H_q=32, H_kv=8, D=128, page_size=16,
+                                    seq_lens=lens, scale=128 ** -0.5, device=DEV)
+    case.block_table = case.block_table.copy()
+    case.block_table[1, 3] = case.num_pages + 5
+    bt, dlens, _ = _meta(case)
+    ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D))
+    os.environ["TS_FP8_DECODE_PATH"] = "mma"
+    try:
+        out, lse = ts.ts_paged_decode_fp8_attn(case.q, case.k_pool, case.v_pool, case.k_scale, case.v_scale, bt,
+                                               dlens, case.scale, workspace=ws, return_lse=True)
+        torch.cuda.synchronize()
+    finally:
+        os.environ.pop("TS_FP8_DECODE_PATH", None)
+    assert ts.ts_read_device_error(ws) & ts.TS_DEVERR_PAGE_RANGE
+    assert torch.isfinite(out.float()).all()
+    good = np.array([0, 2, 3])
+    view = workloads.oracle_view(case, good)
+    o_ref, l_ref = _oracle(case, view)
+    sel = torch.from_numpy(good).to(DEV)
+    compare(out[sel], o_ref, "bf16", lse[sel], l_ref, "fp8 code products, bad page neighbours")
+
+
+def test_decode_fp8_code_mma_repeats_bit_for_bit_and_replays_from_a_graph():
+    """Launches on one workspace without clearing it, and replays of a captured
+    CUDA graph (the same launch epoch every time: the counters of the cut
+    sequences must return to zero), all give the same bits, and those match
+    the oracle. 40 CTAs cut most sequences."""
+    rng = np.random.default_rng(91)
+    lens = rng.integers(1, 3000, size=24)
+    case = workloads.build_fp8_case("fp8_mma_rep", 91, B=len(lens), H_q=32, H_kv=8, D=128, page_size=16,
+                                    seq_lens=lens, scale=128 ** -0.5, device=DEV)
+    bt, dlens, _ = _meta(case)
+    os.environ["TS_PAGED_DECODE_CTAS"] = "40"
+    os.environ["TS_FP8_DECODE_PATH"] = "mma"
+    try:
+        ws = ts.new_workspace(ts.ts_paged_decode_workspace_size(case.B, case.H_q, case.D))
+        out = torch.empty_like(case.q)
+        lse = torch.empty(case.B, case.H_q, dtype=torch.float32, device=DEV)
+        stream = torch.cuda.Stream()
+
+        def call():
+            ts.ts_paged_decode_fp8_attn(case.q, case.k_pool, case.v_pool, case.k_scale, case.v_scale, bt, dlens,
+                                        case.scale, out=out, lse=lse, workspace=ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        first = (out.clone(), lse.clone())
+        for _ in range(2):
+            with torch.cuda.stream(stream):
+                call()
+            torch.cuda.synchronize()
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1])
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        for _ in range(3):
+            out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1])
+        assert ts.ts_read_device_error(ws) == 0
+    finally:
+        os.environ.pop("TS_PAGED_DECODE_CTAS", None)
+        os.environ.pop("TS_FP8_DECODE_PATH", None)
+    o_ref, l_ref = _oracle(case)
+    compare(first[0], o_ref, "bf16", first[1], l_ref, "fp8 code products, repeated")
+
+
+def test_decode_fp8_code_mma_on_the_llama_shape():
+    """The Llama-3-8B layer workload over an fp8 cache (B = 64, lengths
+    U[512, 4096]) in the benchmark's launch configuration: the code-multiplying
+    kernel against the CUDA-core kernel on every output, and against the
+    oracle on a sample of 16 sequences."""
+    case = workloads.llama3_8b_layer_fp8(device=DEV, append=False)
+    o_mm, l_mm = _decode(case, path="mma", expect_kernel="fp8_mma_kernel")
+    o_cc, l_cc = _decode(case, path="cuda", expect_kernel="paged_decode_kernel")
+    assert (o_mm.float() - o_cc.float()).abs().max().item() <= 2e-2
+    assert (l_mm - l_cc).abs().max().item() <= 2e-4
+    idx = workloads.sample_sequences(case, 16)
+    view = workloads.oracle_view(case, idx)
+    o_ref, l_ref = _oracle(case, view)
+    dev_idx = torch.from_numpy(idx).to(DEV)
+    compare(o_mm[dev_idx], o_ref, "bf16", l_mm[dev_idx], l_ref, "llama fp8 code products sample")
