@@ -118,3 +118,36 @@ def test_mutation_truncating_encoder_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "e4m3_encode", truncating)
     with pytest.raises(AssertionError):
         test_encoder_matches_torch_cast()
+
+
+def _three_terms(x):
+    """The three-term e4m3 split of float32 values (hi, then the rounding of
+    what hi leaves, then of what both leave), with the oracle's codec; the
+    differences are exact (Sterbenz), so float64 reproduces float32."""
+    hi = of8.e4m3_decode(of8.e4m3_encode(x))
+    r1 = x - hi
+    mid = of8.e4m3_decode(of8.e4m3_encode(r1))
+    r2 = r1 - mid
+    lo = of8.e4m3_decode(of8.e4m3_encode(r2))
+    return hi, mid, lo
+
+
+def test_three_term_e4m3_split_precision():
+    """The precision reading of the code-multiplying fp8 kernel: a query
+    element (scaled to at most 2^8) or a weighted probability (at most
+    2^8.5) split into three e4m3 terms is reconstructed within
+    max(2^-12 |x|, 2^-10) (each rounding halves a 3-bit mantissa's spacing;
+    below 2^-6 the subnormal grid's 2^-9 spacing sets the floor). Two terms
+    would not meet it: the bound is tight enough to catch a dropped term."""
+    rng = np.random.default_rng(7)
+    mag = np.exp2(rng.uniform(-14.0, 8.5, 400000))
+    x = (mag * np.where(rng.random(mag.size) < 0.5, -1.0, 1.0)).astype(np.float32).astype(np.float64)
+    x = np.concatenate([x, [256.0, 255.9, 2.0 ** 8.5, 2.0 ** -6, 2.0 ** -9, 3 * 2.0 ** -10, 1.0 + 2.0 ** -11,
+                            0.0, 1e-7]])
+    hi, mid, lo = _three_terms(x)
+    err3 = np.abs(x - (hi + mid + lo))
+    bound = np.maximum(2.0 ** -12 * np.abs(x), 2.0 ** -10)
+    assert np.all(err3 <= bound * (1 + 1e-9)), float(np.max(err3 / bound))
+    err2 = np.abs(x - (hi + mid))
+    big = np.abs(x) >= 4.0  # where the relative bound, not the subnormal floor, applies
+    assert np.mean(err2[big] > bound[big]) > 0.5  # a split that stops at two terms fails it
