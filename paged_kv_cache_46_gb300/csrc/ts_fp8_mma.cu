@@ -11,8 +11,9 @@
 //   (N = 128), landing head by head as 128-byte rows (128-byte swizzle).
 // - The 128 rows (TMEM lanes) are the 32 query heads, four lanes each: the
 //   head's query split into three e4m3 terms (hi, then the rounding of what
-//   hi leaves, then of what both leave: at most 2^-12 relative error, below
-//   bf16's own rounding) and a zero lane. The query is first scaled by a
+//   hi leaves, then of what both leave: within max(2^-12 |x|, 2^-10) of the
+//   scaled value, below bf16's own rounding for the elements that carry the
+//   score) and a zero lane. The query is first scaled by a
 //   power of two that brings its largest element to [2^7, 2^8).
 //   S = Q K^T takes the terms from TMEM and the key codes from shared
 //   memory; a lane sums its head's three partial scores with two shuffles.
