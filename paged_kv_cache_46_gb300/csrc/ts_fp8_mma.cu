@@ -253,8 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_mma_kernel(const MmaParams p,
   };
   // the CTA whose range holds global page x
   auto owner = [&](int x) { return static_cast<int>((static_cast<long long>(x + 1) * n - 1) / total); };
-  // tile j begins a segment (one sequence's pages within this CTA's range)
-  auto starts = [&](int j) { return j == 0 || pre[seq_of(lo + j)] == lo + j; };
 
   bool ok = true;
   if (warp == 4) {
