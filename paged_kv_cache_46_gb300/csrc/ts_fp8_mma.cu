@@ -16,7 +16,8 @@
 //   score) and a zero lane. The query is first scaled by a
 //   power of two that brings its largest element to [2^7, 2^8).
 //   S = Q K^T takes the terms from TMEM and the key codes from shared
-//   memory; a lane sums its head's three partial scores with two shuffles.
+//   memory. The head's four lanes split the tile's 16 keys of its kv head:
+//   a reduce-scatter sums the three partial scores, four keys per lane.
 // - Scores take the key row's scale. P follows the same three-term split,
 //   of p x the value row's scale x a power-of-two gain that brings the
 //   tile's largest value scale to [2^7, 2^8); with the running maximum
@@ -132,9 +133,8 @@ __device__ __forceinline__ void e4m3_terms(float a, float b, uint32_t& hi, uint3
   lo = to_e4m3x2(ra - md.x, rb - md.y);
 }
 
-// Word x of lane k's term after an exchange among a head's four lanes: each
-// lane holds all three terms (and a zero fourth) of its own share `tw`, and
-// lane k collects its term `k` of every lane's share (x: the share's lane).
+// t[i] for a run-time i in 0 .. 3, by selects (indexing a register array at
+// run time would move it to local memory).
 __device__ __forceinline__ uint32_t pick4(const uint32_t (&t)[4], int i) {
   return i == 0 ? t[0] : (i == 1 ? t[1] : (i == 2 ? t[2] : t[3]));
 }
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_mma_kernel(const MmaParams p,
       pdl_wait_primary();
       const int oob = p.num_pages * kPS;  // a row past the pool: the box is zero-filled
       for (int j0 = 0; j0 < n_tiles && ok; j0 += 32) {
-        int row = oob, sp = 0;
+        int row = oob, sp = 0;  // a bad page id: zero codes, and page 0's scales (a valid address)
         if (j0 + lane < n_tiles) {
           const int x = lo + j0 + lane, b = seq_of(x);
           const int page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + (x - pre[b])];
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_mma_kernel(const MmaParams p,
       const int e = amax >= 1.17549435e-38f ? min(126, max(-126, 7 - ilog2f(amax))) : 0;
       const float up = pow2i(e);
       if (term == 0) qscale[u * kHq + h] = p.scale_log2 * pow2i(-e);
-      // tw[v][t]: term t of elements 32 term + 8v .. + 3 (first word) and + 4 .. + 7 (second)
+      // tw[i][t]: term t of this lane's elements 32 term + 4 i .. + 3 (t = 3: zero)
       uint32_t tw[8][4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
